@@ -1,0 +1,457 @@
+"""Benchmark of the fused MoE-FFN layer (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qwen] [--impl reference]
+
+A step is one forward + backward of the layer over one batch of the workload (default: the
+Qwen-like layer T=16384, H=2048, I=768, E=128, K=8, uniform top-8 routing), inputs resident in
+device memory. Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the layer on its own GPU ("replicas only": the path has no exchange
+step on one GPU per layer instance); `value` is the tokens of all ranks / the slowest rank's time.
+
+`--impl reference` times the float64 CPU oracle instead (the reference arm), on a bounded
+sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-FFN fwd+bwd tokens/s and TFLOPS (% of GB300 BF16 dense peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# algorithmic FLOPs per slot of each GEMM stage (routed work only, no padding)
+GEMM_FLOPS_PER_SLOT = {"gemm1_swiglu": 4, "gemm2": 2, "act_grad": 2, "w2_grad": 2,
+                       "input_grad": 4, "w1_grad": 4}  # x H*I
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest():
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "moe_ffn_expert_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(stage, workload):
+    """DRAM bytes per launch from a committed ncu summary, valid only for the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{workload}/{stage}")
+    if not e or e.get("source") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_ms: float, units: float, device=None):
+    """Max of the elapsed time and sum of the processed units over all ranks (identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_ms, units
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[0] != self.uuid and not self.uuid.endswith(parts[0][4:]):
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[2]) for r in rows]
+            smax = max(float(r[3]) for r in rows)
+            power = [float(r[4]) for r in rows if r[4] not in ("[N/A]", "N/A")]
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+               "samples": len(rows)}
+        if power:
+            out["power_w_max"] = max(power)
+        return out
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from moe_ffn_expert_gb300 import _abi
+    from moe_ffn_expert_gb300 import build as mm_build
+    from workloads import synth
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the layer has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        mm_build.build()  # no-op when libmm.so is newer than its sources
+    barrier(dev)
+
+    w = synth.BY_NAME[args.workload]
+    T, H, I, E, K = w.T, w.H, w.I, w.E, w.K
+    S = T * K
+    d = _abi.dims(T, H, I, E, K)
+    nbytes = _abi.mm_workspace_size(d)
+    stream = torch.cuda.current_stream(dev)
+    st = stream.cuda_stream
+
+    ids = synth.routing(w).to(dev)
+    tw = synth.topk_weights(w).to(dev)
+    x = synth.x(w, device=dev)
+    dy = synth.dy(w, device=dev)
+    wu = synth.w_up(w, device=dev)
+    wd = synth.w_down(w, device=dev)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    dtk = torch.empty(T, K, dtype=torch.float32, device=dev)
+    du = torch.empty_like(wu)
+    dd = torch.empty_like(wd)
+
+    def fwd():
+        _abi.check(_abi.mm_forward(d, x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
+                                   wd.data_ptr(), y.data_ptr(), ws.data_ptr(), nbytes, st, 0), "fwd")
+
+    def bwd():
+        _abi.check(_abi.mm_backward(d, dy.data_ptr(), x.data_ptr(), ids.data_ptr(), tw.data_ptr(),
+                                    wu.data_ptr(), wd.data_ptr(), ws.data_ptr(), nbytes,
+                                    dx.data_ptr(), dtk.data_ptr(), du.data_ptr(), dd.data_ptr(),
+                                    st, 0), "bwd")
+
+    def step():
+        fwd()
+        bwd()
+
+    def timed(fn, n):
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        return a.elapsed_time(b)
+
+    first_ms = timed(step, 1)  # first call: attribute setup, descriptor fetch, cold caches
+    status = _abi.mm_get_status(ws.data_ptr(), st)
+    if status != _abi.MM_OK:
+        raise SystemExit(f"device status after first step: {_abi.mm_status_string(status)}")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- main timed region: K steps, per-stage CUDA events on the library's stream
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid).start()
+    _abi.mm_timing_read()
+    _abi.mm_timing_enable(True)
+    elapsed = timed(step, args.steps)
+    _abi.mm_timing_enable(False)
+    stages = _abi.mm_timing_read()
+    clocks = sampler.stop()
+    if _abi.mm_get_status(ws.data_ptr(), st) != _abi.MM_OK:
+        raise SystemExit("device status error in the timed region")
+    elapsed_max, tokens_all = aggregate(elapsed, float(T * args.steps), dev)
+    ms_per_step = elapsed_max / args.steps
+    value = tokens_all / (elapsed_max / 1e3)
+
+    # ---- forward alone and backward alone (short extra passes)
+    n_part = max(3, min(args.steps, 10))
+    fwd_ms = timed(fwd, n_part) / n_part
+    fwd()
+    bwd_ms = timed(bwd, n_part) / n_part
+
+    # ---- end to end: host buffers in, results out, copies inside the timed region
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
+    hx, hids, htw, hdy = pin(x), pin(ids), pin(tw), pin(dy)
+    hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    hdx = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+    hdt = torch.empty(dtk.shape, dtype=dtk.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, htw, hdy))
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hdt))
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        ids.copy_(hids, non_blocking=True)
+        tw.copy_(htw, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdt.copy_(dtk, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    n_e2e = max(3, min(args.steps, 10))
+    e2e_ms = timed(e2e_step, n_e2e)
+    e2e_max, e2e_tokens = aggregate(e2e_ms, float(T * n_e2e), dev)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    peaks, peak_src = load_peaks()
+    hi = H * I
+    flops = w.flops()
+    total_flops_step = flops["total"]
+    tflops = total_flops_step * args.steps * world / (elapsed_max / 1e3) / 1e12
+    peak_burst = peaks["bf16_tflops"]
+    peak_sus = peaks.get("bf16_tflops_sustained", peak_burst)
+
+    stage_ms = {k: v[0] / max(1, args.steps) for k, v in stages.items()}
+    launches = int(sum(v[1] for v in stages.values()))
+    gemm_stages = {k: v for k, v in stages.items() if k in GEMM_FLOPS_PER_SLOT and v[1] > 0}
+    top = max(gemm_stages, key=lambda k: gemm_stages[k][0])
+    top_ms, top_n = gemm_stages[top]
+    avg_ms = top_ms / top_n
+    top_flops = GEMM_FLOPS_PER_SLOT[top] * hi * S
+    achieved = top_flops / (avg_ms / 1e3) / 1e12
+
+    # CPU baseline: the oracle on a bounded sample of this workload
+    cpu = cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded counter-based generator; inputs larger than L2 (no flush)",
+        "config": {"workload": f"{w.name} T={T} H={H} I={I} E={E} K={K}", "T": T, "H": H, "I": I,
+                   "E": E, "K": K, "routing": w.routing, "seed": w.seed,
+                   "l2": "inputs larger than L2: 1.2 GB of expert weights and 0.6 GB of slot rows per step",
+                   "parallelism": "single GPU" if world == 1 else f"{world} independent replicas"},
+        "tflops": round(tflops, 2),
+        "frac_of_bf16_peak": {"burst": round(tflops / peak_burst, 4),
+                              "sustained": round(tflops / peak_sus, 4), "peaks": peak_src},
+        "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(T / (fwd_ms / 1e3), 1),
+                "tflops": round(flops["fwd"] / (fwd_ms / 1e3) / 1e12, 2)},
+        "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(T / (bwd_ms / 1e3), 1),
+                "tflops": round(flops["bwd"] / (bwd_ms / 1e3) / 1e12, 2)},
+        "first_call_ms": round(first_ms, 3),
+        "stages_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+        "roofline": {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
+                     "peak_kind": f"bf16 sustained ({peak_src})",
+                     "traffic": profiled_traffic(top, w.name)},
+        "gpu_launches": launches,
+        "e2e": {"value": round(e2e_tokens / (e2e_max / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "x, topk_ids, topk_weights, dy copied in from pinned host memory and y, dx, "
+                        "d_topk_weights copied out every step; expert weights and their gradients "
+                        "stay resident"},
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def _oracle_tokens(w, n, inputs):
+    """fwd+bwd of the float64 oracle over the first n tokens of the workload; returns seconds."""
+    import oracle
+    x, ids, tw, dy, wu, wd = inputs
+    t0 = time.perf_counter()
+    oracle.backward(x[:n], ids[:n], tw[:n], wu, wd, dy[:n])  # includes the forward recompute
+    oracle.forward(x[:n], ids[:n], tw[:n], wu, wd)
+    return time.perf_counter() - t0
+
+
+def _oracle_inputs(w, n_max, device_weights=None):
+    """Host copies of the first n_max tokens' inputs and of the expert weights they use
+    (drawn on the host, or copied from the benchmark's device tensors when given)."""
+    import torch
+
+    from workloads import synth
+    ids = synth.routing(w)[:n_max]
+    tw = synth.topk_weights(w)[:n_max]
+    x = synth.x(w, rows=range(n_max))
+    dy = synth.dy(w, rows=range(n_max))
+    if device_weights is not None:
+        wu, wd = (t.cpu() for t in device_weights)
+    else:
+        wu = synth.LazyExperts(w, "up")
+        wd = synth.LazyExperts(w, "down")
+        for e in torch.unique(ids).tolist():  # draw them before any timing starts
+            wu[e], wd[e]
+    return x, ids, tw, dy, wu, wd
+
+
+def cpu_baseline(w, budget_s=15.0, device_weights=None):
+    import torch
+    torch.set_num_threads(os.cpu_count() or 1)
+    n0 = min(w.T, 32)
+    inp = _oracle_inputs(w, min(w.T, 4096), device_weights)
+    t0 = _oracle_tokens(w, n0, inp)
+    n = int(max(n0, min(inp[0].shape[0], n0 * budget_s / max(t0, 1e-3))))
+    t = _oracle_tokens(w, n, inp) if n != n0 else t0
+    return {"value": round(n / t, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"float64 oracle fwd+bwd of the first {n} tokens of {w.name} "
+                      f"(all experts they route to), {t:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    from workloads import synth
+    torch.set_num_threads(os.cpu_count() or 1)
+    w = synth.BY_NAME[args.workload]
+    inp = _oracle_inputs(w, min(w.T, 2048))
+    n0 = min(w.T, 16)
+    t0 = _oracle_tokens(w, n0, inp)
+    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    n = int(max(1, min(inp[0].shape[0], n0 * per_step_budget / max(t0, 1e-3))))
+    for _ in range(args.warmup):
+        _oracle_tokens(w, n, inp)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _oracle_tokens(w, n, inp)
+    value = n * args.steps / total
+    sample = (f"float64 oracle fwd+bwd of the first {n} tokens of {w.name} per step "
+              f"(all experts they route to)")
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded counter-based generator",
+        "config": {"workload": f"{w.name} T={w.T} H={w.H} I={w.I} E={w.E} K={w.K}", "T": w.T,
+                   "H": w.H, "I": w.I, "E": w.E, "K": w.K, "routing": w.routing, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                         "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample (0: skip)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

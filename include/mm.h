@@ -1,0 +1,133 @@
+/*
+ * mm.h -- C ABI of the fused MoE-FFN layer (forward and backward) for one GB300 GPU.
+ *
+ * The operation is the one defined by the RFC "HyperParallel Multicore HyperMegaMoE fused
+ * forward/backward operator": §2.1 (forward chain Dispatch -> GMM1/up_proj -> SwiGLU ->
+ * GMM2/down_proj -> Combine), §2.2 (backward graph and its gradient list), §2.3 and §10
+ * (the two-phase "query workspace size, then execute" split of the ACLNN interface), §3.1
+ * (the five public tensors) and §4 (routing semantics and boundary checks). On one GPU the
+ * AllToAll dispatch/combine become a permute/unpermute of rows inside device memory.
+ *
+ * Shapes and layouts (all row-major, contiguous, device memory unless stated):
+ *   T tokens, H hidden size, I intermediate size, E experts, K experts per token.
+ *   x                 bf16 [T, H]
+ *   topk_ids          int32 [T, K]   expert id of slot s = t*K + k, in [0, E)
+ *   topk_weights      fp32 [T, K]    routing weight of each slot
+ *   up_proj_weight    bf16 [E, H, 2I] gate in columns [0, I), up in [I, 2I)
+ *                                     (layout from the multicore usage guide, "inputs and weights")
+ *   down_proj_weight  bf16 [E, I, H]
+ *   y, dy, dx         bf16 [T, H]
+ *   d_topk_weights    fp32 [T, K]
+ *   d_up_proj_weight  bf16 [E, H, 2I];  d_down_proj_weight bf16 [E, I, H]
+ *
+ * Math: h_s = silu(x_t W_gate[e]) * (x_t W_up[e]) with silu(z) = z*sigmoid(z),
+ * o_s = h_s W_down[e], y_t = sum_k topk_weights[t,k] * o_{t*K+k} (k ascending, fp32, rounded
+ * once to bf16). Products run on bf16 tensor cores with fp32 accumulation.
+ *
+ * Ownership: the caller allocates every buffer, including the workspace. The library allocates
+ * no device memory. All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and nothing synchronises with the host, except mm_get_status, mm_routing_export
+ * (host destination) and mm_forward with MM_FLAG_VALIDATE_IDS. The calls are not thread-safe
+ * with respect to one another (the optional stage timer is process-global).
+ *
+ * Errors: host-side checks (null or misaligned pointers, sizes out of range, workspace too
+ * small) return an error before anything is enqueued. An expert id outside [0, E) can only be
+ * seen on the device: the first routing kernel records MM_ERR_BAD_EXPERT_ID in the workspace's
+ * status word, every later kernel of the call sees it and does nothing (no out-of-bounds
+ * access), and mm_get_status reports it. Outputs are then unspecified. Device waits are bounded;
+ * a wait that runs out records MM_ERR_TIMEOUT the same way.
+ */
+#ifndef MM_H_
+#define MM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mm_status {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size */
+  MM_ERR_UNSUPPORTED = 2,   /* sizes this build does not handle (see mm_forward) */
+  MM_ERR_WORKSPACE = 3,     /* workspace null, misaligned or smaller than mm_workspace_size */
+  MM_ERR_CUDA = 4,          /* a CUDA runtime call failed (no device, launch error, ...) */
+  MM_ERR_BAD_EXPERT_ID = 5, /* some topk_ids entry is outside [0, E) (found on the device) */
+  MM_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out */
+} mm_status;
+
+/* Layer sizes. Supported: T >= 1, H and I multiples of 8 (16-byte rows), 1 <= E <= 1024,
+ * 1 <= K <= 16, T*K + E*127 < 2^31. */
+typedef struct mm_dims {
+  int64_t T, H, I, E, K;
+} mm_dims;
+
+/* mm_forward flag: run the id check first and wait for it on the host (one device-to-host
+ * read), returning MM_ERR_BAD_EXPERT_ID before any other kernel is enqueued. */
+#define MM_FLAG_VALIDATE_IDS 0x1u
+
+/* Bytes of workspace mm_forward/mm_backward need for `d` (RFC §2.3 workspace query).
+ * Returns 0 if `d` is unsupported. The workspace holds the routing tables, the dispatched
+ * rows x_slot and the saved gate|up activations (kept from mm_forward for mm_backward),
+ * and the scratch of both calls. Its contents need no initialisation. */
+size_t mm_workspace_size(mm_dims d, uint32_t flags);
+
+/* Forward pass (RFC §2.1): routing (per-expert histogram, prefix offsets, stable permute of
+ * the T*K slots), dispatch, GMM1 + SwiGLU, GMM2, weighted combine into y.
+ * `workspace` (>= mm_workspace_size bytes, 256-byte aligned) must not be touched by
+ * anything else until the matching mm_backward has been enqueued; two forwards whose
+ * backwards are still pending need two workspaces. All tensor pointers 16-byte aligned. */
+mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
+                     const float* topk_weights, const void* up_proj_weight,
+                     const void* down_proj_weight, void* y, void* workspace,
+                     size_t workspace_bytes, void* stream, uint32_t flags);
+
+/* Backward pass (RFC §2.2) for the forward that last used `workspace`, with upstream
+ * gradient dy. Writes (overwrites, never accumulates):
+ *   dx                 = sum over k of the input_grad rows of the token's slots,
+ *   d_topk_weights[t,k] = <dy[t], o_{t*K+k}>,
+ *   d_up_proj_weight[e]  = x_slot_e^T [d_gate | d_up]   (zero for an expert with no slot),
+ *   d_down_proj_weight[e] = (w * h)_e^T dy_slot_e        (zero for an expert with no slot).
+ * x, topk_ids, topk_weights and the two weights must be the forward's (the dispatched x rows
+ * and the routing are read back from the workspace; x itself is only checked). */
+mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
+                      const float* topk_weights, const void* up_proj_weight,
+                      const void* down_proj_weight, void* workspace, size_t workspace_bytes,
+                      void* dx, float* d_topk_weights, void* d_up_proj_weight,
+                      void* d_down_proj_weight, void* stream, uint32_t flags);
+
+/* Synchronises `stream`, then returns the device-side status word of `workspace`
+ * (MM_OK, MM_ERR_BAD_EXPERT_ID or MM_ERR_TIMEOUT), or MM_ERR_CUDA if the stream failed.
+ * The word is cleared at the start of every mm_forward. */
+mm_status mm_get_status(const void* workspace, void* stream);
+
+/* Copies the routing tables of the last mm_forward on `workspace` into caller buffers
+ * (device or host memory; the call synchronises `stream` when any destination is host):
+ *   counts[E]        slots per expert,
+ *   offsets[E+1]     exclusive prefix sum of counts (offsets[E] = T*K),
+ *   row_of_slot[T*K] position of slot s in the expert-sorted order, stable in s.
+ * Any destination may be NULL. */
+mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts,
+                            int32_t* offsets, int32_t* row_of_slot, void* stream);
+
+/* Human-readable name of a status code. */
+const char* mm_status_string(mm_status s);
+
+/* ABI version of this library (bumped on any signature change). */
+int mm_abi_version(void);
+
+/* Optional per-stage timer. When enabled, every kernel the library enqueues is bracketed by
+ * CUDA events on its stream. mm_timing_read synchronises those events, writes for each stage
+ * (up to max_stages) the summed milliseconds and the number of launches since the last read,
+ * clears them, and returns the number of stages (MM_NUM_STAGES). mm_stage_name names a stage. */
+#define MM_NUM_STAGES 14
+mm_status mm_timing_enable(int on);
+int mm_timing_read(double* ms, int64_t* launches, int max_stages);
+const char* mm_stage_name(int stage);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_H_ */

@@ -1,0 +1,134 @@
+"""ctypes binding of the C ABI declared in include/mm.h (libmm.so, built in-tree).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+Pointers are plain integers (device addresses, or host addresses where the header allows),
+`stream` is a cudaStream_t as an integer (0 = legacy default stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmm.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "mm.h")
+
+MM_OK = 0
+MM_ERR_INVALID_ARG = 1
+MM_ERR_UNSUPPORTED = 2
+MM_ERR_WORKSPACE = 3
+MM_ERR_CUDA = 4
+MM_ERR_BAD_EXPERT_ID = 5
+MM_ERR_TIMEOUT = 6
+MM_FLAG_VALIDATE_IDS = 0x1
+MM_NUM_STAGES = 14
+
+STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",
+                4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT"}
+
+
+class MMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({_lib().mm_status_string(status).decode()})")
+
+
+class mm_dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
+                ("E", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} is missing "
+                          "(run `python -m moe_ffn_expert_gb300.build`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    st = ctypes.c_int
+    sig = {
+        "mm_workspace_size": (ctypes.c_size_t, [mm_dims, ctypes.c_uint32]),
+        "mm_forward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_uint32]),
+        "mm_backward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P,
+                             _P, ctypes.c_uint32]),
+        "mm_get_status": (st, [_P, _P]),
+        "mm_routing_export": (st, [mm_dims, _P, _P, _P, _P, _P]),
+        "mm_status_string": (ctypes.c_char_p, [st]),
+        "mm_abi_version": (ctypes.c_int, []),
+        "mm_timing_enable": (st, [ctypes.c_int]),
+        "mm_timing_read": (ctypes.c_int, [_P, _P, ctypes.c_int]),
+        "mm_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def header_symbols() -> list[str]:
+    """Function names declared in include/mm.h."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(mm_\w+)\s*\(", text, re.M)))
+
+
+def dims(T, H, I, E, K) -> mm_dims:
+    return mm_dims(int(T), int(H), int(I), int(E), int(K))
+
+
+def mm_workspace_size(d: mm_dims, flags: int = 0) -> int:
+    return int(_lib().mm_workspace_size(d, flags))
+
+
+def mm_forward(d, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y, workspace,
+               workspace_bytes, stream=0, flags=0) -> int:
+    return int(_lib().mm_forward(d, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+                                 workspace, workspace_bytes, stream, flags))
+
+
+def mm_backward(d, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, workspace,
+                workspace_bytes, dx, d_topk_weights, d_up_proj_weight, d_down_proj_weight,
+                stream=0, flags=0) -> int:
+    return int(_lib().mm_backward(d, dy, x, topk_ids, topk_weights, up_proj_weight,
+                                  down_proj_weight, workspace, workspace_bytes, dx, d_topk_weights,
+                                  d_up_proj_weight, d_down_proj_weight, stream, flags))
+
+
+def mm_get_status(workspace, stream=0) -> int:
+    return int(_lib().mm_get_status(workspace, stream))
+
+
+def mm_routing_export(d, workspace, counts, offsets, row_of_slot, stream=0) -> int:
+    return int(_lib().mm_routing_export(d, workspace, counts, offsets, row_of_slot, stream))
+
+
+def mm_status_string(status: int) -> str:
+    return _lib().mm_status_string(status).decode()
+
+
+def mm_abi_version() -> int:
+    return int(_lib().mm_abi_version())
+
+
+def mm_timing_enable(on: bool) -> int:
+    return int(_lib().mm_timing_enable(1 if on else 0))
+
+
+def mm_timing_read() -> dict:
+    """{stage name: (milliseconds, launches)} since the last read."""
+    ms = (ctypes.c_double * MM_NUM_STAGES)()
+    cnt = (ctypes.c_int64 * MM_NUM_STAGES)()
+    n = _lib().mm_timing_read(ctypes.cast(ms, _P), ctypes.cast(cnt, _P), MM_NUM_STAGES)
+    return {_lib().mm_stage_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
+
+
+def check(status: int, where: str):
+    if status != MM_OK:
+        raise MMError(status, where)

@@ -1,0 +1,305 @@
+// C ABI of the fused MoE-FFN layer: argument checks, workspace carve-up, kernel sequence.
+//
+// Forward (RFC "HyperParallel Multicore HyperMegaMoE fused forward/backward operator", §2.1):
+//   status clear -> route count -> route scan -> route rank -> gather x rows ->
+//   GEMM1 + SwiGLU -> GEMM2 -> weighted combine into y.
+// Backward (§2.2): gather dy rows -> act_grad + SwiGLU backward -> d_topk_weights ->
+//   W2Grad -> input_grad -> combine dx -> W1Grad.
+// The host never waits on the device here (except the optional id pre-check); the caller's
+// stream orders everything. The two-phase size query / execute split mirrors §2.3.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "mm_kernels.h"
+#include "mm_layout.h"
+
+namespace mm {
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool dims_ok(const mm_dims& d) {
+  if (d.T < 1 || d.H < 8 || d.I < 8 || d.E < 1 || d.K < 1) return false;
+  if (d.H % 8 || d.I % 8) return false;
+  if (d.E > 1024 || d.K > 16) return false;
+  if (d.T > (int64_t)1 << 31 || d.H > ((int64_t)1 << 20) || d.I > ((int64_t)1 << 20)) return false;
+  const int64_t S = d.T * d.K;
+  if (S + d.E * (BM - 1) + BM >= ((int64_t)1 << 31)) return false;
+  return true;
+}
+
+// ---- optional per-stage timer (process-global, not thread-safe)
+struct TimerRecord {
+  int stage;
+  cudaEvent_t start, stop;
+};
+struct Timer {
+  bool on = false;
+  std::vector<TimerRecord> pending;
+  std::vector<cudaEvent_t> pool;
+  cudaEvent_t get() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+};
+Timer g_timer;
+
+template <typename F>
+cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
+  if (!g_timer.on) return launch();
+  cudaEvent_t a = g_timer.get(), b = g_timer.get();
+  if (a) cudaEventRecord(a, st);
+  cudaError_t e = launch();
+  if (b) cudaEventRecord(b, st);
+  if (a && b)
+    g_timer.pending.push_back({stage, a, b});
+  else {
+    if (a) g_timer.pool.push_back(a);
+    if (b) g_timer.pool.push_back(b);
+  }
+  return e;
+}
+
+const char* kStageNames[ST_COUNT] = {
+    "route_count", "route_scan",  "route_rank", "gather_x",   "gemm1_swiglu",
+    "gemm2",       "combine_y",   "gather_dy",  "act_grad",   "d_topk",
+    "w2_grad",     "input_grad",  "combine_dx", "w1_grad"};
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define MM_TRY(expr)                      \
+  do {                                    \
+    cudaError_t _e = (expr);              \
+    if (_e != cudaSuccess) return MM_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+bool plan_workspace(const mm_dims& d, Workspace* w) {
+  if (!dims_ok(d)) return false;
+  Workspace p{};
+  p.T = d.T;
+  p.H = d.H;
+  p.I = d.I;
+  p.E = d.E;
+  p.K = d.K;
+  p.S = d.T * d.K;
+  const int64_t nonempty = std::min<int64_t>(d.E, p.S);
+  p.S_pad = (p.S + nonempty * (BM - 1) + BM - 1) / BM * BM;
+  p.n_chunks = (p.S + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+  p.n_act_tiles = (d.I + BN - 1) / BN;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  p.off_hdr = take(HDR_WORDS * sizeof(int32_t));
+  p.off_counts = take(d.E * sizeof(int32_t));
+  p.off_offsets = take((d.E + 1) * sizeof(int32_t));
+  p.off_poff = take((d.E + 1) * sizeof(int32_t));
+  p.off_chunk = take((size_t)p.n_chunks * d.E * sizeof(int32_t));
+  p.off_tile_expert = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
+  p.off_row_of_slot = take((size_t)p.S * sizeof(int32_t));
+  p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
+  p.off_w_row = take((size_t)p.S_pad * sizeof(float));
+  p.off_x_slot = take((size_t)p.S_pad * d.H * 2);
+  p.off_gu = take((size_t)p.S_pad * 2 * d.I * 2);
+  p.off_h = take((size_t)p.S_pad * d.I * 2);
+  p.off_o = take((size_t)p.S_pad * d.H * 2);
+  p.off_dy_slot = take((size_t)p.S_pad * d.H * 2);
+  p.off_dgu = take((size_t)p.S_pad * 2 * d.I * 2);
+  p.off_p_part = take((size_t)p.n_act_tiles * p.S_pad * sizeof(float));
+  p.total = off;
+  *w = p;
+  return true;
+}
+
+}  // namespace mm
+
+using namespace mm;
+
+extern "C" {
+
+int mm_abi_version(void) { return 1; }
+
+const char* mm_status_string(mm_status s) {
+  switch (s) {
+    case MM_OK: return "ok";
+    case MM_ERR_INVALID_ARG: return "invalid argument";
+    case MM_ERR_UNSUPPORTED: return "unsupported sizes";
+    case MM_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MM_ERR_CUDA: return "CUDA runtime error";
+    case MM_ERR_BAD_EXPERT_ID: return "expert id out of range";
+    case MM_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t mm_workspace_size(mm_dims d, uint32_t flags) {
+  (void)flags;
+  Workspace w;
+  if (!plan_workspace(d, &w)) return 0;
+  return w.total;
+}
+
+static mm_status check_common(const mm_dims& d, const void* ws, size_t ws_bytes, Workspace* w) {
+  if (d.T < 1 || d.H < 1 || d.I < 1 || d.E < 1 || d.K < 1) return MM_ERR_INVALID_ARG;
+  if (!plan_workspace(d, w)) return MM_ERR_UNSUPPORTED;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < w->total) return MM_ERR_WORKSPACE;
+  return MM_OK;
+}
+
+mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                     const void* up_proj_weight, const void* down_proj_weight, void* y,
+                     void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
+  Workspace w;
+  mm_status s = check_common(d, workspace, workspace_bytes, &w);
+  if (s != MM_OK) return s;
+  if (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !y)
+    return MM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(up_proj_weight, 16) || !aligned(down_proj_weight, 16) ||
+      !aligned(y, 16) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+    return MM_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+
+  MM_TRY(cudaMemsetAsync(ws + w.off_hdr, 0, HDR_WORDS * sizeof(int32_t), st));
+  MM_TRY(timed(ST_ROUTE_COUNT, st, [&] { return launch_route_count(w, ws, topk_ids, st); }));
+  if (flags & MM_FLAG_VALIDATE_IDS) {
+    int32_t status = 0;
+    MM_TRY(cudaMemcpyAsync(&status, ws + w.off_hdr, sizeof(status), cudaMemcpyDeviceToHost, st));
+    MM_TRY(cudaStreamSynchronize(st));
+    if (status != 0) return static_cast<mm_status>(status);
+  }
+  MM_TRY(timed(ST_ROUTE_SCAN, st, [&] { return launch_route_scan(w, ws, st); }));
+  MM_TRY(timed(ST_ROUTE_RANK, st,
+               [&] { return launch_route_rank(w, ws, topk_ids, topk_weights, st); }));
+  MM_TRY(timed(ST_GATHER_X, st,
+               [&] { return launch_gather_rows(w, ws, x, ws + w.off_x_slot, st); }));
+  GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs};
+  MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
+  c.kind = GK_GEMM2;
+  MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
+  MM_TRY(timed(ST_COMBINE_Y, st,
+               [&] { return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st); }));
+  return MM_OK;
+}
+
+mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
+                      const float* topk_weights, const void* up_proj_weight,
+                      const void* down_proj_weight, void* workspace, size_t workspace_bytes,
+                      void* dx, float* d_topk_weights, void* d_up_proj_weight,
+                      void* d_down_proj_weight, void* stream, uint32_t flags) {
+  (void)flags;
+  Workspace w;
+  mm_status s = check_common(d, workspace, workspace_bytes, &w);
+  if (s != MM_OK) return s;
+  if (!dy || !x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !dx ||
+      !d_topk_weights || !d_up_proj_weight || !d_down_proj_weight)
+    return MM_ERR_INVALID_ARG;
+  if (!aligned(dy, 16) || !aligned(x, 16) || !aligned(up_proj_weight, 16) ||
+      !aligned(down_proj_weight, 16) || !aligned(dx, 16) || !aligned(d_up_proj_weight, 16) ||
+      !aligned(d_down_proj_weight, 16) || !aligned(d_topk_weights, 4) || !aligned(topk_ids, 4) ||
+      !aligned(topk_weights, 4))
+    return MM_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+
+  MM_TRY(timed(ST_GATHER_DY, st,
+               [&] { return launch_gather_rows(w, ws, dy, ws + w.off_dy_slot, st); }));
+  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs};
+  MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
+  c.kind = GK_W2_GRAD;
+  c.d_w = d_down_proj_weight;
+  MM_TRY(timed(ST_W2_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  c.kind = GK_INPUT_GRAD;
+  c.d_w = nullptr;
+  MM_TRY(timed(ST_INPUT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  MM_TRY(timed(ST_COMBINE_DX, st,
+               [&] { return launch_combine(w, ws, ws + w.off_o, nullptr, dx, st); }));
+  c.kind = GK_W1_GRAD;
+  c.d_w = d_up_proj_weight;
+  MM_TRY(timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  return MM_OK;
+}
+
+mm_status mm_get_status(const void* workspace, void* stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return MM_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MM_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MM_ERR_CUDA;
+  return static_cast<mm_status>(v);
+}
+
+mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts, int32_t* offsets,
+                            int32_t* row_of_slot, void* stream) {
+  Workspace w;
+  if (!plan_workspace(d, &w)) return MM_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !aligned(workspace, 256)) return MM_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const char* ws = reinterpret_cast<const char*>(workspace);
+  if (counts)
+    MM_TRY(cudaMemcpyAsync(counts, ws + w.off_counts, w.E * sizeof(int32_t), cudaMemcpyDefault, st));
+  if (offsets)
+    MM_TRY(cudaMemcpyAsync(offsets, ws + w.off_offsets, (w.E + 1) * sizeof(int32_t),
+                           cudaMemcpyDefault, st));
+  if (row_of_slot) {
+    // converted into the backward-only p_part scratch, then copied out
+    int32_t* tmp = reinterpret_cast<int32_t*>(const_cast<char*>(ws) + w.off_p_part);
+    MM_TRY(launch_export_rows(w, ws, tmp, st));
+    MM_TRY(cudaMemcpyAsync(row_of_slot, tmp, w.S * sizeof(int32_t), cudaMemcpyDefault, st));
+  }
+  MM_TRY(cudaStreamSynchronize(st));
+  return MM_OK;
+}
+
+mm_status mm_timing_enable(int on) {
+  g_timer.on = on != 0;
+  return MM_OK;
+}
+
+int mm_timing_read(double* ms, int64_t* launches, int max_stages) {
+  double acc[ST_COUNT] = {0};
+  int64_t cnt[ST_COUNT] = {0};
+  for (auto& r : g_timer.pending) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&t, r.start, r.stop) == cudaSuccess) {
+      acc[r.stage] += t;
+      cnt[r.stage] += 1;
+    }
+    g_timer.pool.push_back(r.start);
+    g_timer.pool.push_back(r.stop);
+  }
+  g_timer.pending.clear();
+  for (int i = 0; i < ST_COUNT && i < max_stages; ++i) {
+    if (ms) ms[i] = acc[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return ST_COUNT;
+}
+
+const char* mm_stage_name(int stage) {
+  if (stage < 0 || stage >= ST_COUNT) return "";
+  return kStageNames[stage];
+}
+
+}  // extern "C"

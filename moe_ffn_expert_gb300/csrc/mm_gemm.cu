@@ -1,0 +1,601 @@
+// Grouped GEMMs of the MoE-FFN layer on the sm_103a tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// One persistent, warp-specialised kernel template serves all six products of the layer
+// (RFC "HyperParallel Multicore HyperMegaMoE fused forward/backward operator", §2.1 GMM1/GMM2,
+// §2.2 act_grad, input_grad, W2Grad and W1Grad):
+//
+//   kind         A (rows x red.)          B (red. x cols)              epilogue
+//   GEMM1        x_slot [rows,H]  K-maj   W_up[e]   [H,2I]  N-major    gu = [gate|up], h = silu(gate)*up
+//   GEMM2        h      [rows,I]  K-maj   W_down[e] [I,H]   N-major    o (bf16)
+//   ACT_GRAD     dy_slot[rows,H]  K-maj   W_down[e]^T       K-major    SwiGLU backward: dgu, hw, <g,h>
+//   INPUT_GRAD   dgu    [rows,2I] K-maj   W_up[e]^T         K-major    dx_slot (bf16)
+//   W2_GRAD      hw_e^T [I,M_e]   M-maj   dy_slot_e [M_e,H] N-major    dW_down[e] (bf16)
+//   W1_GRAD      x_slot_e^T[H,M_e] M-maj  dgu_e [M_e,2I]    N-major    dW_up[e] (bf16)
+//
+// Row-grouped kinds walk 128-row tiles of the expert-sorted (padded) row buffers; each tile
+// belongs to one expert, whose weight slab is the third coordinate of a 3-D tensor map.
+// Weight-gradient kinds walk (expert, row tile, column tile) of the weight, reducing over
+// the expert's padded rows (pad rows are zero, an expert with no rows gets a zero tile).
+//
+// Warp roles (192 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
+//   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring (mbarrier per
+//               stage, transaction-count completion);
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
+//               tcgen05.mma (128x256x16 per instruction) and tcgen05.commit's the stage and
+//               accumulator barriers;
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
+//               i.e. one tile row per thread), apply the kind's epilogue, store to global memory,
+//               release the accumulator so the next tile's MMAs overlap this epilogue.
+// All operand tiles use the 128-byte swizzle; every mbarrier wait is bounded by %globaltimer and
+// a wait that runs out records MM_ERR_TIMEOUT, stops the role and still frees TMEM.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mm_device.cuh"
+#include "mm_kernels.h"
+
+namespace mm {
+namespace {
+
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile: 8 KB
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(BK == 64, "one 128-byte swizzle row per k-block");
+
+struct Args {
+  const int* hdr;
+  const int32_t* tile_expert;
+  const int32_t* poff;
+  int* status;
+  int n_tiles_n;   // column tiles
+  int k_iters;     // row-grouped kinds: reduction blocks of BK
+  int E;
+  int m_tiles_w;   // weight-gradient kinds: row tiles of the weight
+  int N;           // valid output columns
+  int M;           // weight-gradient kinds: valid output rows
+  int I;           // intermediate size
+  __nv_bfloat16* out0;
+  int64_t ld0;
+  __nv_bfloat16* out1;
+  int64_t ld1;
+  const __nv_bfloat16* gu;
+  int64_t ld_gu;
+  const float* w_row;
+  float* p_part;
+  int64_t S_pad;
+  int64_t out_expert_stride;
+  uint64_t timeout_ns;
+};
+
+template <int KIND>
+struct Traits {
+  static constexpr bool WGRAD = (KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
+  static constexpr bool A_MN = WGRAD;
+  static constexpr bool B_MN =
+      (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+};
+
+struct Tile {
+  int e, m0, n0, kiters, row0;
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
+  Tile t;
+  if constexpr (Traits<KIND>::WGRAD) {
+    const int per_e = a.m_tiles_w * a.n_tiles_n;
+    t.e = tile / per_e;
+    const int rem = tile - t.e * per_e;
+    const int mt = rem / a.n_tiles_n;
+    const int nt = rem - mt * a.n_tiles_n;
+    t.m0 = mt * BM;
+    t.n0 = nt * BN;
+    t.row0 = __ldg(a.poff + t.e);
+    t.kiters = (__ldg(a.poff + t.e + 1) - t.row0) / BK;
+  } else {
+    const int mt = tile / a.n_tiles_n;
+    const int nt = tile - mt * a.n_tiles_n;
+    t.e = __ldg(a.tile_expert + mt);
+    t.m0 = mt * BM;
+    t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
+    t.row0 = t.m0;
+    t.kiters = a.k_iters;
+  }
+  return t;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, int N) {
+  // 32 consecutive columns starting at n, masked in groups of 8 (N is a multiple of 8)
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (n + 8 * g < N) {
+      uint4 q;
+      q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+      q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+      q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+      q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+      *reinterpret_cast<uint4*>(dst + n + 8 * g) = q;
+    }
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint32_t tacc, int r) {
+  if constexpr (KIND == GK_GEMM1_SWIGLU) {
+    // accumulator columns [0,128) = gate columns n0.., [128,256) = up columns n0..
+    const int64_t row = (int64_t)t.m0 + r;
+    __nv_bfloat16* gu = a.out0 + row * a.ld0;
+    __nv_bfloat16* hh = a.out1 + row * a.ld1;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ga[32], ub[32];
+      tmem_ld_32x32(tacc + c * 32, ga);
+      tmem_ld_32x32(tacc + 128 + c * 32, ub);
+      tmem_ld_wait();
+      const int n = t.n0 + c * 32;
+      float g[32], u[32], h[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = __uint_as_float(ga[j]);
+        u[j] = __uint_as_float(ub[j]);
+        h[j] = g[j] * sigmoidf_(g[j]) * u[j];
+      }
+      store_row_bf16(gu, g, n, a.I);
+      store_row_bf16(gu + a.I, u, n, a.I);
+      store_row_bf16(hh, h, n, a.I);
+    }
+  } else if constexpr (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD) {
+    const int64_t row = (int64_t)t.m0 + r;
+    __nv_bfloat16* o = a.out0 + row * a.ld0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32(tacc + c * 32, v);
+      tmem_ld_wait();
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+      store_row_bf16(o, f, t.n0 + c * 32, a.N);
+    }
+  } else if constexpr (KIND == GK_ACT_GRAD) {
+    // g = dy_slot . W_down^T for columns n0.. of I; recompute SwiGLU from the saved gate|up.
+    const int64_t row = (int64_t)t.m0 + r;
+    const __nv_bfloat16* gu = a.gu + row * a.ld_gu;
+    __nv_bfloat16* dgu = a.out0 + row * a.ld0;
+    __nv_bfloat16* hw = a.out1 + row * a.ld1;
+    const float w = __ldg(a.w_row + row);
+    float p = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int n = t.n0 + c * 32;
+      if (n >= a.I) break;
+      uint32_t v[32];
+      tmem_ld_32x32(tacc + c * 32, v);
+      tmem_ld_wait();
+      float da[32], db[32], hv[32];
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        uint4 av = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
+        if (n + 8 * g8 < a.I) {
+          av = *reinterpret_cast<const uint4*>(gu + n + 8 * g8);
+          bv = *reinterpret_cast<const uint4*>(gu + a.I + n + 8 * g8);
+        }
+        const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float ga = (j & 1) ? bf16_hi(aw[j >> 1]) : bf16_lo(aw[j >> 1]);
+          const float ub = (j & 1) ? bf16_hi(bw[j >> 1]) : bf16_lo(bw[j >> 1]);
+          const float gv = __uint_as_float(v[8 * g8 + j]);
+          const float sg = sigmoidf_(ga);
+          const float sl = ga * sg;
+          const float h = sl * ub;
+          const bool valid = (n + 8 * g8 < a.I);
+          p += valid ? gv * h : 0.f;
+          const float dh = w * gv;
+          da[8 * g8 + j] = dh * ub * sg * (1.0f + ga * (1.0f - sg));
+          db[8 * g8 + j] = dh * sl;
+          hv[8 * g8 + j] = w * h;
+        }
+      }
+      store_row_bf16(dgu, da, n, a.I);
+      store_row_bf16(dgu + a.I, db, n, a.I);
+      store_row_bf16(hw, hv, n, a.I);
+    }
+    a.p_part[(int64_t)(t.n0 / BN) * a.S_pad + row] = p;
+  } else {  // weight gradients (every lane runs the TMEM loads; rows past M store nothing)
+    const int m = t.m0 + r;
+    const bool row_ok = m < a.M;
+    __nv_bfloat16* o = a.out0 + (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32(tacc + c * 32, v);
+      tmem_ld_wait();
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+      if (row_ok) store_row_bf16(o, f, t.n0 + c * 32, a.N);
+    }
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r) {
+  const int m = t.m0 + r;
+  if (m >= a.M) return;
+  __nv_bfloat16* o = a.out0 + (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+  float z[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) z[j] = 0.f;
+  for (int c = 0; c < BN / 32; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+           const Args a) {
+  using TR = Traits<KIND>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform)
+  if (__syncthreads_or(a.hdr[HDR_STATUS] != 0)) return;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  const uint32_t bars = sbase + STAGES * STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t tmem_holder = bars + 8u * (2 * STAGES + 4);
+  volatile uint32_t* tmem_holder_ptr =
+      reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = TR::WGRAD ? a.E * a.m_tiles_w * a.n_tiles_n
+                              : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder_ptr;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile<KIND>(a, tile);
+        for (int kb = 0; kb < t.kiters; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, tmo)) {
+            set_status(a.status, MM_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
+          const int k0 = kb * BK;
+          if constexpr (TR::A_MN) {
+            tma_load_2d(sa, &tmA, full_bar(s), t.m0, t.row0 + k0);
+            tma_load_2d(sa + MN_BLOCK_BYTES, &tmA, full_bar(s), t.m0 + 64, t.row0 + k0);
+          } else {
+            tma_load_2d(sa, &tmA, full_bar(s), k0, t.m0);
+          }
+          if constexpr (KIND == GK_GEMM1_SWIGLU) {
+            tma_load_3d(sb + 0 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0, k0, t.e);
+            tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
+            tma_load_3d(sb + 2 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0, k0, t.e);
+            tma_load_3d(sb + 3 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0 + 64, k0, t.e);
+          } else if constexpr (KIND == GK_GEMM2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_3d(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, k0, t.e);
+          } else if constexpr (KIND == GK_ACT_GRAD || KIND == GK_INPUT_GRAD) {
+            tma_load_3d(sb, &tmB, full_bar(s), k0, t.n0, t.e);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, t.row0 + k0);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile<KIND>(a, tile);
+        if (t.kiters == 0) continue;
+        const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+        if (!mbar_wait(acce_bar(buf), aph ^ 1u, tmo)) {
+          set_status(a.status, MM_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        for (int kb = 0; kb < t.kiters; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, tmo)) {
+            set_status(a.status, MM_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = TR::A_MN ? sdesc_sw128(sa + kk * 2048, MN_BLOCK_BYTES, 1024)
+                                         : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = TR::B_MN ? sdesc_sw128(sb + kk * 2048, MN_BLOCK_BYTES, 1024)
+                                         : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16(d, ad, bd, TR::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        umma_commit(accf_bar(buf));
+        ++acc_it;
+      }
+    }
+  } else {
+    const int q = warp & 3;        // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;   // tile row of this thread
+    uint32_t acc_it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile<KIND>(a, tile);
+      if (t.kiters == 0) {
+        if constexpr (TR::WGRAD) zero_wgrad_tile<KIND>(a, t, r);
+        continue;
+      }
+      const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(accf_bar(buf), aph, tmo) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) set_status(a.status, MM_ERR_TIMEOUT);
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+      epilogue_tile<KIND>(a, t, tacc, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+      ++acc_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/box innermost first; strides in bytes (rank-1).
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, s, b,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_rows(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_cols,
+              uint32_t box_rows) {
+  const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)cols * 2};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return make_map(m, base, 2, dims, strides, box);
+}
+
+bool map_experts(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t E,
+                 uint32_t box_cols, uint32_t box_rows) {
+  const uint64_t dims[3] = {(uint64_t)cols, (uint64_t)rows, (uint64_t)E};
+  const uint64_t strides[2] = {(uint64_t)cols * 2, (uint64_t)cols * rows * 2};
+  const uint32_t box[3] = {box_cols, box_rows, 1};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int KIND>
+cudaError_t set_smem_attr() {
+  static uint64_t done_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done_mask & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(k_gemm<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SMEM_BYTES);
+  if (e == cudaSuccess) done_mask |= bit;
+  return e;
+}
+
+inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+template <int KIND>
+cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
+  cudaError_t err = set_smem_attr<KIND>();
+  if (err != cudaSuccess) return err;
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorNoDevice;
+  const int64_t H = w.H, I = w.I, E = w.E, S_pad = w.S_pad;
+  auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
+
+  Args a{};
+  a.hdr = reinterpret_cast<const int*>(ws + w.off_hdr);
+  a.status = reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS;
+  a.tile_expert = reinterpret_cast<const int32_t*>(ws + w.off_tile_expert);
+  a.poff = reinterpret_cast<const int32_t*>(ws + w.off_poff);
+  a.E = (int)E;
+  a.I = (int)I;
+  a.S_pad = S_pad;
+  a.timeout_ns = c.timeout_ns;
+
+  CUtensorMap ta, tb;
+  bool ok = true;
+  int64_t tiles_max = 0;
+  const int64_t m_tiles_max = S_pad / BM;
+  switch (KIND) {
+    case GK_GEMM1_SWIGLU:
+      ok = map_rows(&ta, ws + w.off_x_slot, H, S_pad, 64, BM) &&
+           map_experts(&tb, c.w_up, 2 * I, H, E, 64, 64);
+      a.n_tiles_n = cdiv(I, BN / 2);
+      a.k_iters = cdiv(H, BK);
+      a.N = (int)I;
+      a.out0 = bf(w.off_gu);
+      a.ld0 = 2 * I;
+      a.out1 = bf(w.off_h);
+      a.ld1 = I;
+      tiles_max = m_tiles_max * a.n_tiles_n;
+      break;
+    case GK_GEMM2:
+      ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, BM) &&
+           map_experts(&tb, c.w_down, H, I, E, 64, 64);
+      a.n_tiles_n = cdiv(H, BN);
+      a.k_iters = cdiv(I, BK);
+      a.N = (int)H;
+      a.out0 = bf(w.off_o);
+      a.ld0 = H;
+      tiles_max = m_tiles_max * a.n_tiles_n;
+      break;
+    case GK_ACT_GRAD:
+      ok = map_rows(&ta, ws + w.off_dy_slot, H, S_pad, 64, BM) &&
+           map_experts(&tb, c.w_down, H, I, E, 64, BN);
+      a.n_tiles_n = cdiv(I, BN);
+      a.k_iters = cdiv(H, BK);
+      a.N = (int)I;
+      a.out0 = bf(w.off_dgu);
+      a.ld0 = 2 * I;
+      a.out1 = bf(w.off_h);  // hw = w * h reuses the forward's h buffer
+      a.ld1 = I;
+      a.gu = bf(w.off_gu);
+      a.ld_gu = 2 * I;
+      a.w_row = reinterpret_cast<const float*>(ws + w.off_w_row);
+      a.p_part = reinterpret_cast<float*>(ws + w.off_p_part);
+      tiles_max = m_tiles_max * a.n_tiles_n;
+      break;
+    case GK_INPUT_GRAD:
+      ok = map_rows(&ta, ws + w.off_dgu, 2 * I, S_pad, 64, BM) &&
+           map_experts(&tb, c.w_up, 2 * I, H, E, 64, BN);
+      a.n_tiles_n = cdiv(H, BN);
+      a.k_iters = cdiv(2 * I, BK);
+      a.N = (int)H;
+      a.out0 = bf(w.off_o);  // dx_slot reuses the forward's o buffer
+      a.ld0 = H;
+      tiles_max = m_tiles_max * a.n_tiles_n;
+      break;
+    case GK_W2_GRAD:
+      ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, 64) &&
+           map_rows(&tb, ws + w.off_dy_slot, H, S_pad, 64, 64);
+      a.m_tiles_w = cdiv(I, BM);
+      a.n_tiles_n = cdiv(H, BN);
+      a.M = (int)I;
+      a.N = (int)H;
+      a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
+      a.ld0 = H;
+      a.out_expert_stride = I * H;
+      tiles_max = E * a.m_tiles_w * a.n_tiles_n;
+      break;
+    case GK_W1_GRAD:
+      ok = map_rows(&ta, ws + w.off_x_slot, H, S_pad, 64, 64) &&
+           map_rows(&tb, ws + w.off_dgu, 2 * I, S_pad, 64, 64);
+      a.m_tiles_w = cdiv(H, BM);
+      a.n_tiles_n = cdiv(2 * I, BN);
+      a.M = (int)H;
+      a.N = (int)(2 * I);
+      a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
+      a.ld0 = 2 * I;
+      a.out_expert_stride = H * 2 * I;
+      tiles_max = E * a.m_tiles_w * a.n_tiles_n;
+      break;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
+  k_gemm<KIND><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
+  switch (c.kind) {
+    case GK_GEMM1_SWIGLU: return run<GK_GEMM1_SWIGLU>(w, ws, c, st);
+    case GK_GEMM2: return run<GK_GEMM2>(w, ws, c, st);
+    case GK_ACT_GRAD: return run<GK_ACT_GRAD>(w, ws, c, st);
+    case GK_INPUT_GRAD: return run<GK_INPUT_GRAD>(w, ws, c, st);
+    case GK_W2_GRAD: return run<GK_W2_GRAD>(w, ws, c, st);
+    case GK_W1_GRAD: return run<GK_W1_GRAD>(w, ws, c, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mm

@@ -1,0 +1,47 @@
+// Host launchers of the library's kernels (each enqueues exactly one kernel on `stream`).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mm_layout.h"
+
+namespace mm {
+
+// ---- routing, dispatch and combine (mm_route.cu)
+cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids, cudaStream_t st);
+cudaError_t launch_route_scan(const Workspace& w, char* ws, cudaStream_t st);
+cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
+                              cudaStream_t st);
+// dst[r] = src[slot_of_row[r] / K] for every real row, zeros for pad rows.
+cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, void* dst,
+                               cudaStream_t st);
+// out[t] = sum_k (weights ? weights[t,k] : 1) * rows[row_of_slot[t*K+k]], k ascending, fp32.
+cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
+                           void* out, cudaStream_t st);
+// d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]].
+cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st);
+// Converts the padded row_of_slot table to positions in the unpadded expert-sorted order.
+cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out, cudaStream_t st);
+
+// ---- grouped GEMMs on tcgen05 (mm_gemm.cu)
+enum GemmKind {
+  GK_GEMM1_SWIGLU = 0,  // gu = x_slot W_up[e]; h = silu(gate) * up
+  GK_GEMM2 = 1,         // o = h W_down[e]
+  GK_ACT_GRAD = 2,      // g = dy_slot W_down[e]^T, SwiGLU backward in the epilogue
+  GK_INPUT_GRAD = 3,    // dx_slot = dgu W_up[e]^T
+  GK_W2_GRAD = 4,       // dW_down[e] = hw_e^T dy_slot_e
+  GK_W1_GRAD = 5,       // dW_up[e] = x_slot_e^T dgu_e
+};
+
+struct GemmCall {
+  GemmKind kind;
+  const void* w_up;    // bf16 [E, H, 2I]
+  const void* w_down;  // bf16 [E, I, H]
+  void* d_w;           // weight-gradient output (W1/W2 grads)
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);
+
+}  // namespace mm

@@ -1,0 +1,64 @@
+// Workspace layout and launch-side declarations shared by the library's translation units.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mm.h"
+
+namespace mm {
+
+// Row tiles of the grouped GEMMs. Every expert's rows are padded up to a multiple of BM in
+// the expert-sorted buffers, so a row tile never straddles two experts and pad rows hold
+// zeros (they then add nothing to the weight-gradient reductions).
+constexpr int BM = 128;
+constexpr int BK = 64;   // 64 bf16 = 128 bytes: one 128B-swizzle row
+constexpr int BN = 256;  // accumulator columns per tile (fp32, one TMEM column each)
+
+// Slots handled by one warp in the routing kernels.
+constexpr int ROUTE_CHUNK = 512;
+
+// Header words (int32) at the start of the workspace.
+enum HeaderWord {
+  HDR_STATUS = 0,      // mm_status of the call (0 = OK)
+  HDR_NUM_MTILES = 1,  // number of BM-row tiles over all experts (padded rows / BM)
+  HDR_BAD_SLOT = 2,    // first slot seen with an invalid expert id (diagnostics)
+  HDR_WORDS = 64
+};
+
+// Stage ids of the per-stage timer.
+enum Stage {
+  ST_ROUTE_COUNT = 0,
+  ST_ROUTE_SCAN,
+  ST_ROUTE_RANK,
+  ST_GATHER_X,
+  ST_GEMM1_SWIGLU,
+  ST_GEMM2,
+  ST_COMBINE_Y,
+  ST_GATHER_DY,
+  ST_ACT_GRAD,
+  ST_D_TOPK,
+  ST_W2_GRAD,
+  ST_INPUT_GRAD,
+  ST_COMBINE_DX,
+  ST_W1_GRAD,
+  ST_COUNT
+};
+static_assert(ST_COUNT == MM_NUM_STAGES, "stage table");
+
+// Byte offsets of every region in the caller's workspace (all 256-byte aligned).
+struct Workspace {
+  int64_t T, H, I, E, K, S;
+  int64_t S_pad;        // worst-case padded rows (multiple of BM)
+  int64_t n_chunks;     // routing chunks of ROUTE_CHUNK slots
+  int64_t n_act_tiles;  // act_grad column tiles (ceil(I / BN)) = rows of the d_topk partials
+  size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
+  size_t off_row_of_slot, off_slot_of_row, off_w_row;
+  size_t off_x_slot, off_gu, off_h, off_o, off_dy_slot, off_dgu, off_p_part;
+  size_t total;
+};
+
+// Fills `w` for the sizes in `d`; returns false if the sizes are unsupported.
+bool plan_workspace(const mm_dims& d, Workspace* w);
+
+}  // namespace mm

@@ -1,0 +1,332 @@
+// Routing preprocessing, dispatch (row gather) and combine (fixed-order weighted unpermute).
+//
+// RFC "HyperParallel Multicore HyperMegaMoE fused forward/backward operator":
+//   §3.3 offsets / group list built inside the operator, §4.1 each token expands into K expert
+//   slots, dispatch sends a slot to its expert, combine merges expert outputs back with
+//   topk_weights; §2.2 Combine(dX) sums the input-gradient rows of a token's slots.
+// On one GPU dispatch is a gather of x rows into expert-sorted order and combine is a gather
+// back, summed over k in ascending order in fp32 (deterministic: no atomics on data).
+//
+// Routing is three small kernels, all integer and bit-exact:
+//   count: one warp per chunk of ROUTE_CHUNK slots builds that chunk's per-expert histogram
+//          (__match_any_sync groups lanes holding the same expert);
+//   scan:  one CTA sums the chunk histograms per expert, scans them into the expert offsets
+//          (plain and padded to BM rows), turns the histograms into per-chunk running bases
+//          and writes the row-tile -> expert table and the pad-row markers;
+//   rank:  each warp replays its chunk in slot order, so a slot's row is its expert's base
+//          plus the number of earlier slots of that expert: a stable order in s.
+#include "mm_device.cuh"
+#include "mm_kernels.h"
+
+namespace mm {
+namespace {
+
+template <typename T>
+T* region(char* ws, size_t off) {
+  return reinterpret_cast<T*>(ws + off);
+}
+template <typename T>
+const T* region(const char* ws, size_t off) {
+  return reinterpret_cast<const T*>(ws + off);
+}
+
+__global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__ ids, int* hdr,
+                                                     int32_t* __restrict__ chunk_cnt, int S, int E,
+                                                     int n_chunks) {
+  extern __shared__ int32_t cnt_smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * 4 + warp;
+  if (chunk >= n_chunks) return;  // whole warp leaves; no CTA-wide barrier below
+  int32_t* cnt = cnt_smem + warp * E;
+  for (int i = lane; i < E; i += 32) cnt[i] = 0;
+  __syncwarp();
+  const int s0 = chunk * ROUTE_CHUNK;
+  const int s1 = min(S, s0 + ROUTE_CHUNK);
+  for (int base = s0; base < s1; base += 32) {
+    const int s = base + lane;
+    int e = -1;
+    if (s < s1) {
+      e = __ldg(ids + s);
+      if (e < 0 || e >= E) {
+        set_status(hdr + HDR_STATUS, MM_ERR_BAD_EXPERT_ID);
+        atomicCAS(hdr + HDR_BAD_SLOT, 0, s + 1);
+        e = -1;
+      }
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(m) - 1) cnt[e] += __popc(m);
+    __syncwarp();
+  }
+  for (int i = lane; i < E; i += 32) chunk_cnt[(size_t)chunk * E + i] = cnt[i];
+}
+
+__global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restrict__ chunk_cnt,
+                                                     int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ poff,
+                                                     int32_t* __restrict__ tile_expert,
+                                                     int32_t* __restrict__ slot_of_row,
+                                                     float* __restrict__ w_row, int E,
+                                                     int n_chunks) {
+  __shared__ int wsum[32], wsum_p[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (hdr[HDR_STATUS] != 0) {  // bad ids: schedule nothing downstream
+    if (tid == 0) hdr[HDR_NUM_MTILES] = 0;
+    return;
+  }
+  int c = 0;
+  if (tid < E)
+    for (int k = 0; k < n_chunks; ++k) c += chunk_cnt[(size_t)k * E + tid];
+  const int pc = (c + BM - 1) / BM * BM;
+  int a = c, b = pc;  // inclusive warp scans
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, a, d);
+    const int yb = __shfl_up_sync(0xffffffffu, b, d);
+    if (lane >= d) {
+      a += ya;
+      b += yb;
+    }
+  }
+  if (lane == 31) {
+    wsum[warp] = a;
+    wsum_p[warp] = b;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int u = lane < nw ? wsum[lane] : 0, v = lane < nw ? wsum_p[lane] : 0;
+    const int u0 = u, v0 = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int yu = __shfl_up_sync(0xffffffffu, u, d);
+      const int yv = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) {
+        u += yu;
+        v += yv;
+      }
+    }
+    wsum[lane] = u - u0;  // exclusive prefix of warp totals
+    wsum_p[lane] = v - v0;
+  }
+  __syncthreads();
+  if (tid >= E) return;
+  const int off = a - c + wsum[warp];
+  const int po = b - pc + wsum_p[warp];
+  counts[tid] = c;
+  offsets[tid] = off;
+  poff[tid] = po;
+  if (tid == E - 1) {
+    offsets[E] = off + c;
+    poff[E] = po + pc;
+    hdr[HDR_NUM_MTILES] = (po + pc) / BM;
+  }
+  int run = po;  // chunk histograms -> running padded-row base of each chunk
+  for (int k = 0; k < n_chunks; ++k) {
+    const int v = chunk_cnt[(size_t)k * E + tid];
+    chunk_cnt[(size_t)k * E + tid] = run;
+    run += v;
+  }
+  for (int t = po / BM; t < (po + pc) / BM; ++t) tile_expert[t] = tid;
+  for (int r = po + c; r < po + pc; ++r) {
+    slot_of_row[r] = -1;
+    w_row[r] = 0.0f;
+  }
+}
+
+__global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ ids,
+                                                    const float* __restrict__ topk_w,
+                                                    const int* hdr,
+                                                    const int32_t* __restrict__ chunk_base,
+                                                    int32_t* __restrict__ row_of_slot,
+                                                    int32_t* __restrict__ slot_of_row,
+                                                    float* __restrict__ w_row, int S, int E,
+                                                    int n_chunks) {
+  extern __shared__ int32_t cnt_smem[];
+  if (hdr[HDR_STATUS] != 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * 4 + warp;
+  if (chunk >= n_chunks) return;
+  int32_t* cnt = cnt_smem + warp * E;
+  for (int i = lane; i < E; i += 32) cnt[i] = chunk_base[(size_t)chunk * E + i];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int s0 = chunk * ROUTE_CHUNK;
+  const int s1 = min(S, s0 + ROUTE_CHUNK);
+  for (int base = s0; base < s1; base += 32) {
+    const int s = base + lane;
+    const int e = s < s1 ? __ldg(ids + s) : -1;
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    int row = 0;
+    if (e >= 0) row = cnt[e] + __popc(m & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) cnt[e] += __popc(m);
+    __syncwarp();
+    if (e >= 0) {
+      row_of_slot[s] = row;
+      slot_of_row[row] = s;
+      w_row[row] = __ldg(topk_w + s);
+    }
+  }
+}
+
+// One warp per destination row, 16-byte vectors.
+__global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src,
+                                                     uint4* __restrict__ dst,
+                                                     const int32_t* __restrict__ slot_of_row,
+                                                     const int* hdr, int K, int vpr) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (hdr[HDR_STATUS] != 0 || row >= hdr[HDR_NUM_MTILES] * BM) return;
+  const int s = slot_of_row[row];
+  uint4* d = dst + (size_t)row * vpr;
+  if (s < 0) {
+    for (int i = lane; i < vpr; i += 32) d[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* p = src + (size_t)(s / K) * vpr;
+#pragma unroll 4
+  for (int i = lane; i < vpr; i += 32) d[i] = __ldg(p + i);
+}
+
+__device__ __forceinline__ void acc8(float (&a)[8], float w, const uint4& v) {
+  a[0] += w * bf16_lo(v.x);
+  a[1] += w * bf16_hi(v.x);
+  a[2] += w * bf16_lo(v.y);
+  a[3] += w * bf16_hi(v.y);
+  a[4] += w * bf16_lo(v.z);
+  a[5] += w * bf16_hi(v.z);
+  a[6] += w * bf16_lo(v.w);
+  a[7] += w * bf16_hi(v.w);
+}
+
+// One warp per token, 8 columns (16 bytes) per lane per step, slots summed in k order.
+__global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
+                                                 const int32_t* __restrict__ row_of_slot,
+                                                 const float* __restrict__ weights,
+                                                 uint4* __restrict__ out, const int* hdr, int T,
+                                                 int K, int vpr) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (hdr[HDR_STATUS] != 0 || t >= T) return;
+  int r[16];
+  float w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    r[k] = k < K ? __ldg(row_of_slot + (size_t)t * K + k) : 0;
+    w[k] = (k < K && weights != nullptr) ? __ldg(weights + (size_t)t * K + k) : 1.0f;
+  }
+  for (int i = lane; i < vpr; i += 32) {
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (k < K) acc8(a, w[k], __ldg(rows + (size_t)r[k] * vpr + i));
+    uint4 o;
+    o.x = pack_bf16(a[0], a[1]);
+    o.y = pack_bf16(a[2], a[3]);
+    o.z = pack_bf16(a[4], a[5]);
+    o.w = pack_bf16(a[6], a[7]);
+    out[(size_t)t * vpr + i] = o;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_d_topk(const float* __restrict__ p_part,
+                                                const int32_t* __restrict__ row_of_slot,
+                                                float* __restrict__ d_topk, const int* hdr, int S,
+                                                int n_tiles, int64_t S_pad) {
+  const int s = blockIdx.x * 256 + threadIdx.x;
+  if (hdr[HDR_STATUS] != 0 || s >= S) return;
+  const int r = row_of_slot[s];
+  float acc = 0.f;
+  for (int j = 0; j < n_tiles; ++j) acc += p_part[(size_t)j * S_pad + r];
+  d_topk[s] = acc;
+}
+
+__global__ void __launch_bounds__(256) k_export_rows(const int32_t* __restrict__ row_of_slot,
+                                                     const int32_t* __restrict__ tile_expert,
+                                                     const int32_t* __restrict__ poff,
+                                                     const int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ out, const int* hdr,
+                                                     int S) {
+  const int s = blockIdx.x * 256 + threadIdx.x;
+  if (s >= S) return;
+  if (hdr[HDR_STATUS] != 0) {
+    out[s] = -1;
+    return;
+  }
+  const int r = row_of_slot[s];
+  const int e = tile_expert[r / BM];
+  out[s] = r - poff[e] + offsets[e];
+}
+
+inline unsigned div_up(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
+
+}  // namespace
+
+cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids, cudaStream_t st) {
+  const unsigned grid = div_up(w.n_chunks, 4);
+  k_route_count<<<grid, 128, 4 * w.E * sizeof(int32_t), st>>>(
+      ids, region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk), (int)w.S, (int)w.E,
+      (int)w.n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_scan(const Workspace& w, char* ws, cudaStream_t st) {
+  k_route_scan<<<1, 1024, 0, st>>>(
+      region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
+      region<int32_t>(ws, w.off_counts), region<int32_t>(ws, w.off_offsets),
+      region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_tile_expert),
+      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row), (int)w.E,
+      (int)w.n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
+                              cudaStream_t st) {
+  const unsigned grid = div_up(w.n_chunks, 4);
+  k_route_rank<<<grid, 128, 4 * w.E * sizeof(int32_t), st>>>(
+      ids, topk_w, region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
+      region<int32_t>(ws, w.off_row_of_slot), region<int32_t>(ws, w.off_slot_of_row),
+      region<float>(ws, w.off_w_row), (int)w.S, (int)w.E, (int)w.n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, void* dst,
+                               cudaStream_t st) {
+  const unsigned grid = div_up(w.S_pad, 8);
+  k_gather_rows<<<grid, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
+      region<int32_t>(ws, w.off_slot_of_row), region<int>(ws, w.off_hdr), (int)w.K,
+      (int)(w.H / 8));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
+                           void* out, cudaStream_t st) {
+  const unsigned grid = div_up(w.T, 8);
+  k_combine<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(rows),
+                                  region<int32_t>(ws, w.off_row_of_slot), weights,
+                                  reinterpret_cast<uint4*>(out), region<int>(ws, w.off_hdr),
+                                  (int)w.T, (int)w.K, (int)(w.H / 8));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st) {
+  const unsigned grid = div_up(w.S, 256);
+  k_d_topk<<<grid, 256, 0, st>>>(region<float>(ws, w.off_p_part),
+                                 region<int32_t>(ws, w.off_row_of_slot), d_topk,
+                                 region<int>(ws, w.off_hdr), (int)w.S, (int)w.n_act_tiles,
+                                 w.S_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out, cudaStream_t st) {
+  const unsigned grid = div_up(w.S, 256);
+  k_export_rows<<<grid, 256, 0, st>>>(
+      region<int32_t>(ws, w.off_row_of_slot), region<int32_t>(ws, w.off_tile_expert),
+      region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_offsets), out,
+      region<int>(ws, w.off_hdr), (int)w.S);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

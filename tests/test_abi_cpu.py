@@ -1,0 +1,60 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every function that
+include/mm.h declares. Only calls that return before touching the device are made here."""
+import ctypes
+import subprocess
+
+import pytest
+
+from moe_ffn_expert_gb300 import _abi
+from moe_ffn_expert_gb300 import build as mm_build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mm_build.build()
+
+
+def test_exports_every_header_symbol():
+    names = _abi.header_symbols()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(_abi.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    assert set(names) <= exported
+
+
+def test_workspace_size_and_limits():
+    d = _abi.dims(16384, 2048, 768, 128, 8)
+    n = _abi.mm_workspace_size(d)
+    S, S_pad = 16384 * 8, 16384 * 8 + 128 * 127 + 128
+    assert n > S_pad * 2048 * 2 * 3  # x_slot, o, dy_slot at least
+    assert n < 4 * 2 ** 30
+    assert _abi.mm_workspace_size(_abi.dims(16, 60, 32, 4, 2)) == 0      # H not a multiple of 8
+    assert _abi.mm_workspace_size(_abi.dims(16, 64, 36, 4, 2)) == 0      # I not a multiple of 8
+    assert _abi.mm_workspace_size(_abi.dims(16, 64, 32, 1025, 2)) == 0   # E > 1024
+    assert _abi.mm_workspace_size(_abi.dims(16, 64, 32, 4, 17)) == 0     # K > 16
+    assert _abi.mm_workspace_size(_abi.dims(0, 64, 32, 4, 2)) == 0
+    assert _abi.mm_workspace_size(_abi.dims(1, 8, 8, 1, 1)) > 0
+
+
+def test_host_validation_without_device():
+    d = _abi.dims(16, 64, 32, 4, 2)
+    n = _abi.mm_workspace_size(d)
+    # null workspace / too small / null tensors are rejected before any CUDA call
+    assert _abi.mm_forward(d, 0, 0, 0, 0, 0, 0, 0, n, 0, 0) == _abi.MM_ERR_WORKSPACE
+    assert _abi.mm_forward(d, 16, 16, 16, 16, 16, 16, 256, n - 1, 0, 0) == _abi.MM_ERR_WORKSPACE
+    assert _abi.mm_forward(d, 0, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_INVALID_ARG
+    assert _abi.mm_forward(d, 24, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_INVALID_ARG
+    assert _abi.mm_forward(_abi.dims(16, 60, 32, 4, 2), 16, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_UNSUPPORTED
+    assert _abi.mm_backward(d, 0, 16, 16, 16, 16, 16, 256, n, 16, 16, 16, 16, 0, 0) == _abi.MM_ERR_INVALID_ARG
+    assert _abi.mm_get_status(0, 0) == _abi.MM_ERR_WORKSPACE
+    assert _abi.mm_status_string(_abi.MM_ERR_BAD_EXPERT_ID) == "expert id out of range"
+    assert _abi.mm_abi_version() == 1
+
+
+def test_stage_table():
+    names = [_abi._lib().mm_stage_name(i).decode() for i in range(_abi.MM_NUM_STAGES)]
+    assert names[0] == "route_count" and names[-1] == "w1_grad" and len(set(names)) == 14
+    assert _abi.mm_timing_read() == {n: (0.0, 0) for n in names}

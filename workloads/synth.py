@@ -180,19 +180,22 @@ def topk_weights(w: Workload) -> torch.Tensor:
 
 # ----------------------------------------------------------------------------- tensors
 
-def x(w: Workload, device="cpu", rows=None) -> torch.Tensor:
-    """bf16 [T, H] ~ N(0,1); `rows` (a list of token indices) draws only those rows."""
-    key = stream_key(w.seed, STREAM_X)
+def _token_rows(key, w: Workload, device, rows):
     if rows is None:
         return normal_bf16(key, (w.T, w.H), 1.0, device)
+    if isinstance(rows, range) and rows.step == 1:
+        return normal_bf16(key, (len(rows), w.H), 1.0, device, start=rows.start * w.H)
     return torch.stack([normal_bf16(key, (w.H,), 1.0, device, start=int(t) * w.H) for t in rows])
+
+
+def x(w: Workload, device="cpu", rows=None) -> torch.Tensor:
+    """bf16 [T, H] ~ N(0,1); `rows` (token indices) draws only those rows."""
+    return _token_rows(stream_key(w.seed, STREAM_X), w, device, rows)
 
 
 def dy(w: Workload, device="cpu", rows=None) -> torch.Tensor:
-    key = stream_key(w.seed, STREAM_DY)
-    if rows is None:
-        return normal_bf16(key, (w.T, w.H), 1.0, device)
-    return torch.stack([normal_bf16(key, (w.H,), 1.0, device, start=int(t) * w.H) for t in rows])
+    """bf16 [T, H] ~ N(0,1): the upstream gradient of y."""
+    return _token_rows(stream_key(w.seed, STREAM_DY), w, device, rows)
 
 
 def w_up(w: Workload, device="cpu", expert=None) -> torch.Tensor:
