@@ -382,14 +382,22 @@ def _oracle_inputs(w, n_max, device_weights=None):
     return x, ids, tw, dy, wu, wd
 
 
+def _calibrate(w, inp, target_s, n_start=32):
+    """Token count whose oracle fwd+bwd takes about target_s (doubling from n_start)."""
+    n_max = inp[0].shape[0]
+    n = min(n_start, n_max)
+    t = _oracle_tokens(w, n, inp)
+    while t < target_s / 2 and n < n_max:
+        n = min(n_max, int(n * min(8.0, max(2.0, 0.8 * target_s / max(t, 1e-3)))))
+        t = _oracle_tokens(w, n, inp)
+    return n, t
+
+
 def cpu_baseline(w, budget_s=15.0, device_weights=None):
     import torch
     torch.set_num_threads(os.cpu_count() or 1)
-    n0 = min(w.T, 32)
-    inp = _oracle_inputs(w, min(w.T, 4096), device_weights)
-    t0 = _oracle_tokens(w, n0, inp)
-    n = int(max(n0, min(inp[0].shape[0], n0 * budget_s / max(t0, 1e-3))))
-    t = _oracle_tokens(w, n, inp) if n != n0 else t0
+    inp = _oracle_inputs(w, w.T, device_weights)
+    n, t = _calibrate(w, inp, budget_s)
     return {"value": round(n / t, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
             "kind": "oracle",
             "sample": f"float64 oracle fwd+bwd of the first {n} tokens of {w.name} "
@@ -405,11 +413,9 @@ def run_reference(args):
     from workloads import synth
     torch.set_num_threads(os.cpu_count() or 1)
     w = synth.BY_NAME[args.workload]
-    inp = _oracle_inputs(w, min(w.T, 2048))
-    n0 = min(w.T, 16)
-    t0 = _oracle_tokens(w, n0, inp)
-    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
-    n = int(max(1, min(inp[0].shape[0], n0 * per_step_budget / max(t0, 1e-3))))
+    inp = _oracle_inputs(w, w.T)
+    per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    n, _ = _calibrate(w, inp, per_step_budget, n_start=8)
     for _ in range(args.warmup):
         _oracle_tokens(w, n, inp)
     total = 0.0
@@ -438,7 +444,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="qwen")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])

@@ -118,11 +118,13 @@ bool plan_workspace(const mm_dims& d, Workspace* w) {
   p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
   p.off_w_row = take((size_t)p.S_pad * sizeof(float));
   p.off_x_slot = take((size_t)p.S_pad * d.H * 2);
-  p.off_gu = take((size_t)p.S_pad * 2 * d.I * 2);
+  p.off_gu = take((size_t)p.S_pad * 2 * d.I * 4);
   p.off_h = take((size_t)p.S_pad * d.I * 2);
+  p.off_hw_lo = take((size_t)p.S_pad * d.I * 2);
   p.off_o = take((size_t)p.S_pad * d.H * 2);
   p.off_dy_slot = take((size_t)p.S_pad * d.H * 2);
   p.off_dgu = take((size_t)p.S_pad * 2 * d.I * 2);
+  p.off_dgu_lo = take((size_t)p.S_pad * 2 * d.I * 2);
   p.off_p_part = take((size_t)p.n_act_tiles * p.S_pad * sizeof(float));
   p.total = off;
   *w = p;

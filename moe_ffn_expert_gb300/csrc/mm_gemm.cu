@@ -12,6 +12,15 @@
 //   W2_GRAD      hw_e^T [I,M_e]   M-maj   dy_slot_e [M_e,H] N-major    dW_down[e] (bf16)
 //   W1_GRAD      x_slot_e^T[H,M_e] M-maj  dgu_e [M_e,2I]    N-major    dW_up[e] (bf16)
 //
+// Precision of the weight gradients. They reduce over all rows of an expert (hundreds to
+// thousands), so a bf16 rounding of every row of an operand would leave errors of ~0.5% of the
+// gradient's rms. The forward therefore keeps the gate|up accumulators in fp32, and the
+// act_grad epilogue writes w*h and [d_gate|d_up] as two bf16 planes, hi = bf16(v) and
+// lo = bf16(v - hi), which together carry ~16 mantissa bits. W2_GRAD issues two MMAs per
+// k-step (hw_hi and hw_lo against the same dy tile), W1_GRAD two (x against dgu_hi and dgu_lo),
+// both accumulating into one fp32 accumulator; their column tiles are 128 wide so every
+// stage still holds 48 KB.
+//
 // Row-grouped kinds walk 128-row tiles of the expert-sorted (padded) row buffers; each tile
 // belongs to one expert, whose weight slab is the third coordinate of a 3-D tensor map.
 // Weight-gradient kinds walk (expert, row tile, column tile) of the weight, reducing over
@@ -20,8 +29,8 @@
 // Warp roles (192 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
 //   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring (mbarrier per
 //               stage, transaction-count completion);
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators); one thread issues
-//               tcgen05.mma (128x256x16 per instruction) and tcgen05.commit's the stage and
+//   warp 1      allocates 2*BN TMEM columns (two 128xBN fp32 accumulators); one thread issues
+//               tcgen05.mma (128xBNx16 per instruction) and tcgen05.commit's the stage and
 //               accumulator barriers;
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
 //               i.e. one tile row per thread), apply the kind's epilogue, store to global memory,
@@ -39,12 +48,10 @@ namespace mm {
 namespace {
 
 constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGE_BYTES = 48 * 1024;       // every kind: A (+A lo) and B (+B lo) tiles
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile: 8 KB
 constexpr int NUM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -62,11 +69,13 @@ struct Args {
   int N;           // valid output columns
   int M;           // weight-gradient kinds: valid output rows
   int I;           // intermediate size
-  __nv_bfloat16* out0;
+  void* out0;  // bf16, except fp32 gate|up of GEMM1
   int64_t ld0;
   __nv_bfloat16* out1;
   int64_t ld1;
-  const __nv_bfloat16* gu;
+  __nv_bfloat16* out2;  // lo planes of the act_grad epilogue
+  __nv_bfloat16* out3;
+  const float* gu;
   int64_t ld_gu;
   const float* w_row;
   float* p_part;
@@ -81,7 +90,17 @@ struct Traits {
   static constexpr bool A_MN = WGRAD;
   static constexpr bool B_MN =
       (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+  static constexpr bool A_SPLIT = (KIND == GK_W2_GRAD);  // hw_hi + hw_lo
+  static constexpr bool B_SPLIT = (KIND == GK_W1_GRAD);  // dgu_hi + dgu_lo
+  static constexpr int TN = WGRAD ? 128 : BN;            // accumulator columns per tile
+  static constexpr int B_BYTES = TN * BK * 2;
+  static constexpr int A_LO_OFF = A_BYTES;                                   // if A_SPLIT
+  static constexpr int B_OFF = A_BYTES * (A_SPLIT ? 2 : 1);
+  static constexpr int B_LO_OFF = B_OFF + B_BYTES;                           // if B_SPLIT
+  static constexpr int USED = B_OFF + B_BYTES * (B_SPLIT ? 2 : 1);
+  static constexpr uint32_t TMEM_COLS = 2 * TN;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+  static_assert(USED == STAGE_BYTES, "stage layout");
 };
 
 struct Tile {
@@ -98,7 +117,7 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
     const int mt = rem / a.n_tiles_n;
     const int nt = rem - mt * a.n_tiles_n;
     t.m0 = mt * BM;
-    t.n0 = nt * BN;
+    t.n0 = nt * Traits<KIND>::TN;
     t.row0 = __ldg(a.poff + t.e);
     t.kiters = (__ldg(a.poff + t.e + 1) - t.row0) / BK;
   } else {
@@ -111,6 +130,28 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
     t.kiters = a.k_iters;
   }
   return t;
+}
+
+__device__ __forceinline__ void store_row_f32(float* dst, const float* v, int n, int N) {
+  // 32 consecutive fp32 columns starting at n, masked in groups of 8
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (n + 8 * g < N) {
+      *reinterpret_cast<float4*>(dst + n + 8 * g) =
+          make_float4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
+      *reinterpret_cast<float4*>(dst + n + 8 * g + 4) =
+          make_float4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
+    }
+  }
+}
+
+// hi = bf16(v), lo = bf16(v - hi)
+__device__ __forceinline__ void split_bf16(const float* v, float* hi, float* lo) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+    lo[j] = v[j] - hi[j];
+  }
 }
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, int N) {
@@ -133,7 +174,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
   if constexpr (KIND == GK_GEMM1_SWIGLU) {
     // accumulator columns [0,128) = gate columns n0.., [128,256) = up columns n0..
     const int64_t row = (int64_t)t.m0 + r;
-    __nv_bfloat16* gu = a.out0 + row * a.ld0;
+    float* gu = reinterpret_cast<float*>(a.out0) + row * a.ld0;
     __nv_bfloat16* hh = a.out1 + row * a.ld1;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -149,13 +190,13 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
         u[j] = __uint_as_float(ub[j]);
         h[j] = g[j] * sigmoidf_(g[j]) * u[j];
       }
-      store_row_bf16(gu, g, n, a.I);
-      store_row_bf16(gu + a.I, u, n, a.I);
+      store_row_f32(gu, g, n, a.I);
+      store_row_f32(gu + a.I, u, n, a.I);
       store_row_bf16(hh, h, n, a.I);
     }
   } else if constexpr (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD) {
     const int64_t row = (int64_t)t.m0 + r;
-    __nv_bfloat16* o = a.out0 + row * a.ld0;
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) + row * a.ld0;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t v[32];
@@ -167,11 +208,13 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
       store_row_bf16(o, f, t.n0 + c * 32, a.N);
     }
   } else if constexpr (KIND == GK_ACT_GRAD) {
-    // g = dy_slot . W_down^T for columns n0.. of I; recompute SwiGLU from the saved gate|up.
+    // g = dy_slot . W_down^T for columns n0.. of I; SwiGLU backward from the saved fp32 gate|up.
     const int64_t row = (int64_t)t.m0 + r;
-    const __nv_bfloat16* gu = a.gu + row * a.ld_gu;
-    __nv_bfloat16* dgu = a.out0 + row * a.ld0;
+    const float* gu = a.gu + row * a.ld_gu;
+    __nv_bfloat16* dgu = reinterpret_cast<__nv_bfloat16*>(a.out0) + row * a.ld0;
+    __nv_bfloat16* dgu_lo = a.out2 + row * a.ld0;
     __nv_bfloat16* hw = a.out1 + row * a.ld1;
+    __nv_bfloat16* hw_lo = a.out3 + row * a.ld1;
     const float w = __ldg(a.w_row + row);
     float p = 0.f;
 #pragma unroll 1
@@ -184,22 +227,28 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
       float da[32], db[32], hv[32];
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
-        uint4 av = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
-        if (n + 8 * g8 < a.I) {
-          av = *reinterpret_cast<const uint4*>(gu + n + 8 * g8);
-          bv = *reinterpret_cast<const uint4*>(gu + a.I + n + 8 * g8);
+        const bool valid = (n + 8 * g8 < a.I);
+        float av[8], bv[8];
+        if (valid) {
+          const float4 a0 = *reinterpret_cast<const float4*>(gu + n + 8 * g8);
+          const float4 a1 = *reinterpret_cast<const float4*>(gu + n + 8 * g8 + 4);
+          const float4 b0 = *reinterpret_cast<const float4*>(gu + a.I + n + 8 * g8);
+          const float4 b1 = *reinterpret_cast<const float4*>(gu + a.I + n + 8 * g8 + 4);
+          av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+          av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+          bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+          bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) av[j] = bv[j] = 0.f;
         }
-        const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float ga = (j & 1) ? bf16_hi(aw[j >> 1]) : bf16_lo(aw[j >> 1]);
-          const float ub = (j & 1) ? bf16_hi(bw[j >> 1]) : bf16_lo(bw[j >> 1]);
+          const float ga = av[j], ub = bv[j];
           const float gv = __uint_as_float(v[8 * g8 + j]);
           const float sg = sigmoidf_(ga);
           const float sl = ga * sg;
           const float h = sl * ub;
-          const bool valid = (n + 8 * g8 < a.I);
           p += valid ? gv * h : 0.f;
           const float dh = w * gv;
           da[8 * g8 + j] = dh * ub * sg * (1.0f + ga * (1.0f - sg));
@@ -207,17 +256,25 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
           hv[8 * g8 + j] = w * h;
         }
       }
-      store_row_bf16(dgu, da, n, a.I);
-      store_row_bf16(dgu + a.I, db, n, a.I);
-      store_row_bf16(hw, hv, n, a.I);
+      float hi[32], lo[32];
+      split_bf16(da, hi, lo);
+      store_row_bf16(dgu, hi, n, a.I);
+      store_row_bf16(dgu_lo, lo, n, a.I);
+      split_bf16(db, hi, lo);
+      store_row_bf16(dgu + a.I, hi, n, a.I);
+      store_row_bf16(dgu_lo + a.I, lo, n, a.I);
+      split_bf16(hv, hi, lo);
+      store_row_bf16(hw, hi, n, a.I);
+      store_row_bf16(hw_lo, lo, n, a.I);
     }
     a.p_part[(int64_t)(t.n0 / BN) * a.S_pad + row] = p;
   } else {  // weight gradients (every lane runs the TMEM loads; rows past M store nothing)
     const int m = t.m0 + r;
     const bool row_ok = m < a.M;
-    __nv_bfloat16* o = a.out0 + (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
+                       (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < Traits<KIND>::TN / 32; ++c) {
       uint32_t v[32];
       tmem_ld_32x32(tacc + c * 32, v);
       tmem_ld_wait();
@@ -233,17 +290,18 @@ template <int KIND>
 __device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r) {
   const int m = t.m0 + r;
   if (m >= a.M) return;
-  __nv_bfloat16* o = a.out0 + (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
+                     (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
   float z[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) z[j] = 0.f;
-  for (int c = 0; c < BN / 32; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
+  for (int c = 0; c < Traits<KIND>::TN / 32; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-           const Args a) {
+           const __grid_constant__ CUtensorMap tmL, const Args a) {
   using TR = Traits<KIND>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform)
@@ -275,9 +333,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (TR::A_SPLIT || TR::B_SPLIT) tma_prefetch_desc(&tmL);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_alloc(tmem_holder, TR::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -299,12 +358,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + TR::B_OFF;
           mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
           const int k0 = kb * BK;
           if constexpr (TR::A_MN) {
             tma_load_2d(sa, &tmA, full_bar(s), t.m0, t.row0 + k0);
             tma_load_2d(sa + MN_BLOCK_BYTES, &tmA, full_bar(s), t.m0 + 64, t.row0 + k0);
+            if constexpr (TR::A_SPLIT) {
+              tma_load_2d(sa + TR::A_LO_OFF, &tmL, full_bar(s), t.m0, t.row0 + k0);
+              tma_load_2d(sa + TR::A_LO_OFF + MN_BLOCK_BYTES, &tmL, full_bar(s), t.m0 + 64,
+                          t.row0 + k0);
+            }
           } else {
             tma_load_2d(sa, &tmA, full_bar(s), k0, t.m0);
           }
@@ -321,8 +385,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_3d(sb, &tmB, full_bar(s), k0, t.n0, t.e);
           } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < TR::TN / 64; ++j)
               tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, t.row0 + k0);
+            if constexpr (TR::B_SPLIT) {
+#pragma unroll
+              for (int j = 0; j < TR::TN / 64; ++j)
+                tma_load_2d(sa + TR::B_LO_OFF + j * MN_BLOCK_BYTES, &tmL, full_bar(s),
+                            t.n0 + 64 * j, t.row0 + k0);
+            }
           }
         }
       }
@@ -340,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t d = tmem_base + buf * TR::TN;
         for (int kb = 0; kb < t.kiters; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(full_bar(s), ph, tmo)) {
@@ -349,14 +419,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+          const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + TR::B_OFF;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = TR::A_MN ? sdesc_sw128(sa + kk * 2048, MN_BLOCK_BYTES, 1024)
-                                         : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = TR::B_MN ? sdesc_sw128(sb + kk * 2048, MN_BLOCK_BYTES, 1024)
-                                         : sdesc_sw128(sb + kk * 32, 16, 1024);
+            // k-step offsets: 16 elements = 32 B along a K-major row, 16 k-rows = 2 KB MN-major
+            const uint32_t ka = TR::A_MN ? kk * 2048 : kk * 32;
+            const uint32_t kbo = TR::B_MN ? kk * 2048 : kk * 32;
+            const uint32_t lbo_a = TR::A_MN ? MN_BLOCK_BYTES : 16;
+            const uint32_t lbo_b = TR::B_MN ? MN_BLOCK_BYTES : 16;
+            const uint64_t ad = sdesc_sw128(sa + ka, lbo_a, 1024);
+            const uint64_t bd = sdesc_sw128(sb + kbo, lbo_b, 1024);
             umma_bf16(d, ad, bd, TR::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (TR::A_SPLIT)
+              umma_bf16(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, TR::IDESC, 1u);
+            if constexpr (TR::B_SPLIT)
+              umma_bf16(d, ad, sdesc_sw128(sa + TR::B_LO_OFF + kbo, lbo_b, 1024), TR::IDESC, 1u);
           }
           umma_commit(empty_bar(s));
         }
@@ -385,7 +462,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
       tc_fence_after();
-      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+      const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
       epilogue_tile<KIND>(a, t, tacc, r);
       tc_fence_before();
       __syncwarp();
@@ -399,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, TR::TMEM_COLS);
   }
 }
 
@@ -500,8 +577,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.S_pad = S_pad;
   a.timeout_ns = c.timeout_ns;
 
-  CUtensorMap ta, tb;
-  bool ok = true;
+  CUtensorMap ta, tb, tl;
+  bool ok = true, has_lo = false;
   int64_t tiles_max = 0;
   const int64_t m_tiles_max = S_pad / BM;
   switch (KIND) {
@@ -511,7 +588,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.n_tiles_n = cdiv(I, BN / 2);
       a.k_iters = cdiv(H, BK);
       a.N = (int)I;
-      a.out0 = bf(w.off_gu);
+      a.out0 = ws + w.off_gu;  // fp32
       a.ld0 = 2 * I;
       a.out1 = bf(w.off_h);
       a.ld1 = I;
@@ -534,10 +611,12 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.k_iters = cdiv(H, BK);
       a.N = (int)I;
       a.out0 = bf(w.off_dgu);
+      a.out2 = bf(w.off_dgu_lo);
       a.ld0 = 2 * I;
-      a.out1 = bf(w.off_h);  // hw = w * h reuses the forward's h buffer
+      a.out1 = bf(w.off_h);  // hi part of w*h reuses the forward's h buffer
+      a.out3 = bf(w.off_hw_lo);
       a.ld1 = I;
-      a.gu = bf(w.off_gu);
+      a.gu = reinterpret_cast<const float*>(ws + w.off_gu);
       a.ld_gu = 2 * I;
       a.w_row = reinterpret_cast<const float*>(ws + w.off_w_row);
       a.p_part = reinterpret_cast<float*>(ws + w.off_p_part);
@@ -555,9 +634,11 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       break;
     case GK_W2_GRAD:
       ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, 64) &&
+           map_rows(&tl, ws + w.off_hw_lo, I, S_pad, 64, 64) &&
            map_rows(&tb, ws + w.off_dy_slot, H, S_pad, 64, 64);
+      has_lo = true;
       a.m_tiles_w = cdiv(I, BM);
-      a.n_tiles_n = cdiv(H, BN);
+      a.n_tiles_n = cdiv(H, Traits<GK_W2_GRAD>::TN);
       a.M = (int)I;
       a.N = (int)H;
       a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
@@ -567,9 +648,11 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       break;
     case GK_W1_GRAD:
       ok = map_rows(&ta, ws + w.off_x_slot, H, S_pad, 64, 64) &&
-           map_rows(&tb, ws + w.off_dgu, 2 * I, S_pad, 64, 64);
+           map_rows(&tb, ws + w.off_dgu, 2 * I, S_pad, 64, 64) &&
+           map_rows(&tl, ws + w.off_dgu_lo, 2 * I, S_pad, 64, 64);
+      has_lo = true;
       a.m_tiles_w = cdiv(H, BM);
-      a.n_tiles_n = cdiv(2 * I, BN);
+      a.n_tiles_n = cdiv(2 * I, Traits<GK_W1_GRAD>::TN);
       a.M = (int)H;
       a.N = (int)(2 * I);
       a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
@@ -579,8 +662,9 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
+  if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
-  k_gemm<KIND><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, a);
+  k_gemm<KIND><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tl, a);
   return cudaGetLastError();
 }
 

@@ -54,7 +54,15 @@ struct Workspace {
   int64_t n_act_tiles;  // act_grad column tiles (ceil(I / BN)) = rows of the d_topk partials
   size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
-  size_t off_x_slot, off_gu, off_h, off_o, off_dy_slot, off_dgu, off_p_part;
+  size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
+  size_t off_gu;       // fp32 [S_pad, 2I]  gate|up accumulators (kept for the backward)
+  size_t off_h;        // bf16 [S_pad, I]   forward: h;  backward: hi part of w*h
+  size_t off_hw_lo;    // bf16 [S_pad, I]   backward: lo part of w*h
+  size_t off_o;        // bf16 [S_pad, H]   forward: o;  backward: dx rows
+  size_t off_dy_slot;  // bf16 [S_pad, H]   dispatched dy rows
+  size_t off_dgu;      // bf16 [S_pad, 2I]  hi part of [d_gate | d_up]
+  size_t off_dgu_lo;   // bf16 [S_pad, 2I]  lo part of [d_gate | d_up]
+  size_t off_p_part;   // fp32 [ceil(I/BN), S_pad] per-column-tile partials of <g, h>
   size_t total;
 };
 
