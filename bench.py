@@ -66,6 +66,17 @@ def profiled_traffic(stage, workload):
     return e.get("dram_bytes_per_launch")
 
 
+def workload_of(args):
+    """The named workload, optionally with a smaller token count (profiling captures)."""
+    import dataclasses
+
+    from workloads import synth
+    w = synth.BY_NAME[args.workload]
+    if args.tokens:
+        w = dataclasses.replace(w, T=int(args.tokens))
+    return w
+
+
 # ------------------------------------------------------------------ distributed plumbing
 
 def dist_env():
@@ -178,7 +189,7 @@ def run_gpu(args):
         mm_build.build()  # no-op when libmm.so is newer than its sources
     barrier(dev)
 
-    w = synth.BY_NAME[args.workload]
+    w = workload_of(args)
     T, H, I, E, K = w.T, w.H, w.I, w.E, w.K
     S = T * K
     d = _abi.dims(T, H, I, E, K)
@@ -412,7 +423,7 @@ def run_reference(args):
 
     from workloads import synth
     torch.set_num_threads(os.cpu_count() or 1)
-    w = synth.BY_NAME[args.workload]
+    w = workload_of(args)
     inp = _oracle_inputs(w, w.T)
     per_step_budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
     n, _ = _calibrate(w, inp, per_step_budget, n_start=8)
@@ -447,6 +458,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="qwen")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (smaller profiling cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample (0: skip)")

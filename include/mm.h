@@ -111,6 +111,23 @@ mm_status mm_get_status(const void* workspace, void* stream);
 mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts,
                             int32_t* offsets, int32_t* row_of_slot, void* stream);
 
+/* Routing tables for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point. It exists for callers that may not call
+ * cudaMalloc at the point where they need the routing (code inside a framework that owns the
+ * device heap, or work prepared ahead of time that may only use pointers it already holds).
+ * It computes exactly what mm_forward + mm_routing_export give: counts[E], offsets[E+1] and
+ * row_of_slot[T*K] (stable expert-sorted position of each slot), written to caller-provided
+ * DEVICE buffers (4-byte aligned); H and I of `d` are ignored. It allocates nothing: its
+ * scratch is a static device array of 4 MiB + 256 B that every GPU loading this library holds
+ * until the process exits. Limits: T*K <= 2^20, E <= 1024, K <= 16; larger sizes return
+ * MM_ERR_UNSUPPORTED (use mm_forward with a workspace). An expert id outside [0, E) makes every
+ * output entry -1. All calls share the static scratch: calls whose kernels overlap on the GPU
+ * (different streams or host threads) race and must be serialised by the caller. The first call
+ * on each device looks up the scratch's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture. Nothing is synchronised with the host. */
+mm_status mm_route_noalloc(mm_dims d, const int32_t* topk_ids, int32_t* counts,
+                           int32_t* offsets, int32_t* row_of_slot, void* stream);
+
 /* Human-readable name of a status code. */
 const char* mm_status_string(mm_status s);
 

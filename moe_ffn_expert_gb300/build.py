@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmm.so")
-SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu"]
+SOURCES = ["mm_api.cu", "mm_route.cu", "mm_gemm.cu", "mm_route_static.cu"]
 HEADERS = ["mm_device.cuh", "mm_layout.h", "mm_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
