@@ -101,7 +101,7 @@ bool plan_workspace(const mm_dims& d, Workspace* w) {
   const int64_t nonempty = std::min<int64_t>(d.E, p.S);
   p.S_pad = (p.S + nonempty * (BM - 1) + BM - 1) / BM * BM;
   p.n_chunks = (p.S + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
-  p.n_act_tiles = (d.I + BN - 1) / BN;
+  p.n_act_tiles = 2 * ((d.I + BN - 1) / BN);  // two column halves per act_grad tile
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;

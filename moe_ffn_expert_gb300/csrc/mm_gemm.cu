@@ -26,14 +26,15 @@
 // Weight-gradient kinds walk (expert, row tile, column tile) of the weight, reducing over
 // the expert's padded rows (pad rows are zero, an expert with no rows gets a zero tile).
 //
-// Warp roles (192 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
+// Warp roles (320 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
 //   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring (mbarrier per
 //               stage, transaction-count completion);
 //   warp 1      allocates 2*BN TMEM columns (two 128xBN fp32 accumulators); one thread issues
 //               tcgen05.mma (128xBNx16 per instruction) and tcgen05.commit's the stage and
 //               accumulator barriers;
-//   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
-//               i.e. one tile row per thread), apply the kind's epilogue, store to global memory,
+//   warps 2-9   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
+//               i.e. one tile row per thread; warps w and w+4 take one column half each), apply
+//               the kind's epilogue, store to global memory,
 //               release the accumulator so the next tile's MMAs overlap this epilogue.
 // All operand tiles use the 128-byte swizzle; every mbarrier wait is bounded by %globaltimer and
 // a wait that runs out records MM_ERR_TIMEOUT, stops the role and still frees TMEM.
@@ -47,14 +48,21 @@
 namespace mm {
 namespace {
 
-constexpr int STAGES = 4;
 constexpr int STAGE_BYTES = 48 * 1024;       // every kind: A (+A lo) and B (+B lo) tiles
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile: 8 KB
-constexpr int NUM_THREADS = 192;
-constexpr int BAR_BYTES = 256;
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr int NUM_EPI_WARPS = 8;             // two per TMEM lane quarter, one per column half
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int BAR_BYTES = 512;
+constexpr int GU_CHUNK_BYTES = 2 * 32 * 16 * 4;  // act_grad: 32 rows x 16 fp32 of gate and of up
+constexpr int OUT_PLANE_BYTES = 32 * 16 * 2;     // act_grad: 32 rows x 16 bf16 of one output plane
+constexpr int OUT_CHUNK_BYTES = 6 * OUT_PLANE_BYTES;  // d_gate, d_up, w*h; hi and lo each
+
+// Store maps of the act_grad epilogue: [d_gate|d_up] hi and lo as [rows][2][I] (so a store
+// never crosses from the gate half into the up half), w*h hi and lo as [rows][I].
+struct alignas(64) EpiMaps {
+  CUtensorMap dgu_hi, dgu_lo, hw_hi, hw_lo;
+};
 static_assert(BK == 64, "one 128-byte swizzle row per k-block");
 
 struct Args {
@@ -101,6 +109,15 @@ struct Traits {
   static constexpr uint32_t TMEM_COLS = 2 * TN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN, A_MN ? 1 : 0, B_MN ? 1 : 0);
   static_assert(USED == STAGE_BYTES, "stage layout");
+  static_assert(!A_SPLIT || A_LO_OFF + A_BYTES == B_OFF, "A lo plane layout");
+  static_assert(!B_SPLIT || B_LO_OFF + B_BYTES == USED, "B lo plane layout");
+  // act_grad trades one mainloop stage for per-warp staging of its gate|up input and of its
+  // six output planes (TMA in, TMA out)
+  static constexpr bool GU_STAGING = (KIND == GK_ACT_GRAD);
+  static constexpr int STAGES = GU_STAGING ? 3 : 4;
+  static constexpr int EPI_BYTES = GU_STAGING ? NUM_EPI_WARPS * (GU_CHUNK_BYTES + OUT_CHUNK_BYTES) : 0;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct Tile {
@@ -145,15 +162,6 @@ __device__ __forceinline__ void store_row_f32(float* dst, const float* v, int n,
   }
 }
 
-// hi = bf16(v), lo = bf16(v - hi)
-__device__ __forceinline__ void split_bf16(const float* v, float* hi, float* lo) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
-    lo[j] = v[j] - hi[j];
-  }
-}
-
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, int N) {
   // 32 consecutive columns starting at n, masked in groups of 8 (N is a multiple of 8)
 #pragma unroll
@@ -169,15 +177,39 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
   }
 }
 
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 q;
+  q.x = pack_bf16(v[0], v[1]);
+  q.y = pack_bf16(v[2], v[3]);
+  q.z = pack_bf16(v[4], v[5]);
+  q.w = pack_bf16(v[6], v[7]);
+  return q;
+}
+
+// hi = bf16(v), lo = bf16(v - hi), 8 values each packed into one 16-byte word.
+__device__ __forceinline__ void split8_bf16(const float* v, uint4& hi, uint4& lo) {
+  float h[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+    l[j] = v[j] - h[j];
+  }
+  hi = pack8_bf16(h);
+  lo = pack8_bf16(l);
+}
+
+// One epilogue warp drains 32 TMEM lanes (tile rows r = 32*q + lane) over half `hf` of the
+// tile's columns.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint32_t tacc, int r) {
+__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint32_t tacc, int r,
+                                              int hf) {
   if constexpr (KIND == GK_GEMM1_SWIGLU) {
     // accumulator columns [0,128) = gate columns n0.., [128,256) = up columns n0..
     const int64_t row = (int64_t)t.m0 + r;
     float* gu = reinterpret_cast<float*>(a.out0) + row * a.ld0;
     __nv_bfloat16* hh = a.out1 + row * a.ld1;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
       uint32_t ga[32], ub[32];
       tmem_ld_32x32(tacc + c * 32, ga);
       tmem_ld_32x32(tacc + 128 + c * 32, ub);
@@ -197,8 +229,9 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
   } else if constexpr (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD) {
     const int64_t row = (int64_t)t.m0 + r;
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) + row * a.ld0;
+    constexpr int NC = BN / 64;  // 32-column chunks per half
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = hf * NC; c < hf * NC + NC; ++c) {
       uint32_t v[32];
       tmem_ld_32x32(tacc + c * 32, v);
       tmem_ld_wait();
@@ -207,74 +240,15 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
       for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
       store_row_bf16(o, f, t.n0 + c * 32, a.N);
     }
-  } else if constexpr (KIND == GK_ACT_GRAD) {
-    // g = dy_slot . W_down^T for columns n0.. of I; SwiGLU backward from the saved fp32 gate|up.
-    const int64_t row = (int64_t)t.m0 + r;
-    const float* gu = a.gu + row * a.ld_gu;
-    __nv_bfloat16* dgu = reinterpret_cast<__nv_bfloat16*>(a.out0) + row * a.ld0;
-    __nv_bfloat16* dgu_lo = a.out2 + row * a.ld0;
-    __nv_bfloat16* hw = a.out1 + row * a.ld1;
-    __nv_bfloat16* hw_lo = a.out3 + row * a.ld1;
-    const float w = __ldg(a.w_row + row);
-    float p = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      const int n = t.n0 + c * 32;
-      if (n >= a.I) break;
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + c * 32, v);
-      tmem_ld_wait();
-      float da[32], db[32], hv[32];
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const bool valid = (n + 8 * g8 < a.I);
-        float av[8], bv[8];
-        if (valid) {
-          const float4 a0 = *reinterpret_cast<const float4*>(gu + n + 8 * g8);
-          const float4 a1 = *reinterpret_cast<const float4*>(gu + n + 8 * g8 + 4);
-          const float4 b0 = *reinterpret_cast<const float4*>(gu + a.I + n + 8 * g8);
-          const float4 b1 = *reinterpret_cast<const float4*>(gu + a.I + n + 8 * g8 + 4);
-          av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
-          av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-          bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
-          bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) av[j] = bv[j] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float ga = av[j], ub = bv[j];
-          const float gv = __uint_as_float(v[8 * g8 + j]);
-          const float sg = sigmoidf_(ga);
-          const float sl = ga * sg;
-          const float h = sl * ub;
-          p += valid ? gv * h : 0.f;
-          const float dh = w * gv;
-          da[8 * g8 + j] = dh * ub * sg * (1.0f + ga * (1.0f - sg));
-          db[8 * g8 + j] = dh * sl;
-          hv[8 * g8 + j] = w * h;
-        }
-      }
-      float hi[32], lo[32];
-      split_bf16(da, hi, lo);
-      store_row_bf16(dgu, hi, n, a.I);
-      store_row_bf16(dgu_lo, lo, n, a.I);
-      split_bf16(db, hi, lo);
-      store_row_bf16(dgu + a.I, hi, n, a.I);
-      store_row_bf16(dgu_lo + a.I, lo, n, a.I);
-      split_bf16(hv, hi, lo);
-      store_row_bf16(hw, hi, n, a.I);
-      store_row_bf16(hw_lo, lo, n, a.I);
-    }
-    a.p_part[(int64_t)(t.n0 / BN) * a.S_pad + row] = p;
-  } else {  // weight gradients (every lane runs the TMEM loads; rows past M store nothing)
+  } else if constexpr (Traits<KIND>::WGRAD) {
+    // every lane runs the TMEM loads; rows past M store nothing
     const int m = t.m0 + r;
     const bool row_ok = m < a.M;
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
                        (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+    constexpr int NC = Traits<KIND>::TN / 64;
 #pragma unroll 1
-    for (int c = 0; c < Traits<KIND>::TN / 32; ++c) {
+    for (int c = hf * NC; c < hf * NC + NC; ++c) {
       uint32_t v[32];
       tmem_ld_32x32(tacc + c * 32, v);
       tmem_ld_wait();
@@ -287,7 +261,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint
 }
 
 template <int KIND>
-__device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r) {
+__device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r, int hf) {
   const int m = t.m0 + r;
   if (m >= a.M) return;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
@@ -295,25 +269,189 @@ __device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, in
   float z[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) z[j] = 0.f;
-  for (int c = 0; c < Traits<KIND>::TN / 32; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
+  constexpr int NC = Traits<KIND>::TN / 64;
+  for (int c = hf * NC; c < hf * NC + NC; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
+}
+
+// SwiGLU backward of one 16-column chunk of one row: g from TMEM, gate (cur[0..3]) and up
+// (cur[4..7]) from the staged fp32 values. Writes this row of the six output planes (d_gate,
+// d_up, w*h; hi and lo each) into the warp's staging planes (32 rows x 32 bytes, 32-byte
+// swizzle: 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)) and accumulates <g, h>.
+__device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cur)[8], float w,
+                                               float& p, uint8_t* out_row, int lane) {
+  uint32_t v[16];
+  tmem_ld_32x16(taddr, v);
+  tmem_ld_wait();
+  const int swz = (lane >> 2) & 1;
+#pragma unroll
+  for (int g8 = 0; g8 < 2; ++g8) {
+    const float4 a0 = cur[2 * g8], a1 = cur[2 * g8 + 1];
+    const float4 b0 = cur[4 + 2 * g8], b1 = cur[4 + 2 * g8 + 1];
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    float da[8], db[8], hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float ga = av[j], ub = bv[j];
+      const float gv = __uint_as_float(v[8 * g8 + j]);
+      const float sg = sigmoidf_(ga);
+      const float sl = ga * sg;
+      const float h = sl * ub;
+      p += gv * h;  // columns past I carry ga = ub = 0, so h = 0
+      const float dh = w * gv;
+      da[j] = dh * ub * sg * (1.0f + ga * (1.0f - sg));
+      db[j] = dh * sl;
+      hv[j] = w * h;
+    }
+    uint8_t* o = out_row + ((g8 ^ swz) << 4);
+    uint4 hi, lo;
+    split8_bf16(da, hi, lo);
+    *reinterpret_cast<uint4*>(o + 0 * OUT_PLANE_BYTES) = hi;
+    *reinterpret_cast<uint4*>(o + 2 * OUT_PLANE_BYTES) = lo;
+    split8_bf16(db, hi, lo);
+    *reinterpret_cast<uint4*>(o + 1 * OUT_PLANE_BYTES) = hi;
+    *reinterpret_cast<uint4*>(o + 3 * OUT_PLANE_BYTES) = lo;
+    split8_bf16(hv, hi, lo);
+    *reinterpret_cast<uint4*>(o + 4 * OUT_PLANE_BYTES) = hi;
+    *reinterpret_cast<uint4*>(o + 5 * OUT_PLANE_BYTES) = lo;
+  }
+}
+
+// act_grad epilogue of one warp: g = dy_slot W_down^T (from TMEM) and the SwiGLU backward.
+// The warp streams the (tile, 16-column chunk) pairs of its 32 rows and column half. Input:
+// lane 0 TMA-loads the fp32 gate and up values of a chunk (two 32x16 boxes, 64-byte swizzle)
+// into the warp's staging buffer, and issues the next chunk's load as soon as the warp has read
+// the current one. Output: the warp writes the chunk's six 32x16 bf16 planes to its output
+// staging buffer and lane 0 stores them with TMA (the tensor maps clip columns past I).
+__device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorMap* tm_gu,
+                                                  const EpiMaps* em, int total, uint32_t tmem_base,
+                                                  uint32_t accf0, uint32_t accf1, uint32_t acce0,
+                                                  uint32_t acce1, uint32_t gbar, uint32_t gbuf,
+                                                  const uint8_t* gbuf_ptr, uint32_t obuf,
+                                                  uint8_t* obuf_ptr, int warp, int lane) {
+  constexpr int KIND = GK_ACT_GRAD;
+  constexpr int NC = BN / 32;      // 16-column chunks per column half
+  const int q = warp & 3;          // TMEM lane quarter = rows 32q..32q+31 of the tile
+  const int hf = (warp - 2) >> 2;  // column half
+  const int c0 = hf * NC;
+  const uint64_t tmo = a.timeout_ns;
+  auto chunk_end = [&](int n0) {   // chunks entirely past I are skipped
+    int ce = c0 + NC;
+    while (ce > c0 && n0 + (ce - 1) * 16 >= a.I) --ce;
+    return ce;
+  };
+  int ld_tile = blockIdx.x, ld_c = c0;  // next (tile, chunk) to load
+  auto issue_next = [&]() {
+    while (ld_tile < total && ld_c >= chunk_end(decode_tile<KIND>(a, ld_tile).n0)) {
+      ld_tile += gridDim.x;
+      ld_c = c0;
+    }
+    if (ld_tile >= total) return;
+    if (lane == 0) {
+      const Tile tn = decode_tile<KIND>(a, ld_tile);
+      fence_proxy_async_smem();  // the buffer's previous contents were read by the warp
+      mbar_arrive_expect_tx(gbar, GU_CHUNK_BYTES);
+      tma_load_2d(gbuf, tm_gu, gbar, tn.n0 + ld_c * 16, tn.m0 + q * 32);
+      tma_load_2d(gbuf + GU_CHUNK_BYTES / 2, tm_gu, gbar, a.I + tn.n0 + ld_c * 16, tn.m0 + q * 32);
+    }
+    ++ld_c;
+  };
+  issue_next();
+  uint32_t acc_it = 0, used = 0;
+  bool failed = false;
+  uint8_t* out_row = obuf_ptr + lane * 32;
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    const Tile t = decode_tile<KIND>(a, tile);
+    const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(buf ? accf1 : accf0, aph, tmo) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) set_status(a.status, MM_ERR_TIMEOUT);
+      break;
+    }
+    __syncwarp();
+    tc_fence_after();
+    const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
+    const int row0 = t.m0 + q * 32;
+    const int64_t row = (int64_t)row0 + lane;
+    const float w = __ldg(a.w_row + row);
+    float p = 0.f;
+    const int c_end = chunk_end(t.n0);
+    for (int c = c0; c < c_end; ++c) {
+      int okg = 1;
+      if (lane == 0) okg = mbar_wait(gbar, used & 1u, tmo) ? 1 : 0;
+      okg = __shfl_sync(0xffffffffu, okg, 0);
+      if (!okg) {
+        if (lane == 0) set_status(a.status, MM_ERR_TIMEOUT);
+        failed = true;
+        break;
+      }
+      __syncwarp();
+      // row `lane` of the two 32x16 fp32 boxes; with the 64-byte swizzle the 16-byte unit u of
+      // row r sits at unit u ^ ((r >> 1) & 3)
+      const uint8_t* base = gbuf_ptr + lane * 64;
+      const int n = t.n0 + c * 16;
+      float4 cur[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pu = (u ^ ((lane >> 1) & 3)) * 16;
+        const bool in = n + 4 * u < a.I;
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        cur[u] = in ? *reinterpret_cast<const float4*>(base + pu) : z;
+        cur[4 + u] = in ? *reinterpret_cast<const float4*>(base + GU_CHUNK_BYTES / 2 + pu) : z;
+      }
+      ++used;
+      __syncwarp();
+      issue_next();  // the staging buffer is free again: start the next chunk's load
+      // the previous chunk's stores must have finished reading the output staging buffer
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      act_grad_chunk(tacc + c * 16, cur, w, p, out_row, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&em->dgu_hi, obuf + 0 * OUT_PLANE_BYTES, n, 0, row0);
+        tma_store_3d(&em->dgu_hi, obuf + 1 * OUT_PLANE_BYTES, n, 1, row0);
+        tma_store_3d(&em->dgu_lo, obuf + 2 * OUT_PLANE_BYTES, n, 0, row0);
+        tma_store_3d(&em->dgu_lo, obuf + 3 * OUT_PLANE_BYTES, n, 1, row0);
+        tma_store_2d(&em->hw_hi, obuf + 4 * OUT_PLANE_BYTES, n, row0);
+        tma_store_2d(&em->hw_lo, obuf + 5 * OUT_PLANE_BYTES, n, row0);
+        bulk_commit();
+      }
+    }
+    if (failed) break;
+    // one partial per (column tile, half): the d_topk kernel sums them in a fixed order
+    a.p_part[(int64_t)(2 * (t.n0 / BN) + hf) * a.S_pad + row] = p;
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(buf ? acce1 : acce0);
+    ++acc_it;
+  }
+  if (lane == 0) bulk_wait_all();  // this warp's output stores are complete before it exits
+  __syncwarp();
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-           const __grid_constant__ CUtensorMap tmL, const Args a) {
+           const __grid_constant__ CUtensorMap tmL, const __grid_constant__ EpiMaps em,
+           const Args a) {
   using TR = Traits<KIND>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform)
   if (__syncthreads_or(a.hdr[HDR_STATUS] != 0)) return;
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  const uint32_t bars = sbase + STAGES * STAGE_BYTES;
+  constexpr int STAGES = TR::STAGES;
+  const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // act_grad gate|up staging
+  const uint32_t bars = epi_base + TR::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
   auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-  const uint32_t tmem_holder = bars + 8u * (2 * STAGES + 4);
+  auto gu_bar = [&](int ew) { return bars + 8u * (2 * STAGES + 4 + ew); };
+  const uint32_t tmem_holder = bars + 8u * (2 * STAGES + 4 + NUM_EPI_WARPS);
   volatile uint32_t* tmem_holder_ptr =
       reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
 
@@ -328,12 +466,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+      mbar_init(acce_bar(b), NUM_EPI_WARPS);  // one arrival per epilogue warp
     }
+    if constexpr (TR::GU_STAGING)
+      for (int ew = 0; ew < NUM_EPI_WARPS; ++ew) mbar_init(gu_bar(ew), 1);
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (TR::A_SPLIT || TR::B_SPLIT) tma_prefetch_desc(&tmL);
+    if constexpr (TR::A_SPLIT || TR::B_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
+    if constexpr (TR::GU_STAGING) {
+      tma_prefetch_desc(&em.dgu_hi);
+      tma_prefetch_desc(&em.dgu_lo);
+      tma_prefetch_desc(&em.hw_hi);
+      tma_prefetch_desc(&em.hw_lo);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, TR::TMEM_COLS);
@@ -442,14 +588,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++acc_it;
       }
     }
+  } else if constexpr (TR::GU_STAGING) {
+    const int ew = warp - 2;
+    const uint32_t gbuf = epi_base + ew * GU_CHUNK_BYTES;
+    const uint32_t obuf = epi_base + NUM_EPI_WARPS * GU_CHUNK_BYTES + ew * OUT_CHUNK_BYTES;
+    act_grad_epilogue(a, &tmL, &em, total, tmem_base, accf_bar(0), accf_bar(1), acce_bar(0),
+                      acce_bar(1), gu_bar(ew), gbuf, smem_raw + (gbuf - raw), obuf,
+                      smem_raw + (obuf - raw), warp, lane);
   } else {
-    const int q = warp & 3;        // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;   // tile row of this thread
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;     // tile row of this thread
+    const int hf = (warp - 2) >> 2;  // column half of the tile
     uint32_t acc_it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile<KIND>(a, tile);
       if (t.kiters == 0) {
-        if constexpr (TR::WGRAD) zero_wgrad_tile<KIND>(a, t, r);
+        if constexpr (TR::WGRAD) zero_wgrad_tile<KIND>(a, t, r, hf);
         continue;
       }
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
@@ -463,7 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
-      epilogue_tile<KIND>(a, t, tacc, r);
+      epilogue_tile<KIND>(a, t, tacc, r, hf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
@@ -496,9 +650,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims/box innermost first; strides in bytes (rank-1).
+// Tensor map; dims/box innermost first; strides in bytes (rank-1). bf16 with the 128-byte
+// swizzle unless stated.
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides, const uint32_t* box) {
+              const uint64_t* strides, const uint32_t* box,
+              CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[3], s[2];
@@ -508,9 +665,9 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     b[i] = box[i];
   }
   for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, s, b,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool map_rows(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_cols,
@@ -551,7 +708,7 @@ cudaError_t set_smem_attr() {
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask & bit) return cudaSuccess;
   e = cudaFuncSetAttribute(k_gemm<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SMEM_BYTES);
+                           (int)Traits<KIND>::SMEM);
   if (e == cudaSuccess) done_mask |= bit;
   return e;
 }
@@ -578,7 +735,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.timeout_ns = c.timeout_ns;
 
   CUtensorMap ta, tb, tl;
-  bool ok = true, has_lo = false;
+  EpiMaps em;
+  bool ok = true, has_lo = false, has_em = false;
   int64_t tiles_max = 0;
   const int64_t m_tiles_max = S_pad / BM;
   switch (KIND) {
@@ -604,9 +762,30 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.ld0 = H;
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
-    case GK_ACT_GRAD:
+    case GK_ACT_GRAD: {
+      // fp32 gate|up rows for the epilogue: boxes of 32 rows x 16 columns, 64-byte swizzle
+      const uint64_t gdims[2] = {(uint64_t)(2 * I), (uint64_t)S_pad};
+      const uint64_t gstr[1] = {(uint64_t)(2 * I) * 4};
+      const uint32_t gbox[2] = {16, 32};
       ok = map_rows(&ta, ws + w.off_dy_slot, H, S_pad, 64, BM) &&
-           map_experts(&tb, c.w_down, H, I, E, 64, BN);
+           map_experts(&tb, c.w_down, H, I, E, 64, BN) &&
+           make_map(&tl, ws + w.off_gu, 2, gdims, gstr, gbox, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+      // output planes, stored in boxes of 32 rows x 16 columns with the 32-byte swizzle
+      const uint64_t d3[3] = {(uint64_t)I, 2, (uint64_t)S_pad};
+      const uint64_t s3[2] = {(uint64_t)I * 2, (uint64_t)(2 * I) * 2};
+      const uint32_t b3[3] = {16, 1, 32};
+      const uint64_t d2[2] = {(uint64_t)I, (uint64_t)S_pad};
+      const uint64_t s2[1] = {(uint64_t)I * 2};
+      const uint32_t b2[2] = {16, 32};
+      const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      const auto SW = CU_TENSOR_MAP_SWIZZLE_32B;
+      ok = ok && make_map(&em.dgu_hi, ws + w.off_dgu, 3, d3, s3, b3, BF, SW) &&
+           make_map(&em.dgu_lo, ws + w.off_dgu_lo, 3, d3, s3, b3, BF, SW) &&
+           make_map(&em.hw_hi, ws + w.off_h, 2, d2, s2, b2, BF, SW) &&
+           make_map(&em.hw_lo, ws + w.off_hw_lo, 2, d2, s2, b2, BF, SW);
+      has_lo = true;
+      has_em = true;
       a.n_tiles_n = cdiv(I, BN);
       a.k_iters = cdiv(H, BK);
       a.N = (int)I;
@@ -622,6 +801,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.p_part = reinterpret_cast<float*>(ws + w.off_p_part);
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
+    }
     case GK_INPUT_GRAD:
       ok = map_rows(&ta, ws + w.off_dgu, 2 * I, S_pad, 64, BM) &&
            map_experts(&tb, c.w_up, 2 * I, H, E, 64, BN);
@@ -663,8 +843,9 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   }
   if (!ok) return cudaErrorInvalidValue;
   if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
+  if (!has_em) em.dgu_hi = em.dgu_lo = em.hw_hi = em.hw_lo = ta;  // unused but initialised
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
-  k_gemm<KIND><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tl, a);
+  k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
   return cudaGetLastError();
 }
 

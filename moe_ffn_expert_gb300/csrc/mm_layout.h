@@ -51,7 +51,7 @@ struct Workspace {
   int64_t T, H, I, E, K, S;
   int64_t S_pad;        // worst-case padded rows (multiple of BM)
   int64_t n_chunks;     // routing chunks of ROUTE_CHUNK slots
-  int64_t n_act_tiles;  // act_grad column tiles (ceil(I / BN)) = rows of the d_topk partials
+  int64_t n_act_tiles;  // rows of the d_topk partials: 2 column halves x ceil(I / BN) tiles
   size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
   size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
@@ -62,7 +62,7 @@ struct Workspace {
   size_t off_dy_slot;  // bf16 [S_pad, H]   dispatched dy rows
   size_t off_dgu;      // bf16 [S_pad, 2I]  hi part of [d_gate | d_up]
   size_t off_dgu_lo;   // bf16 [S_pad, 2I]  lo part of [d_gate | d_up]
-  size_t off_p_part;   // fp32 [ceil(I/BN), S_pad] per-column-tile partials of <g, h>
+  size_t off_p_part;   // fp32 [n_act_tiles, S_pad] per-column-half partials of <g, h>
   size_t total;
 };
 
