@@ -62,7 +62,10 @@ constexpr int OUT_CHUNK_BYTES = 6 * OUT_PLANE_BYTES;  // d_gate, d_up, w*h; hi a
 // never crosses from the gate half into the up half), w*h hi and lo as [rows][I].
 struct alignas(64) EpiMaps {
   CUtensorMap dgu_hi, dgu_lo, hw_hi, hw_lo;
+  CUtensorMap out;  // the bf16 output of GEMM2, INPUT_GRAD and the weight gradients
 };
+
+constexpr int OUT_TILE_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16 of staged output (64-byte rows)
 static_assert(BK == 64, "one 128-byte swizzle row per k-block");
 
 struct Args {
@@ -115,7 +118,12 @@ struct Traits {
   // six output planes (TMA in, TMA out)
   static constexpr bool GU_STAGING = (KIND == GK_ACT_GRAD);
   static constexpr int STAGES = GU_STAGING ? 3 : 4;
-  static constexpr int EPI_BYTES = GU_STAGING ? NUM_EPI_WARPS * (GU_CHUNK_BYTES + OUT_CHUNK_BYTES) : 0;
+  // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
+  // buffers) and store it with TMA
+  static constexpr bool OUT_STAGING = (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD);
+  static constexpr int EPI_BYTES = GU_STAGING    ? NUM_EPI_WARPS * (GU_CHUNK_BYTES + OUT_CHUNK_BYTES)
+                                   : OUT_STAGING ? NUM_EPI_WARPS * 2 * OUT_TILE_BYTES
+                                                 : 0;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -432,6 +440,50 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   __syncwarp();
 }
 
+// Output epilogue of one warp for the bf16-output kinds: 32 tile rows (quarter q) x one column
+// half. Each 32-column chunk is converted to bf16, written to one of the warp's two staging
+// buffers (64-byte swizzle: 16-byte unit u of row r at unit u ^ ((r >> 1) & 3)) and stored with
+// TMA by lane 0; the tensor map clips rows and columns outside the output. `chunk_no` counts the
+// warp's chunks to alternate the buffers; before a buffer is rewritten, the store that used it
+// two chunks earlier must have finished reading it.
+template <int KIND>
+__device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, uint32_t tacc,
+                                                  int q, int hf, int lane, const CUtensorMap* map,
+                                                  uint32_t sbuf, uint8_t* sbuf_ptr,
+                                                  uint32_t& chunk_no) {
+  constexpr int NC = Traits<KIND>::TN / 64;  // 32-column chunks per half
+  const int row0 = t.m0 + q * 32;
+#pragma unroll 1
+  for (int c = hf * NC; c < hf * NC + NC; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32(tacc + c * 32, v);
+    tmem_ld_wait();
+    const uint32_t b = chunk_no & 1u;
+    if (lane == 0) bulk_wait_read_le1();
+    __syncwarp();
+    uint8_t* rowp = sbuf_ptr + b * OUT_TILE_BYTES + lane * 64;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float f[8] = {__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]),
+                          __uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]),
+                          __uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]),
+                          __uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])};
+      *reinterpret_cast<uint4*>(rowp + ((u ^ ((lane >> 1) & 3)) << 4)) = pack8_bf16(f);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int n = t.n0 + c * 32;
+      if constexpr (Traits<KIND>::WGRAD)
+        tma_store_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+      else
+        tma_store_2d(map, sbuf + b * OUT_TILE_BYTES, n, row0);
+      bulk_commit();
+    }
+    ++chunk_no;
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -474,6 +526,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (TR::A_SPLIT || TR::B_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
+    if constexpr (TR::OUT_STAGING) tma_prefetch_desc(&em.out);
     if constexpr (TR::GU_STAGING) {
       tma_prefetch_desc(&em.dgu_hi);
       tma_prefetch_desc(&em.dgu_lo);
@@ -599,6 +652,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;     // tile row of this thread
     const int hf = (warp - 2) >> 2;  // column half of the tile
+    const uint32_t sbuf = epi_base + (warp - 2) * 2 * OUT_TILE_BYTES;  // output staging
+    uint32_t chunk_no = 0;
     uint32_t acc_it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile<KIND>(a, tile);
@@ -617,11 +672,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
-      epilogue_tile<KIND>(a, t, tacc, r, hf);
+      if constexpr (TR::OUT_STAGING)
+        staged_store_tile<KIND>(a, t, tacc, q, hf, lane, &em.out, sbuf, smem_raw + (sbuf - raw),
+                                chunk_no);
+      else
+        epilogue_tile<KIND>(a, t, tacc, r, hf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
       ++acc_it;
+    }
+    if constexpr (TR::OUT_STAGING) {
+      if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
+      __syncwarp();
     }
   }
 
@@ -844,6 +907,24 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   if (!ok) return cudaErrorInvalidValue;
   if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
   if (!has_em) em.dgu_hi = em.dgu_lo = em.hw_hi = em.hw_lo = ta;  // unused but initialised
+  if constexpr (Traits<KIND>::OUT_STAGING) {
+    // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_64B;
+    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N]
+      const uint64_t d3[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)E};
+      const uint64_t s3[2] = {(uint64_t)a.ld0 * 2, (uint64_t)a.out_expert_stride * 2};
+      const uint32_t b3[3] = {32, 32, 1};
+      if (!make_map(&em.out, a.out0, 3, d3, s3, b3, BF, SW)) return cudaErrorInvalidValue;
+    } else {  // [S_pad][N]
+      const uint64_t d2[2] = {(uint64_t)a.N, (uint64_t)S_pad};
+      const uint64_t s2[1] = {(uint64_t)a.ld0 * 2};
+      const uint32_t b2[2] = {32, 32};
+      if (!make_map(&em.out, a.out0, 2, d2, s2, b2, BF, SW)) return cudaErrorInvalidValue;
+    }
+  } else {
+    em.out = ta;  // unused but initialised
+  }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
   k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
   return cudaGetLastError();
