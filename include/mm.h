@@ -67,6 +67,12 @@ typedef struct mm_dims {
  * read), returning MM_ERR_BAD_EXPERT_ID before any other kernel is enqueued. */
 #define MM_FLAG_VALIDATE_IDS 0x1u
 
+/* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
+ * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
+ * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is
+ * unspecified) instead of hanging; the next call on the same workspace runs normally. */
+#define MM_FLAG_TEST_STALL 0x80000000u
+
 /* Bytes of workspace mm_forward/mm_backward need for `d` (RFC §2.3 workspace query).
  * Returns 0 if `d` is unsupported. The workspace holds the routing tables, the dispatched
  * rows x_slot and the saved gate|up activations (kept from mm_forward for mm_backward),

@@ -23,6 +23,7 @@ namespace mm {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bounded device waits: 2 s
+constexpr uint64_t kTestTimeoutNs = 50000000ull;       // with MM_FLAG_TEST_STALL: 50 ms
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -193,9 +194,12 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const fl
                [&] { return launch_route_rank(w, ws, topk_ids, topk_weights, st); }));
   MM_TRY(timed(ST_GATHER_X, st,
                [&] { return launch_gather_rows(w, ws, x, ws + w.off_x_slot, st); }));
-  GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs};
+  const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
+  GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
+             stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0};
   MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.kind = GK_GEMM2;
+  c.inject_stall = 0;
   MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_COMBINE_Y, st,
                [&] { return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st); }));
@@ -224,7 +228,7 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
 
   MM_TRY(timed(ST_GATHER_DY, st,
                [&] { return launch_gather_rows(w, ws, dy, ws + w.off_dy_slot, st); }));
-  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs};
+  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0};
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;

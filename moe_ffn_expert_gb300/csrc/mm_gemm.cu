@@ -93,6 +93,7 @@ struct Args {
   int64_t S_pad;
   int64_t out_expert_stride;
   uint64_t timeout_ns;
+  int inject_stall;
 };
 
 template <int KIND>
@@ -637,7 +638,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_commit(empty_bar(s));
         }
         if (!ok) break;
-        umma_commit(accf_bar(buf));
+        // (test hook: CTA 0 withholds its first hand-off, so its epilogue's wait runs out)
+        if (!(a.inject_stall && blockIdx.x == 0 && acc_it == 0)) umma_commit(accf_bar(buf));
         ++acc_it;
       }
     }
@@ -796,6 +798,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.I = (int)I;
   a.S_pad = S_pad;
   a.timeout_ns = c.timeout_ns;
+  a.inject_stall = c.inject_stall;
 
   CUtensorMap ta, tb, tl;
   EpiMaps em;

@@ -40,6 +40,7 @@ struct GemmCall {
   const void* w_down;  // bf16 [E, I, H]
   void* d_w;           // weight-gradient output (W1/W2 grads)
   uint64_t timeout_ns;
+  int inject_stall;    // test hook: withhold the first accumulator hand-off of CTA 0
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);

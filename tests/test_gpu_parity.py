@@ -254,3 +254,17 @@ def test_torch_autograd_entry_point():
     assert torch.equal(y.detach(), ref["y"])
     assert torch.equal(x.grad, ref["dx"]) and torch.equal(tw.grad, ref["d_topk_weights"])
     assert torch.equal(wu.grad, ref["dW_up"]) and torch.equal(wd.grad, ref["dW_down"])
+
+
+def test_bounded_wait_times_out_and_the_next_call_is_clean():
+    """A withheld accumulator hand-off (test hook) must end in MM_ERR_TIMEOUT reported through
+    the status word, not in a hang or a fault; the same workspace then gives correct results."""
+    w = synth.small("stall", 700, 256, 128, 6, 2, seed=6)
+    inp = make_inputs(w)
+    ref = run_layer(inp)
+    out = run_layer(inp, flags=_abi.MM_FLAG_TEST_STALL, ws=ref["ws"], backward=False)
+    assert out["status"] == _abi.MM_ERR_TIMEOUT
+    again = run_layer(inp, ws=ref["ws"])
+    assert again["status"] == _abi.MM_OK
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+        assert torch.equal(again[k], ref[k]), k
