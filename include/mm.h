@@ -134,6 +134,9 @@ mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts,
 mm_status mm_route_noalloc(mm_dims d, const int32_t* topk_ids, int32_t* counts,
                            int32_t* offsets, int32_t* row_of_slot, void* stream);
 
+/* The step and CUDA error of the last MM_ERR_CUDA returned to the calling thread ("" if none). */
+const char* mm_last_error_detail(void);
+
 /* Human-readable name of a status code. */
 const char* mm_status_string(mm_status s);
 

@@ -32,7 +32,9 @@ STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3:
 class MMError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({_lib().mm_status_string(status).decode()})")
+        detail = _lib().mm_last_error_detail().decode() if status == MM_ERR_CUDA else ""
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} "
+                         f"({_lib().mm_status_string(status).decode()}){' ' + detail if detail else ''}")
 
 
 class mm_dims(ctypes.Structure):
@@ -62,6 +64,7 @@ def _lib():
         "mm_routing_export": (st, [mm_dims, _P, _P, _P, _P, _P]),
         "mm_status_string": (ctypes.c_char_p, [st]),
         "mm_abi_version": (ctypes.c_int, []),
+        "mm_last_error_detail": (ctypes.c_char_p, []),
         "mm_timing_enable": (st, [ctypes.c_int]),
         "mm_timing_read": (ctypes.c_int, [_P, _P, ctypes.c_int]),
         "mm_stage_name": (ctypes.c_char_p, [ctypes.c_int]),

@@ -9,6 +9,8 @@
 // stream orders everything. The two-phase size query / execute split mirrors §2.3.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdarg.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -82,13 +84,41 @@ const char* kStageNames[ST_COUNT] = {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-#define MM_TRY(expr)                      \
-  do {                                    \
-    cudaError_t _e = (expr);              \
-    if (_e != cudaSuccess) return MM_ERR_CUDA; \
+// Text of the last CUDA failure seen by a call of this thread (see mm_last_error_detail).
+thread_local char g_err[256] = "";
+
+mm_status cuda_fail(cudaError_t e, const char* what) {
+  char inner[160];
+  snprintf(inner, sizeof(inner), "%s", g_err);
+  snprintf(g_err, sizeof(g_err), "%s: %s (%s)%s%s", what, cudaGetErrorString(e), cudaGetErrorName(e),
+           inner[0] ? "; " : "", inner);
+  return MM_ERR_CUDA;
+}
+
+#define MM_TRY(expr)                                    \
+  do {                                                  \
+    cudaError_t _e = (expr);                            \
+    if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
   } while (0)
 
+// Makes the current device's primary context current on this thread. Tensor-map encoding is a
+// driver call that needs one, and a thread that has not launched anything yet (an autograd
+// worker thread, say) may not have it bound.
+cudaError_t bind_context() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaSetDevice(dev);
+}
+
 }  // namespace
+
+void note_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
 
 bool plan_workspace(const mm_dims& d, Workspace* w) {
   if (!dims_ok(d)) return false;
@@ -140,6 +170,8 @@ extern "C" {
 
 int mm_abi_version(void) { return 1; }
 
+const char* mm_last_error_detail(void) { return g_err; }
+
 const char* mm_status_string(mm_status s) {
   switch (s) {
     case MM_OK: return "ok";
@@ -180,6 +212,8 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const fl
     return MM_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
+  g_err[0] = 0;
+  MM_TRY(bind_context());
 
   MM_TRY(cudaMemsetAsync(ws + w.off_hdr, 0, HDR_WORDS * sizeof(int32_t), st));
   MM_TRY(timed(ST_ROUTE_COUNT, st, [&] { return launch_route_count(w, ws, topk_ids, st); }));
@@ -225,6 +259,8 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
     return MM_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
+  g_err[0] = 0;
+  MM_TRY(bind_context());
 
   MM_TRY(timed(ST_GATHER_DY, st,
                [&] { return launch_gather_rows(w, ws, dy, ws + w.off_dy_slot, st); }));

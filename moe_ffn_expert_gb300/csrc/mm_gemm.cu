@@ -722,7 +722,10 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) {
+    note_error("cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
   cuuint64_t d[3], s[2];
   cuuint32_t b[3], es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) {
@@ -730,9 +733,15 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     b[i] = box[i];
   }
   for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
-  return fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    note_error("tensor map encode failed (CUresult %d): rank %d dims %llu %llu %llu box %u %u %u",
+               (int)r, rank, (unsigned long long)d[0], (unsigned long long)(rank > 1 ? d[1] : 0),
+               (unsigned long long)(rank > 2 ? d[2] : 0), b[0], rank > 1 ? b[1] : 0u,
+               rank > 2 ? b[2] : 0u);
+  return r == CUDA_SUCCESS;
 }
 
 bool map_rows(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, uint32_t box_cols,

@@ -45,4 +45,7 @@ struct GemmCall {
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);
 
+// Records a description of a host-side failure for mm_last_error_detail (this thread).
+void note_error(const char* fmt, ...);
+
 }  // namespace mm
