@@ -67,6 +67,12 @@ typedef struct mm_dims {
  * read), returning MM_ERR_BAD_EXPERT_ID before any other kernel is enqueued. */
 #define MM_FLAG_VALIDATE_IDS 0x1u
 
+/* mm_backward flag: add the weight gradients into d_up_proj_weight and d_down_proj_weight
+ * (gradient accumulation over micro-batches, RFC §7.1) instead of overwriting them. The addition
+ * is done in bf16 by the stores themselves (one rounding of each addend and of each sum); experts
+ * with no slot leave their slices unchanged. dx and d_topk_weights are still overwritten. */
+#define MM_FLAG_ACCUMULATE_WEIGHT_GRADS 0x2u
+
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
  * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is

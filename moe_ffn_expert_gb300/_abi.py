@@ -23,6 +23,7 @@ MM_ERR_BAD_EXPERT_ID = 5
 MM_ERR_TIMEOUT = 6
 MM_FLAG_VALIDATE_IDS = 0x1
 MM_FLAG_TEST_STALL = 0x80000000
+MM_FLAG_ACCUMULATE_WEIGHT_GRADS = 0x2
 MM_NUM_STAGES = 14
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",

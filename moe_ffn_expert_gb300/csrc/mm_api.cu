@@ -230,7 +230,7 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const fl
                [&] { return launch_gather_rows(w, ws, x, ws + w.off_x_slot, st); }));
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
-             stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0};
+             stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0};
   MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.kind = GK_GEMM2;
   c.inject_stall = 0;
@@ -245,7 +245,6 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
                       const void* down_proj_weight, void* workspace, size_t workspace_bytes,
                       void* dx, float* d_topk_weights, void* d_up_proj_weight,
                       void* d_down_proj_weight, void* stream, uint32_t flags) {
-  (void)flags;
   Workspace w;
   mm_status s = check_common(d, workspace, workspace_bytes, &w);
   if (s != MM_OK) return s;
@@ -264,19 +263,23 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
 
   MM_TRY(timed(ST_GATHER_DY, st,
                [&] { return launch_gather_rows(w, ws, dy, ws + w.off_dy_slot, st); }));
-  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0};
+  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0, 0};
+  const int accumulate = (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) ? 1 : 0;
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;
   c.d_w = d_down_proj_weight;
+  c.accumulate = accumulate;
   MM_TRY(timed(ST_W2_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.kind = GK_INPUT_GRAD;
   c.d_w = nullptr;
+  c.accumulate = 0;
   MM_TRY(timed(ST_INPUT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_COMBINE_DX, st,
                [&] { return launch_combine(w, ws, ws + w.off_o, nullptr, dx, st); }));
   c.kind = GK_W1_GRAD;
   c.d_w = d_up_proj_weight;
+  c.accumulate = accumulate;
   MM_TRY(timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   return MM_OK;
 }

@@ -94,6 +94,7 @@ struct Args {
   int64_t out_expert_stride;
   uint64_t timeout_ns;
   int inject_stall;
+  int accumulate;  // weight gradients: reduce-add into the output
 };
 
 template <int KIND>
@@ -475,8 +476,12 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, 
     __syncwarp();
     if (lane == 0) {
       const int n = t.n0 + c * 32;
-      if constexpr (Traits<KIND>::WGRAD)
-        tma_store_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+      if constexpr (Traits<KIND>::WGRAD) {
+        if (a.accumulate)
+          tma_reduce_add_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+        else
+          tma_store_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+      }
       else
         tma_store_2d(map, sbuf + b * OUT_TILE_BYTES, n, row0);
       bulk_commit();
@@ -660,7 +665,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Tile t = decode_tile<KIND>(a, tile);
       if (t.kiters == 0) {
-        if constexpr (TR::WGRAD) zero_wgrad_tile<KIND>(a, t, r, hf);
+        if constexpr (TR::WGRAD) {
+          if (!a.accumulate) zero_wgrad_tile<KIND>(a, t, r, hf);  // adding zero changes nothing
+        }
         continue;
       }
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
@@ -808,6 +815,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.S_pad = S_pad;
   a.timeout_ns = c.timeout_ns;
   a.inject_stall = c.inject_stall;
+  a.accumulate = c.accumulate;
 
   CUtensorMap ta, tb, tl;
   EpiMaps em;

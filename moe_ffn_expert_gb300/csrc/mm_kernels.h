@@ -41,6 +41,7 @@ struct GemmCall {
   void* d_w;           // weight-gradient output (W1/W2 grads)
   uint64_t timeout_ns;
   int inject_stall;    // test hook: withhold the first accumulator hand-off of CTA 0
+  int accumulate;      // weight gradients: add into the output instead of overwriting it
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);

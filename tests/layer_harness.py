@@ -27,8 +27,11 @@ def make_inputs(w: synth.Workload, device="cuda", ids=None):
     )
 
 
-def run_layer(inp, flags=0, ws=None, stream=None, backward=True):
-    """Forward (+ backward) through the C ABI; returns device tensors and the workspace."""
+def run_layer(inp, flags=0, ws=None, stream=None, backward=True, bwd_flags=0, d_up=None,
+              d_down=None):
+    """Forward (+ backward) through the C ABI; returns device tensors and the workspace.
+    d_up/d_down, when given, are the weight-gradient output buffers (their contents matter with
+    MM_FLAG_ACCUMULATE_WEIGHT_GRADS in bwd_flags)."""
     x, ids, tw = inp["x"], inp["topk_ids"], inp["topk_weights"]
     wu, wd = inp["w_up"], inp["w_down"]
     T, H = x.shape
@@ -48,12 +51,12 @@ def run_layer(inp, flags=0, ws=None, stream=None, backward=True):
     if backward:
         dx = torch.empty_like(x)
         d_topk = torch.empty(T, K, dtype=torch.float32, device=x.device)
-        d_up = torch.empty_like(wu)
-        d_down = torch.empty_like(wd)
+        d_up = torch.empty_like(wu) if d_up is None else d_up
+        d_down = torch.empty_like(wd) if d_down is None else d_down
         _abi.check(_abi.mm_backward(d, inp["dy"].data_ptr(), x.data_ptr(), ids.data_ptr(),
                                     tw.data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(),
                                     nbytes, dx.data_ptr(), d_topk.data_ptr(), d_up.data_ptr(),
-                                    d_down.data_ptr(), st, 0), "mm_backward")
+                                    d_down.data_ptr(), st, bwd_flags), "mm_backward")
         out.update(dx=dx, d_topk_weights=d_topk, dW_up=d_up, dW_down=d_down)
     out["status"] = _abi.mm_get_status(ws.data_ptr(), st)
     return out

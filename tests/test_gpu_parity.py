@@ -268,3 +268,24 @@ def test_bounded_wait_times_out_and_the_next_call_is_clean():
     assert again["status"] == _abi.MM_OK
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(again[k], ref[k]), k
+
+
+def test_accumulate_weight_grads_adds_into_the_outputs():
+    """MM_FLAG_ACCUMULATE_WEIGHT_GRADS: dW += the step's gradient (bf16 adds), experts without
+    slots keep their previous contents bit for bit; dx and d_topk are still overwritten."""
+    T, E, K = 300, 8, 2
+    ids = torch.stack([torch.arange(T) % 7, (torch.arange(T) + 3) % 7], 1).int()  # expert 7 empty
+    w, inp = _custom(T, 256, 128, E, K, ids=ids, seed=13)
+    ref = run_layer(inp)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    base_up = torch.randn(inp["w_up"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    base_down = torch.randn(inp["w_down"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    out = run_layer(inp, bwd_flags=_abi.MM_FLAG_ACCUMULATE_WEIGHT_GRADS, d_up=base_up.clone(),
+                    d_down=base_down.clone())
+    assert out["status"] == _abi.MM_OK
+    for name, base in (("dW_up", base_up), ("dW_down", base_down)):
+        exp = base.double() + ref[name].double()
+        got = out[name].double()
+        assert ((got - exp).abs() <= 2.0 ** -8 * exp.abs() + 1e-6).all(), name
+        assert torch.equal(out[name][7], base[7]), name  # the empty expert is untouched
+    assert torch.equal(out["dx"], ref["dx"]) and torch.equal(out["d_topk_weights"], ref["d_topk_weights"])
