@@ -116,11 +116,20 @@ def expert_forward(X: torch.Tensor, w_up_e: torch.Tensor, w_down_e: torch.Tensor
     return gate, up, h, o
 
 
-def forward(x, topk_ids, topk_weights, w_up, w_down, return_saved=False):
-    """y[T,H] = combine(GMM2(SwiGLU(GMM1(dispatch(x))))).
+def shared_expert_forward(x, shared_up, shared_down):
+    """The shared expert of the RFC's optional shared-expert fusion (§6.1): one SwiGLU FFN
+    applied to every token, whose output the combine adds with weight 1.
+    shared_up [H, 2*I_s] (gate | up), shared_down [I_s, H]."""
+    _, _, _, o = expert_forward(_as64(x), shared_up, shared_down)
+    return o
+
+
+def forward(x, topk_ids, topk_weights, w_up, w_down, return_saved=False, shared=None):
+    """y[T,H] = combine(GMM2(SwiGLU(GMM1(dispatch(x))))) (+ the shared expert's output).
 
     `w_up` / `w_down` only need `[e]` indexing (a [E,...] tensor or a lazy
-    per-expert source). Experts with no slots are never touched."""
+    per-expert source). Experts with no slots are never touched. `shared`, when given, is a
+    (shared_up, shared_down) pair (RFC §6.1)."""
     T, H = x.shape
     K = topk_ids.shape[1]
     E = w_up.shape[0]
@@ -134,6 +143,8 @@ def forward(x, topk_ids, topk_weights, w_up, w_down, return_saved=False):
         _, _, _, o = expert_forward(x_rows[r0:r1], w_up[e], w_down[e])
         o_rows[r0:r1] = o
     y = combine(o_rows, row_of_slot, topk_weights, T, K)
+    if shared is not None:
+        y = y + shared_expert_forward(x, *shared)
     if return_saved:
         return y, dict(counts=counts, offsets=offsets, row_of_slot=row_of_slot,
                        slot_of_row=slot_of_row, o_rows=o_rows)
@@ -169,8 +180,10 @@ def expert_backward(X, dY, w, w_up_e, w_down_e):
     )
 
 
-def backward(x, topk_ids, topk_weights, w_up, w_down, dy):
-    """All gradients of sum(y * dy): dx[T,H], d_topk_weights[T,K], dW_up[E,H,2I], dW_down[E,I,H]."""
+def backward(x, topk_ids, topk_weights, w_up, w_down, dy, shared=None):
+    """All gradients of sum(y * dy): dx[T,H], d_topk_weights[T,K], dW_up[E,H,2I], dW_down[E,I,H]
+    (and, with a shared expert, dS_up[H,2I_s], dS_down[I_s,H]: its rows are all tokens with
+    weight 1)."""
     T, H = x.shape
     K = topk_ids.shape[1]
     E = w_up.shape[0]
@@ -194,7 +207,12 @@ def backward(x, topk_ids, topk_weights, w_up, w_down, dy):
         dW_down[e] = g["dW_down"]
     dx = combine(dx_rows, row_of_slot, None, T, K)
     d_topk = d_topk_rows[row_of_slot].reshape(T, K)
-    return dict(dx=dx, d_topk_weights=d_topk, dW_up=dW_up, dW_down=dW_down)
+    out = dict(dx=dx, d_topk_weights=d_topk, dW_up=dW_up, dW_down=dW_down)
+    if shared is not None:
+        g = expert_backward(_as64(x), _as64(dy), torch.ones(T, dtype=F64), *shared)
+        out["dx"] = dx + g["dx_rows"]
+        out.update(dS_up=g["dW_up"], dS_down=g["dW_down"])
+    return out
 
 
 # ------------------------------------------------------------------ sampled evaluation

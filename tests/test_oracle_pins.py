@@ -311,3 +311,69 @@ def test_planted_gate_up_swap_is_caught(monkeypatch):
     y = oracle.forward(x, torch.zeros(T, 1, dtype=torch.int32), torch.ones(T, 1, dtype=F64),
                        torch.cat([wg, wu], 1)[None], wd[None])
     assert not torch.allclose(y, ref, rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------------------ shared expert (RFC §6.1)
+
+def _shared_case(seed, T=9, H=8, I=4, E=5, K=2, Is=6):
+    x, ids, w, wu, wd, dy = _rand_case(T=T, H=H, I=I, E=E, K=K, seed=seed)
+    g = torch.Generator().manual_seed(seed + 100)
+    su = torch.randn(H, 2 * Is, generator=g, dtype=F64) / math.sqrt(H)
+    sd = torch.randn(Is, H, generator=g, dtype=F64) / math.sqrt(Is)
+    return x, ids, w, wu, wd, dy, (su, sd)
+
+
+def test_shared_expert_alone_is_the_dense_swiglu_ffn():
+    """Routed experts with zero down-projections: y is torch's own SwiGLU FFN of the shared
+    expert, and its weight gradients are torch autograd's."""
+    x, ids, w, wu, wd, dy, (su, sd) = _shared_case(1)
+    Is = sd.shape[0]
+    y = oracle.forward(x, ids, w, wu, torch.zeros_like(wd), shared=(su, sd))
+    assert torch.allclose(y, _dense_swiglu_ffn(x, su[:, :Is], su[:, Is:], sd), rtol=1e-12, atol=1e-12)
+    su_t, sd_t = su.clone().requires_grad_(True), sd.clone().requires_grad_(True)
+    (_dense_swiglu_ffn(x, su_t[:, :Is], su_t[:, Is:], sd_t) * dy).sum().backward()
+    g = oracle.backward(x, ids, w, wu, torch.zeros_like(wd), dy, shared=(su, sd))
+    assert torch.allclose(g["dS_up"], su_t.grad, rtol=1e-12, atol=1e-12)
+    assert torch.allclose(g["dS_down"], sd_t.grad, rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_equals_an_extra_always_on_slot():
+    """A shared expert with I_s = I is the same as an extra expert routed from every token with
+    weight 1 (one more slot per token)."""
+    x, ids, w, wu, wd, dy, (su, sd) = _shared_case(2, Is=4)
+    T, K = ids.shape
+    E = wu.shape[0]
+    ids1 = torch.cat([ids, torch.full((T, 1), E, dtype=torch.int32)], 1)
+    w1 = torch.cat([w, torch.ones(T, 1, dtype=F64)], 1)
+    wu1, wd1 = torch.cat([wu, su[None]]), torch.cat([wd, sd[None]])
+    assert torch.allclose(oracle.forward(x, ids, w, wu, wd, shared=(su, sd)),
+                          oracle.forward(x, ids1, w1, wu1, wd1), rtol=1e-12, atol=1e-12)
+    g = oracle.backward(x, ids, w, wu, wd, dy, shared=(su, sd))
+    g1 = oracle.backward(x, ids1, w1, wu1, wd1, dy)
+    assert torch.allclose(g["dx"], g1["dx"], rtol=1e-12, atol=1e-12)
+    assert torch.allclose(g["dS_up"], g1["dW_up"][E], rtol=1e-12, atol=1e-12)
+    assert torch.allclose(g["dS_down"], g1["dW_down"][E], rtol=1e-12, atol=1e-12)
+    assert torch.allclose(g["d_topk_weights"], g1["d_topk_weights"][:, :K], rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_finite_differences():
+    x, ids, w, wu, wd, dy, (su, sd) = _shared_case(3, Is=6)
+    g = oracle.backward(x, ids, w, wu, wd, dy, shared=(su, sd))
+    eps = 1e-6
+
+    def loss():
+        return float((oracle.forward(x, ids, w, wu, wd, shared=(su, sd)) * dy).sum())
+
+    gen = torch.Generator().manual_seed(4)
+    for name, t, grad in (("x", x, g["dx"]), ("su", su, g["dS_up"]), ("sd", sd, g["dS_down"])):
+        flat = t.view(-1)
+        for i in torch.randperm(flat.numel(), generator=gen)[:20].tolist():
+            old = flat[i].item()
+            flat[i] = old + eps
+            lp = loss()
+            flat[i] = old - eps
+            lm = loss()
+            flat[i] = old
+            fd = (lp - lm) / (2 * eps)
+            an = grad.reshape(-1)[i].item()
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, i, fd, an)
