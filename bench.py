@@ -193,7 +193,8 @@ def run_gpu(args):
     T, H, I, E, K = w.T, w.H, w.I, w.E, w.K
     S = T * K
     d = _abi.dims(T, H, I, E, K)
-    nbytes = _abi.mm_workspace_size(d)
+    I_s = args.shared_intermediate
+    nbytes = _abi.mm_workspace_size_se(d, I_s) if I_s else _abi.mm_workspace_size(d)
     stream = torch.cuda.current_stream(dev)
     st = stream.cuda_stream
 
@@ -209,12 +210,27 @@ def run_gpu(args):
     dtk = torch.empty(T, K, dtype=torch.float32, device=dev)
     du = torch.empty_like(wu)
     dd = torch.empty_like(wd)
+    if I_s:  # a shared expert (always-on SwiGLU FFN of intermediate size I_s)
+        su, sd = synth.shared_up(w, I_s, device=dev), synth.shared_down(w, I_s, device=dev)
+        dsu, dsd = torch.empty_like(su), torch.empty_like(sd)
+        se = _abi.shared_expert(I_s, su.data_ptr(), sd.data_ptr(), dsu.data_ptr(), dsd.data_ptr())
 
     def fwd():
+        if I_s:
+            _abi.check(_abi.mm_forward_se(d, se, x.data_ptr(), ids.data_ptr(), tw.data_ptr(),
+                                          wu.data_ptr(), wd.data_ptr(), y.data_ptr(), ws.data_ptr(),
+                                          nbytes, st, 0), "fwd")
+            return
         _abi.check(_abi.mm_forward(d, x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
                                    wd.data_ptr(), y.data_ptr(), ws.data_ptr(), nbytes, st, 0), "fwd")
 
     def bwd():
+        if I_s:
+            _abi.check(_abi.mm_backward_se(d, se, dy.data_ptr(), x.data_ptr(), ids.data_ptr(),
+                                           tw.data_ptr(), wu.data_ptr(), wd.data_ptr(),
+                                           ws.data_ptr(), nbytes, dx.data_ptr(), dtk.data_ptr(),
+                                           du.data_ptr(), dd.data_ptr(), st, 0), "bwd")
+            return
         _abi.check(_abi.mm_backward(d, dy.data_ptr(), x.data_ptr(), ids.data_ptr(), tw.data_ptr(),
                                     wu.data_ptr(), wd.data_ptr(), ws.data_ptr(), nbytes,
                                     dx.data_ptr(), dtk.data_ptr(), du.data_ptr(), dd.data_ptr(),
@@ -302,6 +318,8 @@ def run_gpu(args):
     peaks, peak_src = load_peaks()
     hi = H * I
     flops = w.flops()
+    if I_s:  # the shared expert adds one SwiGLU FFN over every token: 6*H*I_s fwd, 12 bwd
+        flops = {k: v + m * H * I_s * T for (k, v), m in zip(flops.items(), (6, 12, 18))}
     total_flops_step = flops["total"]
     tflops = total_flops_step * args.steps * world / (elapsed_max / 1e3) / 1e12
     peak_burst = peaks["bf16_tflops"]
@@ -317,7 +335,8 @@ def run_gpu(args):
     achieved = top_flops / (avg_ms / 1e3) / 1e12
 
     # CPU baseline: the oracle on a bounded sample of this workload
-    cpu = cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 else None
+    cpu = (cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 and not I_s
+           else None)
 
     line = {
         "metric": METRIC,
@@ -332,8 +351,10 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic: seeded counter-based generator; inputs larger than L2 (no flush)",
-        "config": {"workload": f"{w.name} T={T} H={H} I={I} E={E} K={K}", "T": T, "H": H, "I": I,
+        "config": {"workload": f"{w.name} T={T} H={H} I={I} E={E} K={K}"
+                               + (f" shared I_s={I_s}" if I_s else ""), "T": T, "H": H, "I": I,
                    "E": E, "K": K, "routing": w.routing, "seed": w.seed,
+                   **({"shared_I": I_s} if I_s else {}),
                    "l2": "inputs larger than L2: 1.2 GB of expert weights and 0.6 GB of slot rows per step",
                    "parallelism": "single GPU" if world == 1 else f"{world} independent replicas"},
         "tflops": round(tflops, 2),
@@ -461,11 +482,15 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (smaller profiling cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--shared-intermediate", type=int, default=0,
+                    help="add a shared expert of this intermediate size (0: none)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
+    if args.impl == "reference" and args.shared_intermediate:
+        ap.error("the oracle arm times the routed layer only (no --shared-intermediate)")
     if args.impl == "reference":
         run_reference(args)
     else:

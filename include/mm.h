@@ -109,6 +109,39 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
                       void* dx, float* d_topk_weights, void* d_up_proj_weight,
                       void* d_down_proj_weight, void* stream, uint32_t flags);
 
+/* Optional shared expert (RFC §6.1, shared-expert fusion): one SwiGLU FFN applied to every token,
+ * whose output the combine adds to y with weight 1 (y_t = sum_k w[t,k] o_{t,k} + o_shared_t, one
+ * fp32 sum rounded once), and whose input-gradient rows are added into dx the same way. Its
+ * intermediate size may differ from the routed experts'. */
+typedef struct mm_shared_expert {
+  int64_t I;                      /* shared intermediate size I_s (a multiple of 8) */
+  const void* up_proj_weight;     /* bf16 [H, 2*I_s]: gate in columns [0, I_s), up in [I_s, 2*I_s) */
+  const void* down_proj_weight;   /* bf16 [I_s, H] */
+  void* d_up_proj_weight;         /* bf16 [H, 2*I_s], written by mm_backward_se (unused forward) */
+  void* d_down_proj_weight;       /* bf16 [I_s, H], written by mm_backward_se (unused forward) */
+} mm_shared_expert;
+
+/* Workspace bytes for mm_forward_se / mm_backward_se with a shared expert of size shared_I
+ * (0 if unsupported). The routed part's layout is the same as mm_workspace_size's, followed by
+ * the shared expert's saved activations and scratch. */
+size_t mm_workspace_size_se(mm_dims d, int64_t shared_I, uint32_t flags);
+
+/* mm_forward with a shared expert `se` (not NULL). Same arguments, errors and workspace rule. */
+mm_status mm_forward_se(mm_dims d, const mm_shared_expert* se, const void* x,
+                        const int32_t* topk_ids, const float* topk_weights,
+                        const void* up_proj_weight, const void* down_proj_weight, void* y,
+                        void* workspace, size_t workspace_bytes, void* stream, uint32_t flags);
+
+/* mm_backward with a shared expert `se`: also writes se->d_up_proj_weight and
+ * se->d_down_proj_weight (accumulated with MM_FLAG_ACCUMULATE_WEIGHT_GRADS) and adds the shared
+ * expert's input gradient into dx. The workspace must come from mm_forward_se with the same se. */
+mm_status mm_backward_se(mm_dims d, const mm_shared_expert* se, const void* dy, const void* x,
+                         const int32_t* topk_ids, const float* topk_weights,
+                         const void* up_proj_weight, const void* down_proj_weight,
+                         void* workspace, size_t workspace_bytes, void* dx,
+                         float* d_topk_weights, void* d_up_proj_weight, void* d_down_proj_weight,
+                         void* stream, uint32_t flags);
+
 /* Synchronises `stream`, then returns the device-side status word of `workspace`
  * (MM_OK, MM_ERR_BAD_EXPERT_ID or MM_ERR_TIMEOUT), or MM_ERR_CUDA if the stream failed.
  * The word is cleared at the start of every mm_forward. */
@@ -153,7 +186,7 @@ int mm_abi_version(void);
  * CUDA events on its stream. mm_timing_read synchronises those events, writes for each stage
  * (up to max_stages) the summed milliseconds and the number of launches since the last read,
  * clears them, and returns the number of stages (MM_NUM_STAGES). mm_stage_name names a stage. */
-#define MM_NUM_STAGES 14
+#define MM_NUM_STAGES 15
 mm_status mm_timing_enable(int on);
 int mm_timing_read(double* ms, int64_t* launches, int max_stages);
 const char* mm_stage_name(int stage);

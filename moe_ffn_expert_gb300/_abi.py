@@ -24,7 +24,7 @@ MM_ERR_TIMEOUT = 6
 MM_FLAG_VALIDATE_IDS = 0x1
 MM_FLAG_TEST_STALL = 0x80000000
 MM_FLAG_ACCUMULATE_WEIGHT_GRADS = 0x2
-MM_NUM_STAGES = 14
+MM_NUM_STAGES = 15
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT"}
@@ -41,6 +41,12 @@ class MMError(RuntimeError):
 class mm_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
                 ("E", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class mm_shared_expert(ctypes.Structure):
+    _fields_ = [("I", ctypes.c_int64), ("up_proj_weight", ctypes.c_void_p),
+                ("down_proj_weight", ctypes.c_void_p), ("d_up_proj_weight", ctypes.c_void_p),
+                ("d_down_proj_weight", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -61,6 +67,11 @@ def _lib():
         "mm_forward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_uint32]),
         "mm_backward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P,
                              _P, ctypes.c_uint32]),
+        "mm_workspace_size_se": (ctypes.c_size_t, [mm_dims, ctypes.c_int64, ctypes.c_uint32]),
+        "mm_forward_se": (st, [mm_dims, ctypes.POINTER(mm_shared_expert), _P, _P, _P, _P, _P, _P,
+                               _P, ctypes.c_size_t, _P, ctypes.c_uint32]),
+        "mm_backward_se": (st, [mm_dims, ctypes.POINTER(mm_shared_expert), _P, _P, _P, _P, _P, _P,
+                                _P, ctypes.c_size_t, _P, _P, _P, _P, _P, ctypes.c_uint32]),
         "mm_get_status": (st, [_P, _P]),
         "mm_routing_export": (st, [mm_dims, _P, _P, _P, _P, _P]),
         "mm_status_string": (ctypes.c_char_p, [st]),
@@ -104,6 +115,31 @@ def mm_backward(d, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weig
     return int(_lib().mm_backward(d, dy, x, topk_ids, topk_weights, up_proj_weight,
                                   down_proj_weight, workspace, workspace_bytes, dx, d_topk_weights,
                                   d_up_proj_weight, d_down_proj_weight, stream, flags))
+
+
+def shared_expert(I, up_proj_weight, down_proj_weight, d_up_proj_weight=0, d_down_proj_weight=0):
+    return mm_shared_expert(int(I), up_proj_weight, down_proj_weight, d_up_proj_weight,
+                            d_down_proj_weight)
+
+
+def mm_workspace_size_se(d: mm_dims, shared_I: int, flags: int = 0) -> int:
+    return int(_lib().mm_workspace_size_se(d, int(shared_I), flags))
+
+
+def mm_forward_se(d, se, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+                  workspace, workspace_bytes, stream=0, flags=0) -> int:
+    return int(_lib().mm_forward_se(d, ctypes.byref(se), x, topk_ids, topk_weights,
+                                    up_proj_weight, down_proj_weight, y, workspace,
+                                    workspace_bytes, stream, flags))
+
+
+def mm_backward_se(d, se, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                   workspace, workspace_bytes, dx, d_topk_weights, d_up_proj_weight,
+                   d_down_proj_weight, stream=0, flags=0) -> int:
+    return int(_lib().mm_backward_se(d, ctypes.byref(se), dy, x, topk_ids, topk_weights,
+                                     up_proj_weight, down_proj_weight, workspace, workspace_bytes,
+                                     dx, d_topk_weights, d_up_proj_weight, d_down_proj_weight,
+                                     stream, flags))
 
 
 def mm_get_status(workspace, stream=0) -> int:

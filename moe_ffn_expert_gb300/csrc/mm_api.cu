@@ -80,7 +80,7 @@ cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
 const char* kStageNames[ST_COUNT] = {
     "route_count", "route_scan",  "route_rank", "gather_x",   "gemm1_swiglu",
     "gemm2",       "combine_y",   "gather_dy",  "act_grad",   "d_topk",
-    "w2_grad",     "input_grad",  "combine_dx", "w1_grad"};
+    "w2_grad",     "input_grad",  "combine_dx", "w1_grad",    "shared_expert"};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -120,7 +120,7 @@ void note_error(const char* fmt, ...) {
   va_end(ap);
 }
 
-bool plan_workspace(const mm_dims& d, Workspace* w) {
+bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows) {
   if (!dims_ok(d)) return false;
   Workspace p{};
   p.T = d.T;
@@ -148,15 +148,16 @@ bool plan_workspace(const mm_dims& d, Workspace* w) {
   p.off_row_of_slot = take((size_t)p.S * sizeof(int32_t));
   p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
   p.off_w_row = take((size_t)p.S_pad * sizeof(float));
-  p.off_x_slot = take((size_t)p.S_pad * d.H * 2);
+  p.off_x_slot = take(direct_rows ? 0 : (size_t)p.S_pad * d.H * 2);
   p.off_gu = take((size_t)p.S_pad * 2 * d.I * 4);
   p.off_h = take((size_t)p.S_pad * d.I * 2);
   p.off_hw_lo = take((size_t)p.S_pad * d.I * 2);
   p.off_o = take((size_t)p.S_pad * d.H * 2);
-  p.off_dy_slot = take((size_t)p.S_pad * d.H * 2);
+  p.off_dy_slot = take(direct_rows ? 0 : (size_t)p.S_pad * d.H * 2);
   p.off_dgu = take((size_t)p.S_pad * 2 * d.I * 2);
   p.off_dgu_lo = take((size_t)p.S_pad * 2 * d.I * 2);
   p.off_p_part = take((size_t)p.n_act_tiles * p.S_pad * sizeof(float));
+  p.off_o_lo = take(direct_rows ? (size_t)p.S_pad * d.H * 2 : 0);
   p.total = off;
   *w = p;
   return true;
@@ -192,23 +193,53 @@ size_t mm_workspace_size(mm_dims d, uint32_t flags) {
   return w.total;
 }
 
-static mm_status check_common(const mm_dims& d, const void* ws, size_t ws_bytes, Workspace* w) {
+// The main layout, and with a shared expert its sub-workspace (sizes T, H, I_s, E = 1, K = 1,
+// no dispatched-row buffers) placed after it.
+struct Plan {
+  Workspace w;
+  bool shared = false;
+  Workspace ws_s;
+  size_t base_s = 0;
+  size_t total = 0;
+};
+
+static bool plan_all(const mm_dims& d, int64_t shared_I, Plan* p) {
+  if (!plan_workspace(d, &p->w)) return false;
+  p->total = p->w.total;
+  p->shared = shared_I > 0;
+  if (!p->shared) return true;
+  const mm_dims ds{d.T, d.H, shared_I, 1, 1};
+  if (!plan_workspace(ds, &p->ws_s, true)) return false;
+  p->base_s = align_up(p->w.total, 256);
+  p->total = p->base_s + p->ws_s.total;
+  return true;
+}
+
+static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, const void* ws,
+                              size_t ws_bytes, Plan* p) {
   if (d.T < 1 || d.H < 1 || d.I < 1 || d.E < 1 || d.K < 1) return MM_ERR_INVALID_ARG;
-  if (!plan_workspace(d, w)) return MM_ERR_UNSUPPORTED;
-  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < w->total) return MM_ERR_WORKSPACE;
+  if (se != nullptr && se->I < 1) return MM_ERR_INVALID_ARG;
+  if (!plan_all(d, se ? se->I : 0, p)) return MM_ERR_UNSUPPORTED;
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < p->total) return MM_ERR_WORKSPACE;
   return MM_OK;
 }
 
-mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const float* topk_weights,
-                     const void* up_proj_weight, const void* down_proj_weight, void* y,
-                     void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
-  Workspace w;
-  mm_status s = check_common(d, workspace, workspace_bytes, &w);
+static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const void* x,
+                              const int32_t* topk_ids, const float* topk_weights,
+                              const void* up_proj_weight, const void* down_proj_weight, void* y,
+                              void* workspace, size_t workspace_bytes, void* stream,
+                              uint32_t flags) {
+  Plan p;
+  mm_status s = check_common(d, se, workspace, workspace_bytes, &p);
   if (s != MM_OK) return s;
+  const Workspace& w = p.w;
   if (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !y)
     return MM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(up_proj_weight, 16) || !aligned(down_proj_weight, 16) ||
       !aligned(y, 16) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+    return MM_ERR_INVALID_ARG;
+  if (se && (!se->up_proj_weight || !se->down_proj_weight || !aligned(se->up_proj_weight, 16) ||
+             !aligned(se->down_proj_weight, 16)))
     return MM_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
@@ -230,24 +261,41 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const fl
                [&] { return launch_gather_rows(w, ws, x, ws + w.off_x_slot, st); }));
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
-             stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0};
+             stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
   MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.kind = GK_GEMM2;
   c.inject_stall = 0;
   MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
-  MM_TRY(timed(ST_COMBINE_Y, st,
-               [&] { return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st); }));
+  const void* extra = nullptr;
+  const void* extra_lo = nullptr;
+  if (p.shared) {  // the shared expert: identity routing over all tokens, weight 1
+    char* wss = ws + p.base_s;
+    GemmCall cs{GK_GEMM1_SWIGLU, se->up_proj_weight, se->down_proj_weight, nullptr,
+                c.timeout_ns, 0, 0, x, reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS,
+                1};  // its output is added with weight 1: kept as a bf16 hi + lo pair
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_shared_tables(p.ws_s, wss, st); }));
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+    cs.kind = GK_GEMM2;
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+    extra = wss + p.ws_s.off_o;
+    extra_lo = wss + p.ws_s.off_o_lo;
+  }
+  MM_TRY(timed(ST_COMBINE_Y, st, [&] {
+    return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo);
+  }));
   return MM_OK;
 }
 
-mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
-                      const float* topk_weights, const void* up_proj_weight,
-                      const void* down_proj_weight, void* workspace, size_t workspace_bytes,
-                      void* dx, float* d_topk_weights, void* d_up_proj_weight,
-                      void* d_down_proj_weight, void* stream, uint32_t flags) {
-  Workspace w;
-  mm_status s = check_common(d, workspace, workspace_bytes, &w);
+static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void* dy,
+                               const void* x, const int32_t* topk_ids, const float* topk_weights,
+                               const void* up_proj_weight, const void* down_proj_weight,
+                               void* workspace, size_t workspace_bytes, void* dx,
+                               float* d_topk_weights, void* d_up_proj_weight,
+                               void* d_down_proj_weight, void* stream, uint32_t flags) {
+  Plan p;
+  mm_status s = check_common(d, se, workspace, workspace_bytes, &p);
   if (s != MM_OK) return s;
+  const Workspace& w = p.w;
   if (!dy || !x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !dx ||
       !d_topk_weights || !d_up_proj_weight || !d_down_proj_weight)
     return MM_ERR_INVALID_ARG;
@@ -256,6 +304,11 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
       !aligned(d_down_proj_weight, 16) || !aligned(d_topk_weights, 4) || !aligned(topk_ids, 4) ||
       !aligned(topk_weights, 4))
     return MM_ERR_INVALID_ARG;
+  if (se && (!se->up_proj_weight || !se->down_proj_weight || !se->d_up_proj_weight ||
+             !se->d_down_proj_weight || !aligned(se->up_proj_weight, 16) ||
+             !aligned(se->down_proj_weight, 16) || !aligned(se->d_up_proj_weight, 16) ||
+             !aligned(se->d_down_proj_weight, 16)))
+    return MM_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* ws = reinterpret_cast<char*>(workspace);
   g_err[0] = 0;
@@ -263,7 +316,8 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
 
   MM_TRY(timed(ST_GATHER_DY, st,
                [&] { return launch_gather_rows(w, ws, dy, ws + w.off_dy_slot, st); }));
-  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0, 0};
+  GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0, 0,
+             nullptr, nullptr};
   const int accumulate = (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) ? 1 : 0;
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
@@ -275,13 +329,87 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
   c.d_w = nullptr;
   c.accumulate = 0;
   MM_TRY(timed(ST_INPUT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
-  MM_TRY(timed(ST_COMBINE_DX, st,
-               [&] { return launch_combine(w, ws, ws + w.off_o, nullptr, dx, st); }));
+  const void* extra = nullptr;
+  const void* extra_lo = nullptr;
+  char* wss = ws + p.base_s;
+  GemmCall cs{GK_ACT_GRAD, nullptr, nullptr, nullptr, kDefaultTimeoutNs, 0, 0, dy,
+              reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS, 1};
+  if (p.shared) {  // shared expert: act_grad, W2Grad (rows = dy), input_grad
+    cs.w_up = se->up_proj_weight;
+    cs.w_down = se->down_proj_weight;
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+    cs.kind = GK_W2_GRAD;
+    cs.d_w = se->d_down_proj_weight;
+    cs.accumulate = accumulate;
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+    cs.kind = GK_INPUT_GRAD;
+    cs.d_w = nullptr;
+    cs.accumulate = 0;
+    cs.rows = nullptr;
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+    extra = wss + p.ws_s.off_o;
+    extra_lo = wss + p.ws_s.off_o_lo;
+  }
+  MM_TRY(timed(ST_COMBINE_DX, st, [&] {
+    return launch_combine(w, ws, ws + w.off_o, nullptr, dx, st, extra, extra_lo);
+  }));
   c.kind = GK_W1_GRAD;
   c.d_w = d_up_proj_weight;
   c.accumulate = accumulate;
   MM_TRY(timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  if (p.shared) {  // shared expert W1Grad (rows = x)
+    cs.kind = GK_W1_GRAD;
+    cs.d_w = se->d_up_proj_weight;
+    cs.accumulate = accumulate;
+    cs.rows = x;
+    MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
+  }
   return MM_OK;
+}
+
+mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const float* topk_weights,
+                     const void* up_proj_weight, const void* down_proj_weight, void* y,
+                     void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
+  return forward_impl(d, nullptr, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+                      workspace, workspace_bytes, stream, flags);
+}
+
+mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
+                      const float* topk_weights, const void* up_proj_weight,
+                      const void* down_proj_weight, void* workspace, size_t workspace_bytes,
+                      void* dx, float* d_topk_weights, void* d_up_proj_weight,
+                      void* d_down_proj_weight, void* stream, uint32_t flags) {
+  return backward_impl(d, nullptr, dy, x, topk_ids, topk_weights, up_proj_weight,
+                       down_proj_weight, workspace, workspace_bytes, dx, d_topk_weights,
+                       d_up_proj_weight, d_down_proj_weight, stream, flags);
+}
+
+size_t mm_workspace_size_se(mm_dims d, int64_t shared_I, uint32_t flags) {
+  (void)flags;
+  Plan p;
+  if (shared_I < 1 || !plan_all(d, shared_I, &p)) return 0;
+  return p.total;
+}
+
+mm_status mm_forward_se(mm_dims d, const mm_shared_expert* se, const void* x,
+                        const int32_t* topk_ids, const float* topk_weights,
+                        const void* up_proj_weight, const void* down_proj_weight, void* y,
+                        void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
+  if (se == nullptr) return MM_ERR_INVALID_ARG;
+  return forward_impl(d, se, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+                      workspace, workspace_bytes, stream, flags);
+}
+
+mm_status mm_backward_se(mm_dims d, const mm_shared_expert* se, const void* dy, const void* x,
+                         const int32_t* topk_ids, const float* topk_weights,
+                         const void* up_proj_weight, const void* down_proj_weight,
+                         void* workspace, size_t workspace_bytes, void* dx,
+                         float* d_topk_weights, void* d_up_proj_weight, void* d_down_proj_weight,
+                         void* stream, uint32_t flags) {
+  if (se == nullptr) return MM_ERR_INVALID_ARG;
+  return backward_impl(d, se, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                       workspace, workspace_bytes, dx, d_topk_weights, d_up_proj_weight,
+                       d_down_proj_weight, stream, flags);
 }
 
 mm_status mm_get_status(const void* workspace, void* stream) {

@@ -60,10 +60,14 @@ constexpr int OUT_CHUNK_BYTES = 6 * OUT_PLANE_BYTES;  // d_gate, d_up, w*h; hi a
 
 // Store maps of the act_grad epilogue: [d_gate|d_up] hi and lo as [rows][2][I] (so a store
 // never crosses from the gate half into the up half), w*h hi and lo as [rows][I].
-struct alignas(64) EpiMaps {
+struct alignas(128) EpiMaps {
   CUtensorMap dgu_hi, dgu_lo, hw_hi, hw_lo;
   CUtensorMap out;  // the bf16 output of GEMM2, INPUT_GRAD and the weight gradients
+  CUtensorMap out_lo;  // its lo part (GEMM2 / INPUT_GRAD with split_out)
 };
+
+static_assert(offsetof(EpiMaps, out_lo) == offsetof(EpiMaps, out) + sizeof(CUtensorMap),
+              "the split output's lo map follows its hi map");
 
 constexpr int OUT_TILE_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16 of staged output (64-byte rows)
 static_assert(BK == 64, "one 128-byte swizzle row per k-block");
@@ -95,6 +99,7 @@ struct Args {
   uint64_t timeout_ns;
   int inject_stall;
   int accumulate;  // weight gradients: reduce-add into the output
+  int split_out;   // GEMM2 / INPUT_GRAD: store the output as bf16 hi and lo planes
 };
 
 template <int KIND>
@@ -447,7 +452,8 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
 // buffers (64-byte swizzle: 16-byte unit u of row r at unit u ^ ((r >> 1) & 3)) and stored with
 // TMA by lane 0; the tensor map clips rows and columns outside the output. `chunk_no` counts the
 // warp's chunks to alternate the buffers; before a buffer is rewritten, the store that used it
-// two chunks earlier must have finished reading it.
+// two chunks earlier must have finished reading it. With a.split_out (row-grouped kinds) the
+// chunk goes out as a bf16 hi tile through map[0] and its residual lo tile through map[1].
 template <int KIND>
 __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, uint32_t tacc,
                                                   int q, int hf, int lane, const CUtensorMap* map,
@@ -455,6 +461,39 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, 
                                                   uint32_t& chunk_no) {
   constexpr int NC = Traits<KIND>::TN / 64;  // 32-column chunks per half
   const int row0 = t.m0 + q * 32;
+  if constexpr (!Traits<KIND>::WGRAD) {
+    if (a.split_out) {  // hi in buffer 0, lo in buffer 1: both free before each chunk
+#pragma unroll 1
+      for (int c = hf * NC; c < hf * NC + NC; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32(tacc + c * 32, v);
+        tmem_ld_wait();
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        uint8_t* rowp = sbuf_ptr + lane * 64;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[8 * u + j]);
+          uint4 hi, lo;
+          split8_bf16(f, hi, lo);
+          const int off = (u ^ ((lane >> 1) & 3)) << 4;
+          *reinterpret_cast<uint4*>(rowp + off) = hi;
+          *reinterpret_cast<uint4*>(rowp + OUT_TILE_BYTES + off) = lo;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int n = t.n0 + c * 32;
+          tma_store_2d(map, sbuf, n, row0);
+          tma_store_2d(map + 1, sbuf + OUT_TILE_BYTES, n, row0);
+          bulk_commit();
+        }
+      }
+      return;
+    }
+  }
 #pragma unroll 1
   for (int c = hf * NC; c < hf * NC + NC; ++c) {
     uint32_t v[32];
@@ -807,7 +846,12 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
 
   Args a{};
   a.hdr = reinterpret_cast<const int*>(ws + w.off_hdr);
-  a.status = reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS;
+  a.status = c.status ? c.status : reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS;
+  // token rows: the dispatched (expert-sorted) copies, or x / dy themselves for the shared
+  // expert (T rows in token order; TMA zero-fills the pad rows past T)
+  const void* xrows = c.rows ? c.rows : ws + w.off_x_slot;
+  const void* dyrows = c.rows ? c.rows : ws + w.off_dy_slot;
+  const int64_t nrows = c.rows ? w.T : S_pad;
   a.tile_expert = reinterpret_cast<const int32_t*>(ws + w.off_tile_expert);
   a.poff = reinterpret_cast<const int32_t*>(ws + w.off_poff);
   a.E = (int)E;
@@ -824,7 +868,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   const int64_t m_tiles_max = S_pad / BM;
   switch (KIND) {
     case GK_GEMM1_SWIGLU:
-      ok = map_rows(&ta, ws + w.off_x_slot, H, S_pad, 64, BM) &&
+      ok = map_rows(&ta, xrows, H, nrows, 64, BM) &&
            map_experts(&tb, c.w_up, 2 * I, H, E, 64, 64);
       a.n_tiles_n = cdiv(I, BN / 2);
       a.k_iters = cdiv(H, BK);
@@ -842,6 +886,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.k_iters = cdiv(I, BK);
       a.N = (int)H;
       a.out0 = bf(w.off_o);
+      a.out1 = bf(w.off_o_lo);
       a.ld0 = H;
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
@@ -850,7 +895,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       const uint64_t gdims[2] = {(uint64_t)(2 * I), (uint64_t)S_pad};
       const uint64_t gstr[1] = {(uint64_t)(2 * I) * 4};
       const uint32_t gbox[2] = {16, 32};
-      ok = map_rows(&ta, ws + w.off_dy_slot, H, S_pad, 64, BM) &&
+      ok = map_rows(&ta, dyrows, H, nrows, 64, BM) &&
            map_experts(&tb, c.w_down, H, I, E, 64, BN) &&
            make_map(&tl, ws + w.off_gu, 2, gdims, gstr, gbox, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     CU_TENSOR_MAP_SWIZZLE_64B);
@@ -892,13 +937,14 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.k_iters = cdiv(2 * I, BK);
       a.N = (int)H;
       a.out0 = bf(w.off_o);  // dx_slot reuses the forward's o buffer
+      a.out1 = bf(w.off_o_lo);
       a.ld0 = H;
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
     case GK_W2_GRAD:
       ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, 64) &&
            map_rows(&tl, ws + w.off_hw_lo, I, S_pad, 64, 64) &&
-           map_rows(&tb, ws + w.off_dy_slot, H, S_pad, 64, 64);
+           map_rows(&tb, dyrows, H, nrows, 64, 64);
       has_lo = true;
       a.m_tiles_w = cdiv(I, BM);
       a.n_tiles_n = cdiv(H, Traits<GK_W2_GRAD>::TN);
@@ -910,7 +956,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       tiles_max = E * a.m_tiles_w * a.n_tiles_n;
       break;
     case GK_W1_GRAD:
-      ok = map_rows(&ta, ws + w.off_x_slot, H, S_pad, 64, 64) &&
+      ok = map_rows(&ta, xrows, H, nrows, 64, 64) &&
            map_rows(&tb, ws + w.off_dgu, 2 * I, S_pad, 64, 64) &&
            map_rows(&tl, ws + w.off_dgu_lo, 2 * I, S_pad, 64, 64);
       has_lo = true;
@@ -936,14 +982,22 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       const uint64_t s3[2] = {(uint64_t)a.ld0 * 2, (uint64_t)a.out_expert_stride * 2};
       const uint32_t b3[3] = {32, 32, 1};
       if (!make_map(&em.out, a.out0, 3, d3, s3, b3, BF, SW)) return cudaErrorInvalidValue;
+      em.out_lo = em.out;  // unused but initialised
     } else {  // [S_pad][N]
       const uint64_t d2[2] = {(uint64_t)a.N, (uint64_t)S_pad};
       const uint64_t s2[1] = {(uint64_t)a.ld0 * 2};
       const uint32_t b2[2] = {32, 32};
       if (!make_map(&em.out, a.out0, 2, d2, s2, b2, BF, SW)) return cudaErrorInvalidValue;
+      a.split_out = c.split_out ? 1 : 0;
+      if (a.split_out) {
+        if (w.off_o_lo == w.total) return cudaErrorInvalidValue;  // layout has no lo rows
+        if (!make_map(&em.out_lo, a.out1, 2, d2, s2, b2, BF, SW)) return cudaErrorInvalidValue;
+      } else {
+        em.out_lo = em.out;  // unused but initialised
+      }
     }
   } else {
-    em.out = ta;  // unused but initialised
+    em.out = em.out_lo = ta;  // unused but initialised
   }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
   k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);

@@ -16,9 +16,13 @@ cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, 
 // dst[r] = src[slot_of_row[r] / K] for every real row, zeros for pad rows.
 cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, void* dst,
                                cudaStream_t st);
-// out[t] = sum_k (weights ? weights[t,k] : 1) * rows[row_of_slot[t*K+k]], k ascending, fp32.
+// out[t] = sum_k (weights ? weights[t,k] : 1) * rows[row_of_slot[t*K+k]], k ascending, fp32,
+// plus extra[t] (weight 1) when extra is not null.
 cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
-                           void* out, cudaStream_t st);
+                           void* out, cudaStream_t st, const void* extra = nullptr,
+                           const void* extra_lo = nullptr);
+// Identity routing tables of the shared expert's sub-workspace (ws points at its base).
+cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st);
 // d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]].
 cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st);
 // Converts the padded row_of_slot table to positions in the unpadded expert-sorted order.
@@ -42,6 +46,9 @@ struct GemmCall {
   uint64_t timeout_ns;
   int inject_stall;    // test hook: withhold the first accumulator hand-off of CTA 0
   int accumulate;      // weight gradients: add into the output instead of overwriting it
+  const void* rows;    // if set: token rows read directly (T of them) instead of x_slot/dy_slot
+  int* status;         // if set: the status word errors are recorded in
+  int split_out;       // GEMM2 / INPUT_GRAD: write o as bf16 hi (off_o) + lo (off_o_lo) rows
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);

@@ -42,6 +42,7 @@ enum Stage {
   ST_INPUT_GRAD,
   ST_COMBINE_DX,
   ST_W1_GRAD,
+  ST_SHARED,  // every launch of the shared expert (forward and backward)
   ST_COUNT
 };
 static_assert(ST_COUNT == MM_NUM_STAGES, "stage table");
@@ -63,10 +64,13 @@ struct Workspace {
   size_t off_dgu;      // bf16 [S_pad, 2I]  hi part of [d_gate | d_up]
   size_t off_dgu_lo;   // bf16 [S_pad, 2I]  lo part of [d_gate | d_up]
   size_t off_p_part;   // fp32 [n_act_tiles, S_pad] per-column-half partials of <g, h>
+  size_t off_o_lo;     // bf16 [S_pad, H]   direct-row layout only: lo part of o / dx rows
   size_t total;
 };
 
-// Fills `w` for the sizes in `d`; returns false if the sizes are unsupported.
-bool plan_workspace(const mm_dims& d, Workspace* w);
+// Fills `w` for the sizes in `d`; returns false if the sizes are unsupported. With direct_rows
+// the layout has no dispatched-row buffers (x_slot, dy_slot): the shared expert's GEMMs read the
+// token rows of x and dy themselves (its routing is the identity).
+bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows = false);
 
 }  // namespace mm

@@ -201,9 +201,14 @@ __device__ __forceinline__ void acc8(float (&a)[8], float w, const uint4& v) {
 }
 
 // One warp per token, 8 columns (16 bytes) per lane per step, slots summed in k order.
+// `extra` (optional): one more row per token, row t, added with weight 1 after the K slots
+// (the shared expert's output, or its input-gradient rows), as a bf16 hi row plus, when
+// `extra_lo` is set, its bf16 lo row (hi + lo carries about 16 significant bits).
 __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
                                                  const int32_t* __restrict__ row_of_slot,
                                                  const float* __restrict__ weights,
+                                                 const uint4* __restrict__ extra,
+                                                 const uint4* __restrict__ extra_lo,
                                                  uint4* __restrict__ out, const int* hdr, int T,
                                                  int K, int vpr) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -221,6 +226,8 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
 #pragma unroll
     for (int k = 0; k < 16; ++k)
       if (k < K) acc8(a, w[k], __ldg(rows + (size_t)r[k] * vpr + i));
+    if (extra != nullptr) acc8(a, 1.0f, __ldg(extra + (size_t)t * vpr + i));
+    if (extra_lo != nullptr) acc8(a, 1.0f, __ldg(extra_lo + (size_t)t * vpr + i));
     uint4 o;
     o.x = pack_bf16(a[0], a[1]);
     o.y = pack_bf16(a[2], a[3]);
@@ -257,6 +264,31 @@ __global__ void __launch_bounds__(256) k_export_rows(const int32_t* __restrict__
   const int r = row_of_slot[s];
   const int e = tile_expert[r / BM];
   out[s] = r - poff[e] + offsets[e];
+}
+
+// Routing tables of the shared expert (one expert, every token, weight 1, identity order):
+// padded row r is token r (r < T), the rows up to the next multiple of BM are pad rows.
+__global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts, int32_t* offsets,
+                                                       int32_t* poff, int32_t* tile_expert,
+                                                       int32_t* slot_of_row, float* w_row,
+                                                       int32_t* row_of_slot, int T) {
+  const int Tp = (T + BM - 1) / BM * BM;
+  const int r = blockIdx.x * 256 + threadIdx.x;
+  if (r == 0) {
+    hdr[HDR_STATUS] = 0;
+    hdr[HDR_NUM_MTILES] = Tp / BM;
+    counts[0] = T;
+    offsets[0] = 0;
+    offsets[1] = T;
+    poff[0] = 0;
+    poff[1] = Tp;
+  }
+  if (r < Tp) {
+    if (r % BM == 0) tile_expert[r / BM] = 0;
+    slot_of_row[r] = r < T ? r : -1;
+    w_row[r] = r < T ? 1.0f : 0.0f;
+    if (r < T) row_of_slot[r] = r;
+  }
 }
 
 inline unsigned div_up(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
@@ -302,10 +334,13 @@ cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, vo
 }
 
 cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
-                           void* out, cudaStream_t st) {
+                           void* out, cudaStream_t st, const void* extra,
+                           const void* extra_lo) {
   const unsigned grid = div_up(w.T, 8);
   k_combine<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(rows),
                                   region<int32_t>(ws, w.off_row_of_slot), weights,
+                                  reinterpret_cast<const uint4*>(extra),
+                                  reinterpret_cast<const uint4*>(extra_lo),
                                   reinterpret_cast<uint4*>(out), region<int>(ws, w.off_hdr),
                                   (int)w.T, (int)w.K, (int)(w.H / 8));
   return cudaGetLastError();
@@ -317,6 +352,16 @@ cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStrea
                                  region<int32_t>(ws, w.off_row_of_slot), d_topk,
                                  region<int>(ws, w.off_hdr), (int)w.S, (int)w.n_act_tiles,
                                  w.S_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st) {
+  const Workspace& w = ws_shared;
+  k_shared_tables<<<div_up((w.T + BM - 1) / BM * BM, 256), 256, 0, st>>>(
+      region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_counts),
+      region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
+      region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
+      region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
   return cudaGetLastError();
 }
 

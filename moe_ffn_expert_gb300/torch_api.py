@@ -42,11 +42,13 @@ def check_inputs(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
 
 
 class Workspace:
-    """A caller-owned workspace buffer for one pending forward/backward pair."""
+    """A caller-owned workspace buffer for one pending forward/backward pair (with room for a
+    shared expert of intermediate size shared_I when given)."""
 
-    def __init__(self, T, H, I, E, K, device):
+    def __init__(self, T, H, I, E, K, device, shared_I=0):
         self.dims = _abi.dims(T, H, I, E, K)
-        self.nbytes = _abi.mm_workspace_size(self.dims)
+        self.nbytes = (_abi.mm_workspace_size_se(self.dims, shared_I) if shared_I
+                       else _abi.mm_workspace_size(self.dims))
         if self.nbytes == 0:
             raise ValueError(f"unsupported sizes T={T} H={H} I={I} E={E} K={K}")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
@@ -79,6 +81,49 @@ def backward(ws: Workspace, dy, x, topk_ids, topk_weights, up_proj_weight, down_
     return dx, d_topk, d_up, d_down
 
 
+class HyperMegaMoESharedFunction(torch.autograd.Function):
+    """The same with a shared expert (RFC §6.1): an always-on SwiGLU FFN merged at the combine."""
+
+    @staticmethod
+    def forward(ctx, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, shared_up,
+                shared_down):
+        T, H, I, E, K = check_inputs(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)
+        I_s = shared_down.shape[0]
+        if shared_up.shape != (H, 2 * I_s) or shared_down.shape != (I_s, H):
+            raise ValueError("expected shared_up_proj_weight[H,2I_s], shared_down_proj_weight[I_s,H]")
+        x = x.contiguous()
+        ids = topk_ids.to(torch.int32).contiguous()
+        w = topk_weights.to(torch.float32).contiguous()
+        wu, wd = up_proj_weight.contiguous(), down_proj_weight.contiguous()
+        su, sd = shared_up.contiguous(), shared_down.contiguous()
+        ws = Workspace(T, H, I, E, K, x.device, shared_I=I_s)
+        y = torch.empty_like(x)
+        se = _abi.shared_expert(I_s, _ptr(su), _ptr(sd))
+        _abi.check(_abi.mm_forward_se(ws.dims, se, _ptr(x), _ptr(ids), _ptr(w), _ptr(wu), _ptr(wd),
+                                      _ptr(y), ws.ptr, ws.nbytes, _stream(x.device), 0),
+                   "mm_forward_se")
+        ctx.ws = ws
+        ctx.wdtype = topk_weights.dtype
+        ctx.save_for_backward(x, ids, w, wu, wd, su, sd)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, ids, w, wu, wd, su, sd = ctx.saved_tensors
+        dy = dy.contiguous().to(torch.bfloat16)
+        dx, d_topk = torch.empty_like(x), torch.empty(ids.shape, dtype=torch.float32, device=x.device)
+        d_up, d_down = torch.empty_like(wu), torch.empty_like(wd)
+        ds_up, ds_down = torch.empty_like(su), torch.empty_like(sd)
+        se = _abi.shared_expert(sd.shape[0], _ptr(su), _ptr(sd), _ptr(ds_up), _ptr(ds_down))
+        ws = ctx.ws
+        _abi.check(_abi.mm_backward_se(ws.dims, se, _ptr(dy), _ptr(x), _ptr(ids), _ptr(w), _ptr(wu),
+                                       _ptr(wd), ws.ptr, ws.nbytes, _ptr(dx), _ptr(d_topk),
+                                       _ptr(d_up), _ptr(d_down), _stream(x.device), 0),
+                   "mm_backward_se")
+        ctx.ws = None
+        return dx, None, d_topk.to(ctx.wdtype), d_up, d_down, ds_up, ds_down
+
+
 class HyperMegaMoEFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
@@ -102,6 +147,14 @@ class HyperMegaMoEFunction(torch.autograd.Function):
         return dx, None, d_topk.to(ctx.wdtype), d_up, d_down
 
 
-def hyper_mega_moe(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
-    """y[T,H] = sum_k topk_weights[t,k] * SwiGLU-FFN_{topk_ids[t,k]}(x[t])."""
+def hyper_mega_moe(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, *,
+                   shared_up_proj_weight=None, shared_down_proj_weight=None):
+    """y[T,H] = sum_k topk_weights[t,k] * SwiGLU-FFN_{topk_ids[t,k]}(x[t])
+    (+ SwiGLU-FFN_shared(x[t]) when the keyword-only shared-expert weights are given)."""
+    if (shared_up_proj_weight is None) != (shared_down_proj_weight is None):
+        raise ValueError("give both shared-expert weights or neither")
+    if shared_up_proj_weight is not None:
+        return HyperMegaMoESharedFunction.apply(x, topk_ids, topk_weights, up_proj_weight,
+                                                down_proj_weight, shared_up_proj_weight,
+                                                shared_down_proj_weight)
     return HyperMegaMoEFunction.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)

@@ -62,6 +62,41 @@ def run_layer(inp, flags=0, ws=None, stream=None, backward=True, bwd_flags=0, d_
     return out
 
 
+def run_layer_se(inp, su, sd, flags=0, ws=None, backward=True, bwd_flags=0):
+    """Forward (+ backward) with a shared expert (su [H, 2*I_s], sd [I_s, H]) through the C ABI."""
+    x, ids, tw = inp["x"], inp["topk_ids"], inp["topk_weights"]
+    wu, wd = inp["w_up"], inp["w_down"]
+    T, H = x.shape
+    E, _, I2 = wu.shape
+    K = ids.shape[1]
+    I_s = sd.shape[0]
+    d = _abi.dims(T, H, I2 // 2, E, K)
+    nbytes = _abi.mm_workspace_size_se(d, I_s)
+    assert nbytes > 0
+    if ws is None:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    st = torch.cuda.current_stream().cuda_stream
+    ds_up, ds_down = torch.empty_like(su), torch.empty_like(sd)
+    se = _abi.shared_expert(I_s, su.data_ptr(), sd.data_ptr(), ds_up.data_ptr(), ds_down.data_ptr())
+    y = torch.empty_like(x)
+    _abi.check(_abi.mm_forward_se(d, se, x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
+                                  wd.data_ptr(), y.data_ptr(), ws.data_ptr(), nbytes, st, flags),
+               "mm_forward_se")
+    out = dict(y=y, ws=ws, dims=d)
+    if backward:
+        dx = torch.empty_like(x)
+        d_topk = torch.empty(T, K, dtype=torch.float32, device=x.device)
+        d_up, d_down = torch.empty_like(wu), torch.empty_like(wd)
+        _abi.check(_abi.mm_backward_se(d, se, inp["dy"].data_ptr(), x.data_ptr(), ids.data_ptr(),
+                                       tw.data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(),
+                                       nbytes, dx.data_ptr(), d_topk.data_ptr(), d_up.data_ptr(),
+                                       d_down.data_ptr(), st, bwd_flags), "mm_backward_se")
+        out.update(dx=dx, d_topk_weights=d_topk, dW_up=d_up, dW_down=d_down, dS_up=ds_up,
+                   dS_down=ds_down)
+    out["status"] = _abi.mm_get_status(ws.data_ptr(), st)
+    return out
+
+
 def export_routing(out, E, S):
     counts = torch.empty(E, dtype=torch.int32)
     offsets = torch.empty(E + 1, dtype=torch.int32)

@@ -61,6 +61,7 @@ BY_NAME = {w.name: w for w in WORKLOADS}
 
 # Stream identifiers (combined with the workload seed into a per-stream key).
 STREAM_X, STREAM_WUP, STREAM_WDOWN, STREAM_DY, STREAM_ROUTE, STREAM_TOPKW, STREAM_POS = range(1, 8)
+STREAM_SHARED_UP, STREAM_SHARED_DOWN = 8, 9
 
 
 def _mix32(x: torch.Tensor) -> torch.Tensor:
@@ -214,6 +215,16 @@ def w_down(w: Workload, device="cpu", expert=None) -> torch.Tensor:
     if expert is None:
         return normal_bf16(key, (w.E, w.I, w.H), 1.0 / math.sqrt(w.I), device)
     return normal_bf16(key, (w.I, w.H), 1.0 / math.sqrt(w.I), device, start=int(expert) * n)
+
+
+def shared_up(w: Workload, I_s: int, device="cpu") -> torch.Tensor:
+    """Shared expert's bf16 [H, 2*I_s] ~ N(0, 1/H), gate in the first I_s columns."""
+    return normal_bf16(stream_key(w.seed, STREAM_SHARED_UP), (w.H, 2 * I_s), 1.0 / math.sqrt(w.H), device)
+
+
+def shared_down(w: Workload, I_s: int, device="cpu") -> torch.Tensor:
+    """Shared expert's bf16 [I_s, H] ~ N(0, 1/I_s)."""
+    return normal_bf16(stream_key(w.seed, STREAM_SHARED_DOWN), (I_s, w.H), 1.0 / math.sqrt(I_s), device)
 
 
 class LazyExperts:
