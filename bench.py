@@ -194,7 +194,6 @@ def run_gpu(args):
     S = T * K
     d = _abi.dims(T, H, I, E, K)
     I_s = args.shared_intermediate
-    nbytes = _abi.mm_workspace_size_se(d, I_s) if I_s else _abi.mm_workspace_size(d)
     stream = torch.cuda.current_stream(dev)
     st = stream.cuda_stream
 
@@ -204,7 +203,6 @@ def run_gpu(args):
     dy = synth.dy(w, device=dev)
     wu = synth.w_up(w, device=dev)
     wd = synth.w_down(w, device=dev)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     y = torch.empty_like(x)
     dx = torch.empty_like(x)
     dtk = torch.empty(T, K, dtype=torch.float32, device=dev)
@@ -214,10 +212,13 @@ def run_gpu(args):
         su, sd = synth.shared_up(w, I_s, device=dev), synth.shared_down(w, I_s, device=dev)
         dsu, dsd = torch.empty_like(su), torch.empty_like(sd)
         se = _abi.shared_expert(I_s, su.data_ptr(), sd.data_ptr(), dsu.data_ptr(), dsd.data_ptr())
+        opt = _abi.options(se)
+    nbytes = _abi.mm_workspace_size_ex(d, opt) if I_s else _abi.mm_workspace_size(d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def fwd():
         if I_s:
-            _abi.check(_abi.mm_forward_se(d, se, x.data_ptr(), ids.data_ptr(), tw.data_ptr(),
+            _abi.check(_abi.mm_forward_ex(d, opt, x.data_ptr(), ids.data_ptr(), tw.data_ptr(),
                                           wu.data_ptr(), wd.data_ptr(), y.data_ptr(), ws.data_ptr(),
                                           nbytes, st, 0), "fwd")
             return
@@ -226,7 +227,7 @@ def run_gpu(args):
 
     def bwd():
         if I_s:
-            _abi.check(_abi.mm_backward_se(d, se, dy.data_ptr(), x.data_ptr(), ids.data_ptr(),
+            _abi.check(_abi.mm_backward_ex(d, opt, dy.data_ptr(), x.data_ptr(), ids.data_ptr(),
                                            tw.data_ptr(), wu.data_ptr(), wd.data_ptr(),
                                            ws.data_ptr(), nbytes, dx.data_ptr(), dtk.data_ptr(),
                                            du.data_ptr(), dd.data_ptr(), st, 0), "bwd")

@@ -19,6 +19,7 @@
  *   y, dy, dx         bf16 [T, H]
  *   d_topk_weights    fp32 [T, K]
  *   d_up_proj_weight  bf16 [E, H, 2I];  d_down_proj_weight bf16 [E, I, H]
+ *                     (fp32, same shapes, with MM_FLAG_FP32_WEIGHT_GRADS)
  *
  * Math: h_s = silu(x_t W_gate[e]) * (x_t W_up[e]) with silu(z) = z*sigmoid(z),
  * o_s = h_s W_down[e], y_t = sum_k topk_weights[t,k] * o_{t*K+k} (k ascending, fp32, rounded
@@ -54,7 +55,8 @@ typedef enum mm_status {
   MM_ERR_WORKSPACE = 3,     /* workspace null, misaligned or smaller than mm_workspace_size */
   MM_ERR_CUDA = 4,          /* a CUDA runtime call failed (no device, launch error, ...) */
   MM_ERR_BAD_EXPERT_ID = 5, /* some topk_ids entry is outside [0, E) (found on the device) */
-  MM_ERR_TIMEOUT = 6        /* a bounded device-side wait ran out */
+  MM_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out */
+  MM_ERR_TOKENS_PER_EXPERT = 7 /* a caller's tokens_per_expert differs from the ids' histogram */
 } mm_status;
 
 /* Layer sizes. Supported: T >= 1, H and I multiples of 8 (16-byte rows), 1 <= E <= 1024,
@@ -63,8 +65,9 @@ typedef struct mm_dims {
   int64_t T, H, I, E, K;
 } mm_dims;
 
-/* mm_forward flag: run the id check first and wait for it on the host (one device-to-host
- * read), returning MM_ERR_BAD_EXPERT_ID before any other kernel is enqueued. */
+/* mm_forward flag: run the id check (and the tokens_per_expert check of mm_forward_ex) first
+ * and wait for it on the host (one device-to-host read), returning MM_ERR_BAD_EXPERT_ID or
+ * MM_ERR_TOKENS_PER_EXPERT before any GEMM is enqueued. */
 #define MM_FLAG_VALIDATE_IDS 0x1u
 
 /* mm_backward flag: add the weight gradients into d_up_proj_weight and d_down_proj_weight
@@ -72,6 +75,12 @@ typedef struct mm_dims {
  * is done in bf16 by the stores themselves (one rounding of each addend and of each sum); experts
  * with no slot leave their slices unchanged. dx and d_topk_weights are still overwritten. */
 #define MM_FLAG_ACCUMULATE_WEIGHT_GRADS 0x2u
+
+/* mm_backward flag: the weight-gradient outputs (d_up_proj_weight, d_down_proj_weight and a shared
+ * expert's) are fp32 arrays of the same shapes instead of bf16, written straight from the fp32
+ * accumulators. With MM_FLAG_ACCUMULATE_WEIGHT_GRADS the stores add in fp32: gradient
+ * accumulation into fp32 "main grad" buffers with one rounding per addition. */
+#define MM_FLAG_FP32_WEIGHT_GRADS 0x4u
 
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
@@ -96,7 +105,7 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
                      size_t workspace_bytes, void* stream, uint32_t flags);
 
 /* Backward pass (RFC §2.2) for the forward that last used `workspace`, with upstream
- * gradient dy. Writes (overwrites, never accumulates):
+ * gradient dy. Writes (the weight gradients are added in with MM_FLAG_ACCUMULATE_WEIGHT_GRADS):
  *   dx                 = sum over k of the input_grad rows of the token's slots,
  *   d_topk_weights[t,k] = <dy[t], o_{t*K+k}>,
  *   d_up_proj_weight[e]  = x_slot_e^T [d_gate | d_up]   (zero for an expert with no slot),
@@ -117,25 +126,40 @@ typedef struct mm_shared_expert {
   int64_t I;                      /* shared intermediate size I_s (a multiple of 8) */
   const void* up_proj_weight;     /* bf16 [H, 2*I_s]: gate in columns [0, I_s), up in [I_s, 2*I_s) */
   const void* down_proj_weight;   /* bf16 [I_s, H] */
-  void* d_up_proj_weight;         /* bf16 [H, 2*I_s], written by mm_backward_se (unused forward) */
-  void* d_down_proj_weight;       /* bf16 [I_s, H], written by mm_backward_se (unused forward) */
+  void* d_up_proj_weight;         /* [H, 2*I_s], written by mm_backward_ex (unused forward) */
+  void* d_down_proj_weight;       /* [I_s, H], written by mm_backward_ex (unused forward);
+                                     both bf16, or fp32 with MM_FLAG_FP32_WEIGHT_GRADS */
 } mm_shared_expert;
 
-/* Workspace bytes for mm_forward_se / mm_backward_se with a shared expert of size shared_I
- * (0 if unsupported). The routed part's layout is the same as mm_workspace_size's, followed by
- * the shared expert's saved activations and scratch. */
-size_t mm_workspace_size_se(mm_dims d, int64_t shared_I, uint32_t flags);
+/* Optional inputs of the extended entry points. A NULL mm_options, or one whose fields are all
+ * NULL, means the plain mm_forward / mm_backward. */
+typedef struct mm_options {
+  /* A shared expert (NULL: none). The same one must be given to the workspace query, the forward
+   * and its backward. */
+  const mm_shared_expert* shared;
+  /* Forward only, NULL: none. The caller's per-expert slot histogram, device int32 [E], which the
+   * multicore usage guide lets a caller pass when it already has it. The layer still computes
+   * its own histogram (the routing tables need per-chunk counts) and only compares: a mismatch
+   * records MM_ERR_TOKENS_PER_EXPERT in the status word and the rest of the call does nothing. */
+  const int32_t* tokens_per_expert;
+} mm_options;
 
-/* mm_forward with a shared expert `se` (not NULL). Same arguments, errors and workspace rule. */
-mm_status mm_forward_se(mm_dims d, const mm_shared_expert* se, const void* x,
+/* Workspace bytes for mm_forward_ex / mm_backward_ex with options `opt` (0 if unsupported). The
+ * routed part's layout is the same as mm_workspace_size's, followed, with a shared expert, by its
+ * saved activations and scratch. */
+size_t mm_workspace_size_ex(mm_dims d, const mm_options* opt, uint32_t flags);
+
+/* mm_forward with options: same arguments, errors and workspace rule. */
+mm_status mm_forward_ex(mm_dims d, const mm_options* opt, const void* x,
                         const int32_t* topk_ids, const float* topk_weights,
                         const void* up_proj_weight, const void* down_proj_weight, void* y,
                         void* workspace, size_t workspace_bytes, void* stream, uint32_t flags);
 
-/* mm_backward with a shared expert `se`: also writes se->d_up_proj_weight and
- * se->d_down_proj_weight (accumulated with MM_FLAG_ACCUMULATE_WEIGHT_GRADS) and adds the shared
- * expert's input gradient into dx. The workspace must come from mm_forward_se with the same se. */
-mm_status mm_backward_se(mm_dims d, const mm_shared_expert* se, const void* dy, const void* x,
+/* mm_backward with options. With a shared expert it also writes opt->shared->d_up_proj_weight and
+ * d_down_proj_weight (subject to the same flags as the routed weight gradients) and adds the
+ * shared expert's input gradient into dx. The workspace must come from mm_forward_ex with the
+ * same shared expert. */
+mm_status mm_backward_ex(mm_dims d, const mm_options* opt, const void* dy, const void* x,
                          const int32_t* topk_ids, const float* topk_weights,
                          const void* up_proj_weight, const void* down_proj_weight,
                          void* workspace, size_t workspace_bytes, void* dx,
@@ -143,7 +167,8 @@ mm_status mm_backward_se(mm_dims d, const mm_shared_expert* se, const void* dy, 
                          void* stream, uint32_t flags);
 
 /* Synchronises `stream`, then returns the device-side status word of `workspace`
- * (MM_OK, MM_ERR_BAD_EXPERT_ID or MM_ERR_TIMEOUT), or MM_ERR_CUDA if the stream failed.
+ * (MM_OK, MM_ERR_BAD_EXPERT_ID, MM_ERR_TOKENS_PER_EXPERT or MM_ERR_TIMEOUT), or MM_ERR_CUDA if
+ * the stream failed.
  * The word is cleared at the start of every mm_forward. */
 mm_status mm_get_status(const void* workspace, void* stream);
 

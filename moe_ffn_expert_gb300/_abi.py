@@ -21,13 +21,16 @@ MM_ERR_WORKSPACE = 3
 MM_ERR_CUDA = 4
 MM_ERR_BAD_EXPERT_ID = 5
 MM_ERR_TIMEOUT = 6
+MM_ERR_TOKENS_PER_EXPERT = 7
 MM_FLAG_VALIDATE_IDS = 0x1
 MM_FLAG_TEST_STALL = 0x80000000
 MM_FLAG_ACCUMULATE_WEIGHT_GRADS = 0x2
+MM_FLAG_FP32_WEIGHT_GRADS = 0x4
 MM_NUM_STAGES = 15
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",
-                4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT"}
+                4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT",
+                7: "MM_ERR_TOKENS_PER_EXPERT"}
 
 
 class MMError(RuntimeError):
@@ -49,6 +52,11 @@ class mm_shared_expert(ctypes.Structure):
                 ("d_down_proj_weight", ctypes.c_void_p)]
 
 
+class mm_options(ctypes.Structure):
+    _fields_ = [("shared", ctypes.POINTER(mm_shared_expert)),
+                ("tokens_per_expert", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _LIB = None
 
@@ -67,10 +75,11 @@ def _lib():
         "mm_forward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_uint32]),
         "mm_backward": (st, [mm_dims, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P, _P,
                              _P, ctypes.c_uint32]),
-        "mm_workspace_size_se": (ctypes.c_size_t, [mm_dims, ctypes.c_int64, ctypes.c_uint32]),
-        "mm_forward_se": (st, [mm_dims, ctypes.POINTER(mm_shared_expert), _P, _P, _P, _P, _P, _P,
+        "mm_workspace_size_ex": (ctypes.c_size_t, [mm_dims, ctypes.POINTER(mm_options),
+                                                   ctypes.c_uint32]),
+        "mm_forward_ex": (st, [mm_dims, ctypes.POINTER(mm_options), _P, _P, _P, _P, _P, _P,
                                _P, ctypes.c_size_t, _P, ctypes.c_uint32]),
-        "mm_backward_se": (st, [mm_dims, ctypes.POINTER(mm_shared_expert), _P, _P, _P, _P, _P, _P,
+        "mm_backward_ex": (st, [mm_dims, ctypes.POINTER(mm_options), _P, _P, _P, _P, _P, _P,
                                 _P, ctypes.c_size_t, _P, _P, _P, _P, _P, ctypes.c_uint32]),
         "mm_get_status": (st, [_P, _P]),
         "mm_routing_export": (st, [mm_dims, _P, _P, _P, _P, _P]),
@@ -122,21 +131,31 @@ def shared_expert(I, up_proj_weight, down_proj_weight, d_up_proj_weight=0, d_dow
                             d_down_proj_weight)
 
 
-def mm_workspace_size_se(d: mm_dims, shared_I: int, flags: int = 0) -> int:
-    return int(_lib().mm_workspace_size_se(d, int(shared_I), flags))
+def options(shared=None, tokens_per_expert=0) -> mm_options:
+    """An mm_options; `shared` is an mm_shared_expert (kept alive by the returned object)."""
+    o = mm_options(ctypes.pointer(shared) if shared is not None else None, tokens_per_expert or None)
+    o._keep = shared
+    return o
 
 
-def mm_forward_se(d, se, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
+def _opt(opt):
+    return ctypes.byref(opt) if opt is not None else None
+
+
+def mm_workspace_size_ex(d: mm_dims, opt=None, flags: int = 0) -> int:
+    return int(_lib().mm_workspace_size_ex(d, _opt(opt), flags))
+
+
+def mm_forward_ex(d, opt, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
                   workspace, workspace_bytes, stream=0, flags=0) -> int:
-    return int(_lib().mm_forward_se(d, ctypes.byref(se), x, topk_ids, topk_weights,
-                                    up_proj_weight, down_proj_weight, y, workspace,
-                                    workspace_bytes, stream, flags))
+    return int(_lib().mm_forward_ex(d, _opt(opt), x, topk_ids, topk_weights, up_proj_weight,
+                                    down_proj_weight, y, workspace, workspace_bytes, stream, flags))
 
 
-def mm_backward_se(d, se, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+def mm_backward_ex(d, opt, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
                    workspace, workspace_bytes, dx, d_topk_weights, d_up_proj_weight,
                    d_down_proj_weight, stream=0, flags=0) -> int:
-    return int(_lib().mm_backward_se(d, ctypes.byref(se), dy, x, topk_ids, topk_weights,
+    return int(_lib().mm_backward_ex(d, _opt(opt), dy, x, topk_ids, topk_weights,
                                      up_proj_weight, down_proj_weight, workspace, workspace_bytes,
                                      dx, d_topk_weights, d_up_proj_weight, d_down_proj_weight,
                                      stream, flags))

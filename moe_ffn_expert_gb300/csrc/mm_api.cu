@@ -169,7 +169,7 @@ using namespace mm;
 
 extern "C" {
 
-int mm_abi_version(void) { return 1; }
+int mm_abi_version(void) { return 2; }
 
 const char* mm_last_error_detail(void) { return g_err; }
 
@@ -182,6 +182,7 @@ const char* mm_status_string(mm_status s) {
     case MM_ERR_CUDA: return "CUDA runtime error";
     case MM_ERR_BAD_EXPERT_ID: return "expert id out of range";
     case MM_ERR_TIMEOUT: return "device-side wait timed out";
+    case MM_ERR_TOKENS_PER_EXPERT: return "tokens_per_expert does not match topk_ids";
   }
   return "unknown status";
 }
@@ -224,7 +225,8 @@ static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, cons
   return MM_OK;
 }
 
-static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const void* x,
+static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32_t* tpe,
+                              const void* x,
                               const int32_t* topk_ids, const float* topk_weights,
                               const void* up_proj_weight, const void* down_proj_weight, void* y,
                               void* workspace, size_t workspace_bytes, void* stream,
@@ -248,13 +250,13 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const void*
 
   MM_TRY(cudaMemsetAsync(ws + w.off_hdr, 0, HDR_WORDS * sizeof(int32_t), st));
   MM_TRY(timed(ST_ROUTE_COUNT, st, [&] { return launch_route_count(w, ws, topk_ids, st); }));
+  MM_TRY(timed(ST_ROUTE_SCAN, st, [&] { return launch_route_scan(w, ws, tpe, st); }));
   if (flags & MM_FLAG_VALIDATE_IDS) {
     int32_t status = 0;
     MM_TRY(cudaMemcpyAsync(&status, ws + w.off_hdr, sizeof(status), cudaMemcpyDeviceToHost, st));
     MM_TRY(cudaStreamSynchronize(st));
     if (status != 0) return static_cast<mm_status>(status);
   }
-  MM_TRY(timed(ST_ROUTE_SCAN, st, [&] { return launch_route_scan(w, ws, st); }));
   MM_TRY(timed(ST_ROUTE_RANK, st,
                [&] { return launch_route_rank(w, ws, topk_ids, topk_weights, st); }));
   MM_TRY(timed(ST_GATHER_X, st,
@@ -319,6 +321,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   GemmCall c{GK_ACT_GRAD, up_proj_weight, down_proj_weight, nullptr, kDefaultTimeoutNs, 0, 0,
              nullptr, nullptr};
   const int accumulate = (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) ? 1 : 0;
+  c.wgrad_f32 = (flags & MM_FLAG_FP32_WEIGHT_GRADS) ? 1 : 0;
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;
@@ -333,7 +336,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   const void* extra_lo = nullptr;
   char* wss = ws + p.base_s;
   GemmCall cs{GK_ACT_GRAD, nullptr, nullptr, nullptr, kDefaultTimeoutNs, 0, 0, dy,
-              reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS, 1};
+              reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS, 1, c.wgrad_f32};
   if (p.shared) {  // shared expert: act_grad, W2Grad (rows = dy), input_grad
     cs.w_up = se->up_proj_weight;
     cs.w_down = se->down_proj_weight;
@@ -370,8 +373,8 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
 mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids, const float* topk_weights,
                      const void* up_proj_weight, const void* down_proj_weight, void* y,
                      void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
-  return forward_impl(d, nullptr, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
-                      workspace, workspace_bytes, stream, flags);
+  return forward_impl(d, nullptr, nullptr, x, topk_ids, topk_weights, up_proj_weight,
+                      down_proj_weight, y, workspace, workspace_bytes, stream, flags);
 }
 
 mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
@@ -384,32 +387,35 @@ mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* t
                        d_up_proj_weight, d_down_proj_weight, stream, flags);
 }
 
-size_t mm_workspace_size_se(mm_dims d, int64_t shared_I, uint32_t flags) {
+size_t mm_workspace_size_ex(mm_dims d, const mm_options* opt, uint32_t flags) {
   (void)flags;
+  const mm_shared_expert* se = opt ? opt->shared : nullptr;
+  if (se != nullptr && se->I < 1) return 0;
   Plan p;
-  if (shared_I < 1 || !plan_all(d, shared_I, &p)) return 0;
+  if (!plan_all(d, se ? se->I : 0, &p)) return 0;
   return p.total;
 }
 
-mm_status mm_forward_se(mm_dims d, const mm_shared_expert* se, const void* x,
+mm_status mm_forward_ex(mm_dims d, const mm_options* opt, const void* x,
                         const int32_t* topk_ids, const float* topk_weights,
                         const void* up_proj_weight, const void* down_proj_weight, void* y,
                         void* workspace, size_t workspace_bytes, void* stream, uint32_t flags) {
-  if (se == nullptr) return MM_ERR_INVALID_ARG;
-  return forward_impl(d, se, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y,
-                      workspace, workspace_bytes, stream, flags);
+  if (opt && opt->tokens_per_expert && !aligned(opt->tokens_per_expert, 4))
+    return MM_ERR_INVALID_ARG;
+  return forward_impl(d, opt ? opt->shared : nullptr, opt ? opt->tokens_per_expert : nullptr, x,
+                      topk_ids, topk_weights, up_proj_weight, down_proj_weight, y, workspace,
+                      workspace_bytes, stream, flags);
 }
 
-mm_status mm_backward_se(mm_dims d, const mm_shared_expert* se, const void* dy, const void* x,
+mm_status mm_backward_ex(mm_dims d, const mm_options* opt, const void* dy, const void* x,
                          const int32_t* topk_ids, const float* topk_weights,
                          const void* up_proj_weight, const void* down_proj_weight,
                          void* workspace, size_t workspace_bytes, void* dx,
                          float* d_topk_weights, void* d_up_proj_weight, void* d_down_proj_weight,
                          void* stream, uint32_t flags) {
-  if (se == nullptr) return MM_ERR_INVALID_ARG;
-  return backward_impl(d, se, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
-                       workspace, workspace_bytes, dx, d_topk_weights, d_up_proj_weight,
-                       d_down_proj_weight, stream, flags);
+  return backward_impl(d, opt ? opt->shared : nullptr, dy, x, topk_ids, topk_weights,
+                       up_proj_weight, down_proj_weight, workspace, workspace_bytes, dx,
+                       d_topk_weights, d_up_proj_weight, d_down_proj_weight, stream, flags);
 }
 
 mm_status mm_get_status(const void* workspace, void* stream) {

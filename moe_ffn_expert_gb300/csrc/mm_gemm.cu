@@ -84,7 +84,7 @@ struct Args {
   int N;           // valid output columns
   int M;           // weight-gradient kinds: valid output rows
   int I;           // intermediate size
-  void* out0;  // bf16, except fp32 gate|up of GEMM1
+  void* out0;  // bf16, except fp32 gate|up of GEMM1 and fp32 weight gradients (wgrad_f32)
   int64_t ld0;
   __nv_bfloat16* out1;
   int64_t ld1;
@@ -100,6 +100,7 @@ struct Args {
   int inject_stall;
   int accumulate;  // weight gradients: reduce-add into the output
   int split_out;   // GEMM2 / INPUT_GRAD: store the output as bf16 hi and lo planes
+  int wgrad_f32;   // weight gradients: fp32 output (else bf16)
 };
 
 template <int KIND>
@@ -279,12 +280,18 @@ template <int KIND>
 __device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r, int hf) {
   const int m = t.m0 + r;
   if (m >= a.M) return;
-  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
-                     (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+  constexpr int NC = Traits<KIND>::TN / 64;
+  const int64_t row = (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
+  if (a.wgrad_f32) {  // fp32 rows: 4 columns per 16-byte store (N is a multiple of 8)
+    float* o = reinterpret_cast<float*>(a.out0) + row;
+    for (int n = t.n0 + hf * NC * 32; n < t.n0 + (hf + 1) * NC * 32 && n < a.N; n += 4)
+      *reinterpret_cast<float4*>(o + n) = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) + row;
   float z[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) z[j] = 0.f;
-  constexpr int NC = Traits<KIND>::TN / 64;
   for (int c = hf * NC; c < hf * NC + NC; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
 }
 
@@ -488,6 +495,33 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, 
           const int n = t.n0 + c * 32;
           tma_store_2d(map, sbuf, n, row0);
           tma_store_2d(map + 1, sbuf + OUT_TILE_BYTES, n, row0);
+          bulk_commit();
+        }
+      }
+      return;
+    }
+  } else {
+    if (a.wgrad_f32) {  // 32 rows x 32 fp32 (128-byte rows, 128-byte swizzle) in both buffers
+#pragma unroll 1
+      for (int c = hf * NC; c < hf * NC + NC; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32(tacc + c * 32, v);
+        tmem_ld_wait();
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        uint8_t* rowp = sbuf_ptr + lane * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int n = t.n0 + c * 32;
+          if (a.accumulate)
+            tma_reduce_add_3d(map, sbuf, n, row0, t.e);
+          else
+            tma_store_3d(map, sbuf, n, row0, t.e);
           bulk_commit();
         }
       }
@@ -977,11 +1011,16 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
     // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_64B;
-    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N]
+    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N], bf16 or fp32 (128-byte swizzle)
+      a.wgrad_f32 = c.wgrad_f32 ? 1 : 0;
+      const uint64_t es = a.wgrad_f32 ? 4 : 2;
       const uint64_t d3[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)E};
-      const uint64_t s3[2] = {(uint64_t)a.ld0 * 2, (uint64_t)a.out_expert_stride * 2};
+      const uint64_t s3[2] = {(uint64_t)a.ld0 * es, (uint64_t)a.out_expert_stride * es};
       const uint32_t b3[3] = {32, 32, 1};
-      if (!make_map(&em.out, a.out0, 3, d3, s3, b3, BF, SW)) return cudaErrorInvalidValue;
+      if (!make_map(&em.out, a.out0, 3, d3, s3, b3,
+                    a.wgrad_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : BF,
+                    a.wgrad_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : SW))
+        return cudaErrorInvalidValue;
       em.out_lo = em.out;  // unused but initialised
     } else {  // [S_pad][N]
       const uint64_t d2[2] = {(uint64_t)a.N, (uint64_t)S_pad};

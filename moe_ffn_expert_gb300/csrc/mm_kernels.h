@@ -10,7 +10,10 @@ namespace mm {
 
 // ---- routing, dispatch and combine (mm_route.cu)
 cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids, cudaStream_t st);
-cudaError_t launch_route_scan(const Workspace& w, char* ws, cudaStream_t st);
+// tokens_per_expert (optional, device int32 [E]): compared with the computed counts; a
+// mismatch records MM_ERR_TOKENS_PER_EXPERT in the status word.
+cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* tokens_per_expert,
+                              cudaStream_t st);
 cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
                               cudaStream_t st);
 // dst[r] = src[slot_of_row[r] / K] for every real row, zeros for pad rows.
@@ -49,6 +52,7 @@ struct GemmCall {
   const void* rows;    // if set: token rows read directly (T of them) instead of x_slot/dy_slot
   int* status;         // if set: the status word errors are recorded in
   int split_out;       // GEMM2 / INPUT_GRAD: write o as bf16 hi (off_o) + lo (off_o_lo) rows
+  int wgrad_f32;       // weight gradients: fp32 output arrays (else bf16)
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);

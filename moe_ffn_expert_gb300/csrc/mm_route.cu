@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      int32_t* __restrict__ poff,
                                                      int32_t* __restrict__ tile_expert,
                                                      int32_t* __restrict__ slot_of_row,
-                                                     float* __restrict__ w_row, int E,
+                                                     float* __restrict__ w_row,
+                                                     const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks) {
   __shared__ int wsum[32], wsum_p[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -77,6 +78,9 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   int c = 0;
   if (tid < E)
     for (int k = 0; k < n_chunks; ++k) c += chunk_cnt[(size_t)k * E + tid];
+  // a caller's histogram is only compared, never used for addressing
+  if (tpe != nullptr && tid < E && __ldg(tpe + tid) != c)
+    set_status(hdr + HDR_STATUS, MM_ERR_TOKENS_PER_EXPERT);
   const int pc = (c + BM - 1) / BM * BM;
   int a = c, b = pc;  // inclusive warp scans
 #pragma unroll
@@ -303,13 +307,14 @@ cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids,
   return cudaGetLastError();
 }
 
-cudaError_t launch_route_scan(const Workspace& w, char* ws, cudaStream_t st) {
+cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* tokens_per_expert,
+                              cudaStream_t st) {
   k_route_scan<<<1, 1024, 0, st>>>(
       region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
       region<int32_t>(ws, w.off_counts), region<int32_t>(ws, w.off_offsets),
       region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_tile_expert),
-      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row), (int)w.E,
-      (int)w.n_chunks);
+      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row), tokens_per_expert,
+      (int)w.E, (int)w.n_chunks);
   return cudaGetLastError();
 }
 

@@ -47,10 +47,10 @@ class Workspace:
 
     def __init__(self, T, H, I, E, K, device, shared_I=0):
         self.dims = _abi.dims(T, H, I, E, K)
-        self.nbytes = (_abi.mm_workspace_size_se(self.dims, shared_I) if shared_I
-                       else _abi.mm_workspace_size(self.dims))
+        opt = _abi.options(_abi.shared_expert(shared_I, 0, 0)) if shared_I else None
+        self.nbytes = _abi.mm_workspace_size_ex(self.dims, opt)
         if self.nbytes == 0:
-            raise ValueError(f"unsupported sizes T={T} H={H} I={I} E={E} K={K}")
+            raise ValueError(f"unsupported sizes T={T} H={H} I={I} E={E} K={K} I_s={shared_I}")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
 
     @property
@@ -58,103 +58,113 @@ class Workspace:
         return self.buf.data_ptr()
 
 
+def _options(shared=None, tokens_per_expert=None):
+    """mm_options for (shared_up, shared_down[, d_shared_up, d_shared_down]) and a tokens_per_expert
+    tensor (device int32 [E]), or None when neither is given."""
+    if shared is None and tokens_per_expert is None:
+        return None
+    se = None
+    if shared is not None:
+        su, sd, *grads = shared
+        dsu, dsd = grads if grads else (None, None)
+        se = _abi.shared_expert(sd.shape[0], _ptr(su), _ptr(sd), _ptr(dsu) if dsu is not None else 0,
+                                _ptr(dsd) if dsd is not None else 0)
+    return _abi.options(se, _ptr(tokens_per_expert) if tokens_per_expert is not None else 0)
+
+
 def forward(ws: Workspace, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, y=None,
-            flags: int = 0):
+            flags: int = 0, shared=None, tokens_per_expert=None):
+    """One mm_forward(_ex) on the current stream; `shared` = (shared_up, shared_down)."""
     if y is None:
         y = torch.empty_like(x)
-    st = _abi.mm_forward(ws.dims, _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(up_proj_weight),
-                         _ptr(down_proj_weight), _ptr(y), ws.ptr, ws.nbytes, _stream(x.device), flags)
+    st = _abi.mm_forward_ex(ws.dims, _options(shared, tokens_per_expert), _ptr(x), _ptr(topk_ids),
+                            _ptr(topk_weights), _ptr(up_proj_weight), _ptr(down_proj_weight), _ptr(y),
+                            ws.ptr, ws.nbytes, _stream(x.device), flags)
     _abi.check(st, "mm_forward")
     return y
 
 
 def backward(ws: Workspace, dy, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
-             dx=None, d_topk=None, d_up=None, d_down=None):
+             dx=None, d_topk=None, d_up=None, d_down=None, flags: int = 0, shared=None,
+             d_shared=None):
+    """One mm_backward(_ex). Returns dx, d_topk, d_up, d_down (+ d_shared_up, d_shared_down)."""
+    gdt = torch.float32 if flags & _abi.MM_FLAG_FP32_WEIGHT_GRADS else torch.bfloat16
     dx = torch.empty_like(x) if dx is None else dx
     d_topk = torch.empty(topk_ids.shape, dtype=torch.float32, device=x.device) if d_topk is None else d_topk
-    d_up = torch.empty_like(up_proj_weight) if d_up is None else d_up
-    d_down = torch.empty_like(down_proj_weight) if d_down is None else d_down
-    st = _abi.mm_backward(ws.dims, _ptr(dy), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
-                          _ptr(up_proj_weight), _ptr(down_proj_weight), ws.ptr, ws.nbytes, _ptr(dx),
-                          _ptr(d_topk), _ptr(d_up), _ptr(d_down), _stream(x.device), 0)
+    d_up = torch.empty(up_proj_weight.shape, dtype=gdt, device=x.device) if d_up is None else d_up
+    d_down = torch.empty(down_proj_weight.shape, dtype=gdt, device=x.device) if d_down is None else d_down
+    if shared is not None and d_shared is None:
+        d_shared = tuple(torch.empty(t.shape, dtype=gdt, device=x.device) for t in shared)
+    opt = _options((*shared, *d_shared) if shared is not None else None)
+    st = _abi.mm_backward_ex(ws.dims, opt, _ptr(dy), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                             _ptr(up_proj_weight), _ptr(down_proj_weight), ws.ptr, ws.nbytes,
+                             _ptr(dx), _ptr(d_topk), _ptr(d_up), _ptr(d_down), _stream(x.device),
+                             flags)
     _abi.check(st, "mm_backward")
+    if shared is not None:
+        return dx, d_topk, d_up, d_down, d_shared[0], d_shared[1]
     return dx, d_topk, d_up, d_down
 
 
-class HyperMegaMoESharedFunction(torch.autograd.Function):
-    """The same with a shared expert (RFC §6.1): an always-on SwiGLU FFN merged at the combine."""
+class HyperMegaMoEFunction(torch.autograd.Function):
+    """Forward and backward of the layer (RFC §3.2); optional shared expert (RFC §6.1) and
+    caller histogram (usage guide, tokens_per_expert)."""
 
     @staticmethod
     def forward(ctx, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, shared_up,
-                shared_down):
+                shared_down, tokens_per_expert):
         T, H, I, E, K = check_inputs(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)
-        I_s = shared_down.shape[0]
-        if shared_up.shape != (H, 2 * I_s) or shared_down.shape != (I_s, H):
-            raise ValueError("expected shared_up_proj_weight[H,2I_s], shared_down_proj_weight[I_s,H]")
+        shared = None
+        I_s = 0
+        if shared_up is not None:
+            I_s = shared_down.shape[0]
+            if shared_up.shape != (H, 2 * I_s) or shared_down.shape != (I_s, H):
+                raise ValueError("expected shared_up_proj_weight[H,2I_s], shared_down_proj_weight[I_s,H]")
+            if shared_up.dtype != torch.bfloat16 or shared_down.dtype != torch.bfloat16:
+                raise TypeError("shared-expert weights must be bfloat16")
+            shared = (shared_up.contiguous(), shared_down.contiguous())
+        tpe = None
+        if tokens_per_expert is not None:
+            if tokens_per_expert.shape != (E,) or tokens_per_expert.device != x.device:
+                raise ValueError("tokens_per_expert must be a [E] tensor on x's device")
+            tpe = tokens_per_expert.to(torch.int32).contiguous()
         x = x.contiguous()
         ids = topk_ids.to(torch.int32).contiguous()
         w = topk_weights.to(torch.float32).contiguous()
         wu, wd = up_proj_weight.contiguous(), down_proj_weight.contiguous()
-        su, sd = shared_up.contiguous(), shared_down.contiguous()
         ws = Workspace(T, H, I, E, K, x.device, shared_I=I_s)
-        y = torch.empty_like(x)
-        se = _abi.shared_expert(I_s, _ptr(su), _ptr(sd))
-        _abi.check(_abi.mm_forward_se(ws.dims, se, _ptr(x), _ptr(ids), _ptr(w), _ptr(wu), _ptr(wd),
-                                      _ptr(y), ws.ptr, ws.nbytes, _stream(x.device), 0),
-                   "mm_forward_se")
+        # with a caller histogram the id and histogram checks are waited for, so that a mismatch
+        # raises here instead of leaving y unspecified
+        flags = _abi.MM_FLAG_VALIDATE_IDS if tpe is not None else 0
+        y = forward(ws, x, ids, w, wu, wd, flags=flags, shared=shared, tokens_per_expert=tpe)
         ctx.ws = ws
         ctx.wdtype = topk_weights.dtype
-        ctx.save_for_backward(x, ids, w, wu, wd, su, sd)
+        ctx.has_shared = shared is not None
+        ctx.save_for_backward(x, ids, w, wu, wd, *(shared or ()))
         return y
 
     @staticmethod
     def backward(ctx, dy):
-        x, ids, w, wu, wd, su, sd = ctx.saved_tensors
-        dy = dy.contiguous().to(torch.bfloat16)
-        dx, d_topk = torch.empty_like(x), torch.empty(ids.shape, dtype=torch.float32, device=x.device)
-        d_up, d_down = torch.empty_like(wu), torch.empty_like(wd)
-        ds_up, ds_down = torch.empty_like(su), torch.empty_like(sd)
-        se = _abi.shared_expert(sd.shape[0], _ptr(su), _ptr(sd), _ptr(ds_up), _ptr(ds_down))
-        ws = ctx.ws
-        _abi.check(_abi.mm_backward_se(ws.dims, se, _ptr(dy), _ptr(x), _ptr(ids), _ptr(w), _ptr(wu),
-                                       _ptr(wd), ws.ptr, ws.nbytes, _ptr(dx), _ptr(d_topk),
-                                       _ptr(d_up), _ptr(d_down), _stream(x.device), 0),
-                   "mm_backward_se")
+        x, ids, w, wu, wd, *shared = ctx.saved_tensors
+        out = backward(ctx.ws, dy.contiguous().to(torch.bfloat16), x, ids, w, wu, wd,
+                       shared=tuple(shared) if ctx.has_shared else None)
         ctx.ws = None
-        return dx, None, d_topk.to(ctx.wdtype), d_up, d_down, ds_up, ds_down
-
-
-class HyperMegaMoEFunction(torch.autograd.Function):
-    @staticmethod
-    def forward(ctx, x, topk_ids, topk_weights, up_proj_weight, down_proj_weight):
-        T, H, I, E, K = check_inputs(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)
-        x = x.contiguous()
-        ids = topk_ids.to(torch.int32).contiguous()
-        w = topk_weights.to(torch.float32).contiguous()
-        wu, wd = up_proj_weight.contiguous(), down_proj_weight.contiguous()
-        ws = Workspace(T, H, I, E, K, x.device)
-        y = forward(ws, x, ids, w, wu, wd)
-        ctx.ws = ws
-        ctx.wdtype = topk_weights.dtype
-        ctx.save_for_backward(x, ids, w, wu, wd)
-        return y
-
-    @staticmethod
-    def backward(ctx, dy):
-        x, ids, w, wu, wd = ctx.saved_tensors
-        dx, d_topk, d_up, d_down = backward(ctx.ws, dy.contiguous().to(torch.bfloat16), x, ids, w, wu, wd)
-        ctx.ws = None
-        return dx, None, d_topk.to(ctx.wdtype), d_up, d_down
+        dx, d_topk, d_up, d_down = out[:4]
+        ds_up, ds_down = out[4:] if ctx.has_shared else (None, None)
+        return dx, None, d_topk.to(ctx.wdtype), d_up, d_down, ds_up, ds_down, None
 
 
 def hyper_mega_moe(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight, *,
-                   shared_up_proj_weight=None, shared_down_proj_weight=None):
+                   shared_up_proj_weight=None, shared_down_proj_weight=None,
+                   tokens_per_expert=None):
     """y[T,H] = sum_k topk_weights[t,k] * SwiGLU-FFN_{topk_ids[t,k]}(x[t])
-    (+ SwiGLU-FFN_shared(x[t]) when the keyword-only shared-expert weights are given)."""
+    (+ SwiGLU-FFN_shared(x[t]) when the keyword-only shared-expert weights are given).
+
+    tokens_per_expert (optional, [E] on x's device, int32 used as is, int64 or non-contiguous
+    converted) is the caller's histogram of topk_ids; the layer checks it against its own (one
+    host wait) and raises MMError(MM_ERR_TOKENS_PER_EXPERT) if they differ."""
     if (shared_up_proj_weight is None) != (shared_down_proj_weight is None):
         raise ValueError("give both shared-expert weights or neither")
-    if shared_up_proj_weight is not None:
-        return HyperMegaMoESharedFunction.apply(x, topk_ids, topk_weights, up_proj_weight,
-                                                down_proj_weight, shared_up_proj_weight,
-                                                shared_down_proj_weight)
-    return HyperMegaMoEFunction.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight)
+    return HyperMegaMoEFunction.apply(x, topk_ids, topk_weights, up_proj_weight, down_proj_weight,
+                                      shared_up_proj_weight, shared_down_proj_weight,
+                                      tokens_per_expert)

@@ -28,71 +28,58 @@ def make_inputs(w: synth.Workload, device="cuda", ids=None):
 
 
 def run_layer(inp, flags=0, ws=None, stream=None, backward=True, bwd_flags=0, d_up=None,
-              d_down=None):
+              d_down=None, shared=None, tokens_per_expert=None, ds_up=None, ds_down=None):
     """Forward (+ backward) through the C ABI; returns device tensors and the workspace.
-    d_up/d_down, when given, are the weight-gradient output buffers (their contents matter with
-    MM_FLAG_ACCUMULATE_WEIGHT_GRADS in bwd_flags)."""
+
+    d_up/d_down (and ds_up/ds_down for a shared expert), when given, are the weight-gradient
+    output buffers: their contents matter with MM_FLAG_ACCUMULATE_WEIGHT_GRADS, and they must be
+    fp32 with MM_FLAG_FP32_WEIGHT_GRADS. `shared` = (shared_up [H, 2I_s], shared_down [I_s, H])
+    and `tokens_per_expert` (device int32 [E]) go through mm_forward_ex / mm_backward_ex."""
     x, ids, tw = inp["x"], inp["topk_ids"], inp["topk_weights"]
     wu, wd = inp["w_up"], inp["w_down"]
     T, H = x.shape
     E, _, I2 = wu.shape
     K = ids.shape[1]
     d = _abi.dims(T, H, I2 // 2, E, K)
-    nbytes = _abi.mm_workspace_size(d)
+    gdt = torch.float32 if bwd_flags & _abi.MM_FLAG_FP32_WEIGHT_GRADS else torch.bfloat16
+    ex = shared is not None or tokens_per_expert is not None
+    se = opt = None
+    if shared is not None:
+        su, sd = shared
+        ds_up = torch.empty(su.shape, dtype=gdt, device=x.device) if ds_up is None else ds_up
+        ds_down = torch.empty(sd.shape, dtype=gdt, device=x.device) if ds_down is None else ds_down
+        se = _abi.shared_expert(sd.shape[0], su.data_ptr(), sd.data_ptr(), ds_up.data_ptr(),
+                                ds_down.data_ptr())
+    if ex:
+        opt = _abi.options(se, tokens_per_expert.data_ptr() if tokens_per_expert is not None else 0)
+    nbytes = _abi.mm_workspace_size_ex(d, opt) if ex else _abi.mm_workspace_size(d)
     assert nbytes > 0
     if ws is None:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
     st = (stream or torch.cuda.current_stream()).cuda_stream
     y = torch.empty_like(x)
-    _abi.check(_abi.mm_forward(d, x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
-                               wd.data_ptr(), y.data_ptr(), ws.data_ptr(), nbytes, st, flags),
-               "mm_forward")
+    fargs = (x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(), wd.data_ptr(),
+             y.data_ptr(), ws.data_ptr(), nbytes, st, flags)
+    if ex:
+        _abi.check(_abi.mm_forward_ex(d, opt, *fargs), "mm_forward_ex")
+    else:
+        _abi.check(_abi.mm_forward(d, *fargs), "mm_forward")
     out = dict(y=y, ws=ws, dims=d)
     if backward:
         dx = torch.empty_like(x)
         d_topk = torch.empty(T, K, dtype=torch.float32, device=x.device)
-        d_up = torch.empty_like(wu) if d_up is None else d_up
-        d_down = torch.empty_like(wd) if d_down is None else d_down
-        _abi.check(_abi.mm_backward(d, inp["dy"].data_ptr(), x.data_ptr(), ids.data_ptr(),
-                                    tw.data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(),
-                                    nbytes, dx.data_ptr(), d_topk.data_ptr(), d_up.data_ptr(),
-                                    d_down.data_ptr(), st, bwd_flags), "mm_backward")
+        d_up = torch.empty(wu.shape, dtype=gdt, device=x.device) if d_up is None else d_up
+        d_down = torch.empty(wd.shape, dtype=gdt, device=x.device) if d_down is None else d_down
+        bargs = (inp["dy"].data_ptr(), x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
+                 wd.data_ptr(), ws.data_ptr(), nbytes, dx.data_ptr(), d_topk.data_ptr(),
+                 d_up.data_ptr(), d_down.data_ptr(), st, bwd_flags)
+        if ex:
+            _abi.check(_abi.mm_backward_ex(d, opt, *bargs), "mm_backward_ex")
+        else:
+            _abi.check(_abi.mm_backward(d, *bargs), "mm_backward")
         out.update(dx=dx, d_topk_weights=d_topk, dW_up=d_up, dW_down=d_down)
-    out["status"] = _abi.mm_get_status(ws.data_ptr(), st)
-    return out
-
-
-def run_layer_se(inp, su, sd, flags=0, ws=None, backward=True, bwd_flags=0):
-    """Forward (+ backward) with a shared expert (su [H, 2*I_s], sd [I_s, H]) through the C ABI."""
-    x, ids, tw = inp["x"], inp["topk_ids"], inp["topk_weights"]
-    wu, wd = inp["w_up"], inp["w_down"]
-    T, H = x.shape
-    E, _, I2 = wu.shape
-    K = ids.shape[1]
-    I_s = sd.shape[0]
-    d = _abi.dims(T, H, I2 // 2, E, K)
-    nbytes = _abi.mm_workspace_size_se(d, I_s)
-    assert nbytes > 0
-    if ws is None:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
-    st = torch.cuda.current_stream().cuda_stream
-    ds_up, ds_down = torch.empty_like(su), torch.empty_like(sd)
-    se = _abi.shared_expert(I_s, su.data_ptr(), sd.data_ptr(), ds_up.data_ptr(), ds_down.data_ptr())
-    y = torch.empty_like(x)
-    _abi.check(_abi.mm_forward_se(d, se, x.data_ptr(), ids.data_ptr(), tw.data_ptr(), wu.data_ptr(),
-                                  wd.data_ptr(), y.data_ptr(), ws.data_ptr(), nbytes, st, flags),
-               "mm_forward_se")
-    out = dict(y=y, ws=ws, dims=d)
-    if backward:
-        dx = torch.empty_like(x)
-        d_topk = torch.empty(T, K, dtype=torch.float32, device=x.device)
-        d_up, d_down = torch.empty_like(wu), torch.empty_like(wd)
-        _abi.check(_abi.mm_backward_se(d, se, inp["dy"].data_ptr(), x.data_ptr(), ids.data_ptr(),
-                                       tw.data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(),
-                                       nbytes, dx.data_ptr(), d_topk.data_ptr(), d_up.data_ptr(),
-                                       d_down.data_ptr(), st, bwd_flags), "mm_backward_se")
-        out.update(dx=dx, d_topk_weights=d_topk, dW_up=d_up, dW_down=d_down, dS_up=ds_up,
-                   dS_down=ds_down)
+        if shared is not None:
+            out.update(dS_up=ds_up, dS_down=ds_down)
     out["status"] = _abi.mm_get_status(ws.data_ptr(), st)
     return out
 

@@ -51,7 +51,36 @@ def test_host_validation_without_device():
     assert _abi.mm_backward(d, 0, 16, 16, 16, 16, 16, 256, n, 16, 16, 16, 16, 0, 0) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_get_status(0, 0) == _abi.MM_ERR_WORKSPACE
     assert _abi.mm_status_string(_abi.MM_ERR_BAD_EXPERT_ID) == "expert id out of range"
-    assert _abi.mm_abi_version() == 1
+    assert _abi.mm_abi_version() == 2
+    assert _abi.mm_status_string(_abi.MM_ERR_TOKENS_PER_EXPERT) == \
+        "tokens_per_expert does not match topk_ids"
+
+
+def test_extended_entry_points_host_checks():
+    d = _abi.dims(16, 64, 32, 4, 2)
+    n = _abi.mm_workspace_size(d)
+    # no options, or empty options: the plain layout
+    assert _abi.mm_workspace_size_ex(d, None) == n
+    assert _abi.mm_workspace_size_ex(d, _abi.options()) == n
+    # a shared expert adds its own region; its size follows the same rules as I
+    ns = _abi.mm_workspace_size_ex(d, _abi.options(_abi.shared_expert(48, 0, 0)))
+    assert ns > n
+    assert _abi.mm_workspace_size_ex(d, _abi.options(_abi.shared_expert(96, 0, 0))) > ns
+    assert _abi.mm_workspace_size_ex(d, _abi.options(_abi.shared_expert(0, 0, 0))) == 0
+    assert _abi.mm_workspace_size_ex(d, _abi.options(_abi.shared_expert(36, 0, 0))) == 0
+    # shared-expert weights missing or misaligned; misaligned tokens_per_expert
+    se_null = _abi.options(_abi.shared_expert(48, 0, 0))
+    assert _abi.mm_forward_ex(d, se_null, 16, 16, 16, 16, 16, 16, 256, ns, 0, 0) == _abi.MM_ERR_INVALID_ARG
+    se_odd = _abi.options(_abi.shared_expert(48, 16, 24))
+    assert _abi.mm_forward_ex(d, se_odd, 16, 16, 16, 16, 16, 16, 256, ns, 0, 0) == _abi.MM_ERR_INVALID_ARG
+    se_nograd = _abi.options(_abi.shared_expert(48, 16, 16))
+    assert _abi.mm_backward_ex(d, se_nograd, 16, 16, 16, 16, 16, 16, 256, ns, 16, 16, 16, 16, 0,
+                               0) == _abi.MM_ERR_INVALID_ARG
+    # a shared expert needs the larger workspace
+    assert _abi.mm_forward_ex(d, _abi.options(_abi.shared_expert(48, 16, 16)), 16, 16, 16, 16, 16,
+                              16, 256, n, 0, 0) == _abi.MM_ERR_WORKSPACE
+    assert _abi.mm_forward_ex(d, _abi.options(None, 18), 16, 16, 16, 16, 16, 16, 256, n, 0,
+                              0) == _abi.MM_ERR_INVALID_ARG
 
 
 def test_stage_table():

@@ -1,0 +1,110 @@
+"""The boundary's optional behaviour: fp32 weight-gradient outputs (alone and accumulated) and a
+caller-supplied tokens_per_expert histogram (multicore usage guide, torch managed API: an exact
+per-expert histogram the caller may pass; the layer checks it and never addresses with it)."""
+import pytest
+import torch
+
+import oracle
+from layer_harness import assert_close, make_inputs, run_layer
+from moe_ffn_expert_gb300 import _abi
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+F32 = _abi.MM_FLAG_FP32_WEIGHT_GRADS
+ACC = _abi.MM_FLAG_ACCUMULATE_WEIGHT_GRADS
+
+
+def _inputs(T=300, H=256, I=128, E=8, K=2, seed=17, empty_last=True):
+    w = synth.small("opt", T, H, I, E, K, seed=seed)
+    ids = None
+    if empty_last:  # expert E-1 gets no slot
+        ids = torch.stack([(torch.arange(T) + k * 3) % (E - 1) for k in range(K)], 1).int()
+    return w, make_inputs(w, ids=ids)
+
+
+def test_fp32_weight_grads_are_the_unrounded_accumulators():
+    """bf16(fp32 output) equals the bf16 output bit for bit (same accumulators, one rounding);
+    the fp32 output meets the oracle bound; an expert with no slot gets exact zeros."""
+    w, inp = _inputs()
+    ref = run_layer(inp)
+    out = run_layer(inp, bwd_flags=F32)
+    assert out["status"] == _abi.MM_OK
+    for name in ("dW_up", "dW_down"):
+        assert out[name].dtype == torch.float32
+        assert torch.equal(out[name].to(torch.bfloat16), ref[name]), name
+        assert torch.count_nonzero(out[name][-1]) == 0, name
+    h = {k: v.cpu() for k, v in inp.items()}
+    g = oracle.backward(h["x"], h["topk_ids"], h["topk_weights"], h["w_up"], h["w_down"], h["dy"])
+    assert_close("dW_up", out["dW_up"], g["dW_up"])
+    assert_close("dW_down", out["dW_down"], g["dW_down"])
+    assert torch.equal(out["dx"], ref["dx"]) and torch.equal(out["d_topk_weights"], ref["d_topk_weights"])
+
+
+def test_fp32_accumulate_is_one_fp32_add_per_element():
+    """With both flags the stores add in fp32: exactly base + the fp32 gradient (one rounding),
+    and the slice of an expert with no slot keeps its contents."""
+    w, inp = _inputs(seed=23)
+    ref = run_layer(inp, bwd_flags=F32)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    base_up = torch.randn(inp["w_up"].shape, generator=g, device="cuda")
+    base_down = torch.randn(inp["w_down"].shape, generator=g, device="cuda")
+    out = run_layer(inp, bwd_flags=F32 | ACC, d_up=base_up.clone(), d_down=base_down.clone())
+    assert out["status"] == _abi.MM_OK
+    for name, base in (("dW_up", base_up), ("dW_down", base_down)):
+        assert torch.equal(out[name], base + ref[name]), name
+        assert torch.equal(out[name][-1], base[-1]), name
+
+
+def test_fp32_weight_grads_with_a_shared_expert():
+    w, inp = _inputs(T=200, E=5, seed=29, empty_last=False)
+    su, sd = synth.shared_up(w, 136, device="cuda"), synth.shared_down(w, 136, device="cuda")
+    ref = run_layer(inp, shared=(su, sd))
+    out = run_layer(inp, shared=(su, sd), bwd_flags=F32)
+    for name in ("dW_up", "dW_down", "dS_up", "dS_down"):
+        assert out[name].dtype == torch.float32
+        assert torch.equal(out[name].to(torch.bfloat16), ref[name]), name
+
+
+def test_tokens_per_expert_matching_changes_nothing():
+    w, inp = _inputs(seed=31)
+    tpe = torch.bincount(inp["topk_ids"].long().flatten(), minlength=8).int()
+    a = run_layer(inp)
+    b = run_layer(inp, tokens_per_expert=tpe, flags=_abi.MM_FLAG_VALIDATE_IDS)
+    assert b["status"] == _abi.MM_OK
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_tokens_per_expert_mismatch_is_reported_and_recovers():
+    w, inp = _inputs(seed=37)
+    good = torch.bincount(inp["topk_ids"].long().flatten(), minlength=8).int()
+    bad = good.clone()
+    bad[0] += 1
+    bad[1] -= 1  # same total: only the per-expert check can see it
+    # without the validate flag: recorded in the status word, the rest of the call does nothing
+    out = run_layer(inp, tokens_per_expert=bad, backward=False)
+    assert out["status"] == _abi.MM_ERR_TOKENS_PER_EXPERT
+    # with it: returned by the forward itself
+    with pytest.raises(_abi.MMError) as e:
+        run_layer(inp, tokens_per_expert=bad, ws=out["ws"], flags=_abi.MM_FLAG_VALIDATE_IDS,
+                  backward=False)
+    assert e.value.status == _abi.MM_ERR_TOKENS_PER_EXPERT
+    # the same workspace then runs a clean call
+    ok = run_layer(inp, tokens_per_expert=good, ws=out["ws"])
+    ref = run_layer(inp)
+    assert ok["status"] == _abi.MM_OK and torch.equal(ok["y"], ref["y"])
+
+
+def test_torch_entry_point_tokens_per_expert():
+    from moe_ffn_expert_gb300.torch_api import hyper_mega_moe
+    w, inp = _inputs(seed=41)
+    tpe64 = torch.bincount(inp["topk_ids"].long().flatten(), minlength=8)  # int64: converted
+    y = hyper_mega_moe(inp["x"], inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"],
+                       tokens_per_expert=tpe64)
+    assert torch.equal(y, run_layer(inp, backward=False)["y"])
+    bad = tpe64.clone()
+    bad[2] += 5
+    with pytest.raises(_abi.MMError):
+        hyper_mega_moe(inp["x"], inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"],
+                       tokens_per_expert=bad)

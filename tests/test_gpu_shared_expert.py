@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from layer_harness import assert_close, assert_dtopk, make_inputs, run_layer, run_layer_se
+from layer_harness import assert_close, assert_dtopk, make_inputs, run_layer
 from moe_ffn_expert_gb300 import _abi
 from workloads import synth
 
@@ -23,7 +23,7 @@ def _case(T, H, I, E, K, I_s, seed):
                                            (96, 136, 72, 5, 2, 72)])      # H, I, I_s not /64
 def test_shared_expert_parity(T, H, I, E, K, I_s):
     w, inp, su, sd = _case(T, H, I, E, K, I_s, seed=21)
-    out = run_layer_se(inp, su, sd)
+    out = run_layer(inp, shared=(su, sd))
     assert out["status"] == _abi.MM_OK
     h = {k: v.cpu() for k, v in inp.items()}
     sh = (su.cpu(), sd.cpu())
@@ -43,7 +43,7 @@ def test_shared_expert_leaves_the_routed_gradients_unchanged():
     """The routed experts' weight gradients and d_topk do not depend on the shared expert."""
     w, inp, su, sd = _case(300, 256, 128, 6, 2, 256, seed=5)
     a = run_layer(inp)
-    b = run_layer_se(inp, su, sd)
+    b = run_layer(inp, shared=(su, sd))
     for k in ("dW_up", "dW_down", "d_topk_weights"):
         assert torch.equal(a[k], b[k]), k
 
@@ -51,7 +51,7 @@ def test_shared_expert_leaves_the_routed_gradients_unchanged():
 def test_shared_expert_torch_autograd():
     from moe_ffn_expert_gb300.torch_api import hyper_mega_moe
     w, inp, su, sd = _case(200, 256, 128, 5, 2, 192, seed=8)
-    ref = run_layer_se(inp, su, sd)
+    ref = run_layer(inp, shared=(su, sd))
     x = inp["x"].clone().requires_grad_(True)
     su_t, sd_t = su.clone().requires_grad_(True), sd.clone().requires_grad_(True)
     y = hyper_mega_moe(x, inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"],
