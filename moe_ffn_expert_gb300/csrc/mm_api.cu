@@ -101,6 +101,36 @@ mm_status cuda_fail(cudaError_t e, const char* what) {
     if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
   } while (0)
 
+// A second stream per device, for work that may overlap the caller's stream inside one call,
+// with the two events that fork it from and join it back to the caller's stream. Created once per
+// device (non-blocking, highest priority, so its small grids are scheduled ahead of a persistent
+// GEMM's CTAs as soon as an SM has room).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t side_stream(SideStream** out) {
+  static std::mutex mu;
+  static SideStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = per_dev[dev];
+  if (ss.s == nullptr) {
+    int lo = 0, hi = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, hi)) != cudaSuccess)
+      return e;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 // Makes the current device's primary context current on this thread. Tensor-map encoding is a
 // driver call that needs one, and a thread that has not launched anything yet (an autograd
 // worker thread, say) may not have it bound.
@@ -353,13 +383,23 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
     extra = wss + p.ws_s.off_o;
     extra_lo = wss + p.ws_s.off_o_lo;
   }
-  MM_TRY(timed(ST_COMBINE_DX, st, [&] {
-    return launch_combine(w, ws, ws + w.off_o, nullptr, dx, st, extra, extra_lo);
-  }));
+  // Combine(dX) is HBM-bound and independent of W1Grad (tensor-bound): it runs on the side
+  // stream, forked after input_grad and joined back after W1Grad has been enqueued.
+  SideStream* side = nullptr;
+  MM_TRY(side_stream(&side));
+  MM_TRY(cudaEventRecord(side->fork, st));
+  MM_TRY(cudaStreamWaitEvent(side->s, side->fork, 0));
+  const cudaError_t e_comb = timed(ST_COMBINE_DX, side->s, [&] {
+    return launch_combine(w, ws, ws + w.off_o, nullptr, dx, side->s, extra, extra_lo);
+  });
   c.kind = GK_W1_GRAD;
   c.d_w = d_up_proj_weight;
   c.accumulate = accumulate;
-  MM_TRY(timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  const cudaError_t e_w1 = timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); });
+  MM_TRY(cudaEventRecord(side->join, side->s));  // the join is enqueued whatever happened above
+  MM_TRY(cudaStreamWaitEvent(st, side->join, 0));
+  MM_TRY(e_comb);
+  MM_TRY(e_w1);
   if (p.shared) {  // shared expert W1Grad (rows = x)
     cs.kind = GK_W1_GRAD;
     cs.d_w = se->d_up_proj_weight;

@@ -129,8 +129,11 @@ struct Traits {
   // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
   // buffers) and store it with TMA
   static constexpr bool OUT_STAGING = (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD);
+  // GEMM1 copies its outputs out through a 4 KB per-warp buffer with coalesced stores
+  static constexpr bool ROW_STAGING = (KIND == GK_GEMM1_SWIGLU);
   static constexpr int EPI_BYTES = GU_STAGING    ? NUM_EPI_WARPS * (GU_CHUNK_BYTES + OUT_CHUNK_BYTES)
                                    : OUT_STAGING ? NUM_EPI_WARPS * 2 * OUT_TILE_BYTES
+                                   : ROW_STAGING ? NUM_EPI_WARPS * 4096
                                                  : 0;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -212,6 +215,95 @@ __device__ __forceinline__ void split8_bf16(const float* v, uint4& hi, uint4& lo
   }
   hi = pack8_bf16(h);
   lo = pack8_bf16(l);
+}
+
+// Coalesced copy-out through a per-warp 4 KB staging buffer. A lane first writes its own row
+// (32 values) into the buffer; after __syncwarp the warp reads it back row-major so that each
+// store instruction covers whole 128-byte lines of consecutive rows, instead of 32 rows at
+// 16 bytes each. 16-byte unit u of row r sits at unit u ^ (r & 7) (fp32, 128-byte rows) or
+// u ^ ((r >> 1) & 3) (bf16, 64-byte rows), so both the row writes and the line reads are free of
+// bank conflicts.
+__device__ __forceinline__ void stage_row_f32(uint8_t* stage, int lane, const float* v) {
+  uint8_t* rowp = stage + lane * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4*>(rowp + ((u ^ (lane & 7)) << 4)) =
+        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+}
+
+// Rows row0..row0+31 of an fp32 matrix (leading dimension ld), columns n..n+31 masked at N.
+__device__ __forceinline__ void copy_out_f32(const uint8_t* stage, int lane, float* base,
+                                             int64_t row0, int64_t ld, int n, int N) {
+  const int u = lane & 7;
+  if (n + 4 * u >= N) return;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const float4 v = *reinterpret_cast<const float4*>(stage + r * 128 + ((u ^ (r & 7)) << 4));
+    *reinterpret_cast<float4*>(base + (row0 + r) * ld + n + 4 * u) = v;
+  }
+}
+
+__device__ __forceinline__ void stage_row_bf16(uint8_t* stage, int lane, const float* v) {
+  uint8_t* rowp = stage + lane * 64;
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<uint4*>(rowp + ((u ^ ((lane >> 1) & 3)) << 4)) = pack8_bf16(v + 8 * u);
+}
+
+__device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __nv_bfloat16* base,
+                                              int64_t row0, int64_t ld, int n, int N) {
+  const int u = lane & 3;
+  if (n + 8 * u >= N) return;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+    *reinterpret_cast<uint4*>(base + (row0 + r) * ld + n + 8 * u) = v;
+  }
+}
+
+// GEMM1 + SwiGLU epilogue of one warp: 32 tile rows (quarter q) x one column half. Accumulator
+// columns [0,128) are gate columns n0.., [128,256) up columns n0..; each 32-column chunk writes
+// the fp32 gate, the fp32 up and h = silu(gate) * up (bf16) through the staging buffer. The
+// accumulator is released (`acce`) right after the last TMEM read, before the last stores.
+__device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile& t, uint32_t tacc,
+                                                      int q, int hf, int lane, uint8_t* stage,
+                                                      uint32_t acce) {
+  const int64_t row0 = (int64_t)t.m0 + q * 32;
+  float* gu = reinterpret_cast<float*>(a.out0);
+#pragma unroll 1
+  for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+    uint32_t ga[32], ub[32];
+    tmem_ld_32x32(tacc + c * 32, ga);
+    tmem_ld_32x32(tacc + 128 + c * 32, ub);
+    tmem_ld_wait();
+    if (c == 2 * hf + 1) {  // last TMEM read of this warp for the tile
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+    }
+    const int n = t.n0 + c * 32;
+    float g[32], u[32], h[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      g[j] = __uint_as_float(ga[j]);
+      u[j] = __uint_as_float(ub[j]);
+      h[j] = g[j] * sigmoidf_(g[j]) * u[j];
+    }
+    stage_row_f32(stage, lane, g);
+    __syncwarp();
+    copy_out_f32(stage, lane, gu, row0, a.ld0, n, a.I);
+    __syncwarp();
+    stage_row_f32(stage, lane, u);
+    __syncwarp();
+    copy_out_f32(stage, lane, gu + a.I, row0, a.ld0, n, a.I);
+    __syncwarp();
+    stage_row_bf16(stage, lane, h);
+    __syncwarp();
+    copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I);
+    __syncwarp();
+  }
 }
 
 // One epilogue warp drains 32 TMEM lanes (tile rows r = 32*q + lane) over half `hf` of the
@@ -754,6 +846,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
+      if constexpr (TR::ROW_STAGING) {  // releases the accumulator itself
+        gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw), acce_bar(buf));
+        ++acc_it;
+        continue;
+      }
       if constexpr (TR::OUT_STAGING)
         staged_store_tile<KIND>(a, t, tacc, q, hf, lane, &em.out, sbuf, smem_raw + (sbuf - raw),
                                 chunk_no);
