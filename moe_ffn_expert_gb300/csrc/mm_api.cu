@@ -88,10 +88,12 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 thread_local char g_err[256] = "";
 
 mm_status cuda_fail(cudaError_t e, const char* what) {
+  // the previous detail (a note from a lower layer) is kept after this one, shortened to fit
   char inner[160];
-  snprintf(inner, sizeof(inner), "%s", g_err);
-  snprintf(g_err, sizeof(g_err), "%s: %s (%s)%s%s", what, cudaGetErrorString(e), cudaGetErrorName(e),
-           inner[0] ? "; " : "", inner);
+  memcpy(inner, g_err, sizeof(inner) - 1);
+  inner[sizeof(inner) - 1] = 0;
+  snprintf(g_err, sizeof(g_err), "%.80s: %.60s (%.40s)%s%.60s", what, cudaGetErrorString(e),
+           cudaGetErrorName(e), inner[0] ? "; " : "", inner);
   return MM_ERR_CUDA;
 }
 

@@ -109,23 +109,26 @@ struct Traits {
   static constexpr bool A_MN = WGRAD;
   static constexpr bool B_MN =
       (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
-  static constexpr bool A_SPLIT = (KIND == GK_W2_GRAD);  // hw_hi + hw_lo
-  static constexpr bool B_SPLIT = (KIND == GK_W1_GRAD);  // dgu_hi + dgu_lo
-  static constexpr int TN = WGRAD ? 128 : BN;            // accumulator columns per tile
+  // The weight gradients' split operand (bf16 hi + lo, two MMAs per k-step into one fp32
+  // accumulator) is always A: W2Grad computes (w h)^T dy_rows with A = w h; W1Grad computes the
+  // transpose dW_up^T = [d_gate|d_up]^T x_rows with A = [d_gate|d_up] and its epilogue stores the
+  // transpose. Both then run 128 x 256 tiles like the row-grouped kinds.
+  static constexpr bool A_SPLIT = WGRAD;
+  static constexpr bool TRANSPOSED_OUT = (KIND == GK_W1_GRAD);
+  static_assert(!TRANSPOSED_OUT || WGRAD, "only a weight gradient is stored transposed");
+  static constexpr int TN = BN;  // accumulator columns per tile
   static constexpr int B_BYTES = TN * BK * 2;
   static constexpr int A_LO_OFF = A_BYTES;                                   // if A_SPLIT
   static constexpr int B_OFF = A_BYTES * (A_SPLIT ? 2 : 1);
-  static constexpr int B_LO_OFF = B_OFF + B_BYTES;                           // if B_SPLIT
-  static constexpr int USED = B_OFF + B_BYTES * (B_SPLIT ? 2 : 1);
+  static constexpr int STAGE_BYTES = B_OFF + B_BYTES;  // 48 KB, 64 KB with the A lo plane
   static constexpr uint32_t TMEM_COLS = 2 * TN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN, A_MN ? 1 : 0, B_MN ? 1 : 0);
-  static_assert(USED == STAGE_BYTES, "stage layout");
+  static_assert(A_SPLIT || STAGE_BYTES == ::mm::STAGE_BYTES, "stage layout");
   static_assert(!A_SPLIT || A_LO_OFF + A_BYTES == B_OFF, "A lo plane layout");
-  static_assert(!B_SPLIT || B_LO_OFF + B_BYTES == USED, "B lo plane layout");
   // act_grad trades one mainloop stage for per-warp staging of its gate|up input and of its
-  // six output planes (TMA in, TMA out)
+  // six output planes (TMA in, TMA out); the weight gradients' 64 KB stages fit three times
   static constexpr bool GU_STAGING = (KIND == GK_ACT_GRAD);
-  static constexpr int STAGES = GU_STAGING ? 3 : 4;
+  static constexpr int STAGES = (GU_STAGING || WGRAD) ? 3 : 4;
   // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
   // buffers) and store it with TMA
   static constexpr bool OUT_STAGING = (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD);
@@ -166,34 +169,6 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
     t.kiters = a.k_iters;
   }
   return t;
-}
-
-__device__ __forceinline__ void store_row_f32(float* dst, const float* v, int n, int N) {
-  // 32 consecutive fp32 columns starting at n, masked in groups of 8
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (n + 8 * g < N) {
-      *reinterpret_cast<float4*>(dst + n + 8 * g) =
-          make_float4(v[8 * g + 0], v[8 * g + 1], v[8 * g + 2], v[8 * g + 3]);
-      *reinterpret_cast<float4*>(dst + n + 8 * g + 4) =
-          make_float4(v[8 * g + 4], v[8 * g + 5], v[8 * g + 6], v[8 * g + 7]);
-    }
-  }
-}
-
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v, int n, int N) {
-  // 32 consecutive columns starting at n, masked in groups of 8 (N is a multiple of 8)
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (n + 8 * g < N) {
-      uint4 q;
-      q.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
-      q.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
-      q.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
-      q.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
-      *reinterpret_cast<uint4*>(dst + n + 8 * g) = q;
-    }
-  }
 }
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
@@ -304,87 +279,6 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
     copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I);
     __syncwarp();
   }
-}
-
-// One epilogue warp drains 32 TMEM lanes (tile rows r = 32*q + lane) over half `hf` of the
-// tile's columns.
-template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const Args& a, const Tile& t, uint32_t tacc, int r,
-                                              int hf) {
-  if constexpr (KIND == GK_GEMM1_SWIGLU) {
-    // accumulator columns [0,128) = gate columns n0.., [128,256) = up columns n0..
-    const int64_t row = (int64_t)t.m0 + r;
-    float* gu = reinterpret_cast<float*>(a.out0) + row * a.ld0;
-    __nv_bfloat16* hh = a.out1 + row * a.ld1;
-#pragma unroll 1
-    for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
-      uint32_t ga[32], ub[32];
-      tmem_ld_32x32(tacc + c * 32, ga);
-      tmem_ld_32x32(tacc + 128 + c * 32, ub);
-      tmem_ld_wait();
-      const int n = t.n0 + c * 32;
-      float g[32], u[32], h[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        g[j] = __uint_as_float(ga[j]);
-        u[j] = __uint_as_float(ub[j]);
-        h[j] = g[j] * sigmoidf_(g[j]) * u[j];
-      }
-      store_row_f32(gu, g, n, a.I);
-      store_row_f32(gu + a.I, u, n, a.I);
-      store_row_bf16(hh, h, n, a.I);
-    }
-  } else if constexpr (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD) {
-    const int64_t row = (int64_t)t.m0 + r;
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) + row * a.ld0;
-    constexpr int NC = BN / 64;  // 32-column chunks per half
-#pragma unroll 1
-    for (int c = hf * NC; c < hf * NC + NC; ++c) {
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + c * 32, v);
-      tmem_ld_wait();
-      float f[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-      store_row_bf16(o, f, t.n0 + c * 32, a.N);
-    }
-  } else if constexpr (Traits<KIND>::WGRAD) {
-    // every lane runs the TMEM loads; rows past M store nothing
-    const int m = t.m0 + r;
-    const bool row_ok = m < a.M;
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) +
-                       (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
-    constexpr int NC = Traits<KIND>::TN / 64;
-#pragma unroll 1
-    for (int c = hf * NC; c < hf * NC + NC; ++c) {
-      uint32_t v[32];
-      tmem_ld_32x32(tacc + c * 32, v);
-      tmem_ld_wait();
-      float f[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
-      if (row_ok) store_row_bf16(o, f, t.n0 + c * 32, a.N);
-    }
-  }
-}
-
-template <int KIND>
-__device__ __forceinline__ void zero_wgrad_tile(const Args& a, const Tile& t, int r, int hf) {
-  const int m = t.m0 + r;
-  if (m >= a.M) return;
-  constexpr int NC = Traits<KIND>::TN / 64;
-  const int64_t row = (int64_t)t.e * a.out_expert_stride + (int64_t)m * a.ld0;
-  if (a.wgrad_f32) {  // fp32 rows: 4 columns per 16-byte store (N is a multiple of 8)
-    float* o = reinterpret_cast<float*>(a.out0) + row;
-    for (int n = t.n0 + hf * NC * 32; n < t.n0 + (hf + 1) * NC * 32 && n < a.N; n += 4)
-      *reinterpret_cast<float4*>(o + n) = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
-  }
-  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out0) + row;
-  float z[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) z[j] = 0.f;
-  for (int c = hf * NC; c < hf * NC + NC; ++c) store_row_bf16(o, z, t.n0 + c * 32, a.N);
 }
 
 // SwiGLU backward of one 16-column chunk of one row: g from TMEM, gate (cur[0..3]) and up
@@ -546,109 +440,104 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   __syncwarp();
 }
 
-// Output epilogue of one warp for the bf16-output kinds: 32 tile rows (quarter q) x one column
-// half. Each 32-column chunk is converted to bf16, written to one of the warp's two staging
-// buffers (64-byte swizzle: 16-byte unit u of row r at unit u ^ ((r >> 1) & 3)) and stored with
-// TMA by lane 0; the tensor map clips rows and columns outside the output. `chunk_no` counts the
-// warp's chunks to alternate the buffers; before a buffer is rewritten, the store that used it
-// two chunks earlier must have finished reading it. With a.split_out (row-grouped kinds) the
-// chunk goes out as a bf16 hi tile through map[0] and its residual lo tile through map[1].
+// Output epilogue of one warp for the kinds with a TMA-stored output (GEMM2, INPUT_GRAD, the
+// weight gradients): 32 tile rows (quarter q) x one column half, in 32-column chunks. Each chunk
+// is converted, written to the warp's staging buffers and stored (or, for accumulated weight
+// gradients, reduce-added) with TMA by lane 0; the tensor map clips rows and columns outside the
+// output.
+//  * bf16 (default): 32 x 32 bf16 (64-byte rows, 64-byte swizzle: 16-byte unit u of row r at
+//    u ^ ((r >> 1) & 3)), alternating between the warp's two 2 KB buffers; before a buffer is
+//    rewritten, the store that used it two chunks earlier must have finished reading it
+//    (`chunk_no` counts the warp's chunks).
+//  * a.split_out (GEMM2 / INPUT_GRAD): bf16 hi in buffer 0 and the residual lo in buffer 1, stored
+//    through map[0] and map[1].
+//  * a.wgrad_f32 (weight gradients): 32 x 32 fp32 (128-byte rows, 128-byte swizzle: unit u of
+//    row r at u ^ (r & 7)) across both buffers.
+// W1Grad's accumulator holds dW_up^T (rows = columns of dW_up): its chunks are written to the
+// staging buffer transposed (lane = output column, value j = output row) and stored at the
+// swapped coordinates. `zero` stores zeros without reading TMEM (an expert with no rows).
 template <int KIND>
 __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, uint32_t tacc,
                                                   int q, int hf, int lane, const CUtensorMap* map,
                                                   uint32_t sbuf, uint8_t* sbuf_ptr,
-                                                  uint32_t& chunk_no) {
-  constexpr int NC = Traits<KIND>::TN / 64;  // 32-column chunks per half
+                                                  uint32_t& chunk_no, bool zero = false) {
+  using TR = Traits<KIND>;
+  constexpr int NC = TR::TN / 64;  // 32-column chunks per half
   const int row0 = t.m0 + q * 32;
-  if constexpr (!Traits<KIND>::WGRAD) {
-    if (a.split_out) {  // hi in buffer 0, lo in buffer 1: both free before each chunk
-#pragma unroll 1
-      for (int c = hf * NC; c < hf * NC + NC; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32(tacc + c * 32, v);
-        tmem_ld_wait();
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        uint8_t* rowp = sbuf_ptr + lane * 64;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float f[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[8 * u + j]);
-          uint4 hi, lo;
-          split8_bf16(f, hi, lo);
-          const int off = (u ^ ((lane >> 1) & 3)) << 4;
-          *reinterpret_cast<uint4*>(rowp + off) = hi;
-          *reinterpret_cast<uint4*>(rowp + OUT_TILE_BYTES + off) = lo;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int n = t.n0 + c * 32;
-          tma_store_2d(map, sbuf, n, row0);
-          tma_store_2d(map + 1, sbuf + OUT_TILE_BYTES, n, row0);
-          bulk_commit();
-        }
-      }
-      return;
-    }
-  } else {
-    if (a.wgrad_f32) {  // 32 rows x 32 fp32 (128-byte rows, 128-byte swizzle) in both buffers
-#pragma unroll 1
-      for (int c = hf * NC; c < hf * NC + NC; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32(tacc + c * 32, v);
-        tmem_ld_wait();
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        uint8_t* rowp = sbuf_ptr + lane * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(rowp + ((u ^ (lane & 7)) << 4)) =
-              make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          const int n = t.n0 + c * 32;
-          if (a.accumulate)
-            tma_reduce_add_3d(map, sbuf, n, row0, t.e);
-          else
-            tma_store_3d(map, sbuf, n, row0, t.e);
-          bulk_commit();
-        }
-      }
-      return;
-    }
-  }
+  const bool f32 = TR::WGRAD && a.wgrad_f32;
+  const bool split = !TR::WGRAD && a.split_out;
 #pragma unroll 1
   for (int c = hf * NC; c < hf * NC + NC; ++c) {
     uint32_t v[32];
-    tmem_ld_32x32(tacc + c * 32, v);
-    tmem_ld_wait();
-    const uint32_t b = chunk_no & 1u;
-    if (lane == 0) bulk_wait_read_le1();
-    __syncwarp();
-    uint8_t* rowp = sbuf_ptr + b * OUT_TILE_BYTES + lane * 64;
+    if (zero) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float f[8] = {__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]),
-                          __uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]),
-                          __uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]),
-                          __uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])};
-      *reinterpret_cast<uint4*>(rowp + ((u ^ ((lane >> 1) & 3)) << 4)) = pack8_bf16(f);
+      for (int j = 0; j < 32; ++j) v[j] = 0u;
+    } else {
+      tmem_ld_32x32(tacc + c * 32, v);
+      tmem_ld_wait();
+    }
+    // both buffers for the fp32 and split forms, else the one used two chunks ago
+    const uint32_t b = (f32 || split) ? 0u : (chunk_no & 1u);
+    if (lane == 0) {
+      if (f32 || split)
+        bulk_wait_read_all();
+      else
+        bulk_wait_read_le1();
+    }
+    __syncwarp();
+    uint8_t* buf = sbuf_ptr + b * OUT_TILE_BYTES;
+    if constexpr (TR::TRANSPOSED_OUT) {
+      if (f32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<uint32_t*>(buf + j * 128 + (((lane >> 2) ^ (j & 7)) << 4) +
+                                       (lane & 3) * 4) = v[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<__nv_bfloat16*>(buf + j * 64 + (((lane >> 3) ^ ((j >> 1) & 3)) << 4) +
+                                            (lane & 7) * 2) =
+              __float2bfloat16_rn(__uint_as_float(v[j]));
+      }
+    } else if (f32) {
+      uint8_t* rowp = buf + lane * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(rowp + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    } else {
+      uint8_t* rowp = buf + lane * 64;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[8 * u + j]);
+        const int off = (u ^ ((lane >> 1) & 3)) << 4;
+        if (split) {
+          uint4 hi, lo;
+          split8_bf16(f, hi, lo);
+          *reinterpret_cast<uint4*>(rowp + off) = hi;
+          *reinterpret_cast<uint4*>(rowp + OUT_TILE_BYTES + off) = lo;
+        } else {
+          *reinterpret_cast<uint4*>(rowp + off) = pack8_bf16(f);
+        }
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       const int n = t.n0 + c * 32;
-      if constexpr (Traits<KIND>::WGRAD) {
+      const uint32_t src = sbuf + b * OUT_TILE_BYTES;
+      if constexpr (TR::WGRAD) {
+        const int x = TR::TRANSPOSED_OUT ? row0 : n, y = TR::TRANSPOSED_OUT ? n : row0;
         if (a.accumulate)
-          tma_reduce_add_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+          tma_reduce_add_3d(map, src, x, y, t.e);
         else
-          tma_store_3d(map, sbuf + b * OUT_TILE_BYTES, n, row0, t.e);
+          tma_store_3d(map, src, x, y, t.e);
+      } else {
+        tma_store_2d(map, src, n, row0);
+        if (split) tma_store_2d(map + 1, src + OUT_TILE_BYTES, n, row0);
       }
-      else
-        tma_store_2d(map, sbuf + b * OUT_TILE_BYTES, n, row0);
       bulk_commit();
     }
     ++chunk_no;
@@ -667,6 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   constexpr int STAGES = TR::STAGES;
+  constexpr uint32_t STAGE_BYTES = TR::STAGE_BYTES;
   const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // act_grad gate|up staging
   const uint32_t bars = epi_base + TR::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -696,7 +586,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if constexpr (TR::A_SPLIT || TR::B_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
+    if constexpr (TR::A_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
     if constexpr (TR::OUT_STAGING) tma_prefetch_desc(&em.out);
     if constexpr (TR::GU_STAGING) {
       tma_prefetch_desc(&em.dgu_hi);
@@ -757,12 +647,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < TR::TN / 64; ++j)
               tma_load_2d(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, t.row0 + k0);
-            if constexpr (TR::B_SPLIT) {
-#pragma unroll
-              for (int j = 0; j < TR::TN / 64; ++j)
-                tma_load_2d(sa + TR::B_LO_OFF + j * MN_BLOCK_BYTES, &tmL, full_bar(s),
-                            t.n0 + 64 * j, t.row0 + k0);
-            }
           }
         }
       }
@@ -802,8 +686,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(d, ad, bd, TR::IDESC, (kb | kk) != 0 ? 1u : 0u);
             if constexpr (TR::A_SPLIT)
               umma_bf16(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, TR::IDESC, 1u);
-            if constexpr (TR::B_SPLIT)
-              umma_bf16(d, ad, sdesc_sw128(sa + TR::B_LO_OFF + kbo, lbo_b, 1024), TR::IDESC, 1u);
           }
           umma_commit(empty_bar(s));
         }
@@ -822,7 +704,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       smem_raw + (obuf - raw), warp, lane);
   } else {
     const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;     // tile row of this thread
     const int hf = (warp - 2) >> 2;  // column half of the tile
     const uint32_t sbuf = epi_base + (warp - 2) * 2 * OUT_TILE_BYTES;  // output staging
     uint32_t chunk_no = 0;
@@ -831,7 +712,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile t = decode_tile<KIND>(a, tile);
       if (t.kiters == 0) {
         if constexpr (TR::WGRAD) {
-          if (!a.accumulate) zero_wgrad_tile<KIND>(a, t, r, hf);  // adding zero changes nothing
+          if (!a.accumulate)  // adding zero changes nothing
+            staged_store_tile<KIND>(a, t, 0u, q, hf, lane, &em.out, sbuf,
+                                    smem_raw + (sbuf - raw), chunk_no, true);
         }
         continue;
       }
@@ -854,8 +737,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if constexpr (TR::OUT_STAGING)
         staged_store_tile<KIND>(a, t, tacc, q, hf, lane, &em.out, sbuf, smem_raw + (sbuf - raw),
                                 chunk_no);
-      else
-        epilogue_tile<KIND>(a, t, tacc, r, hf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
@@ -1086,15 +967,15 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.out_expert_stride = I * H;
       tiles_max = E * a.m_tiles_w * a.n_tiles_n;
       break;
-    case GK_W1_GRAD:
-      ok = map_rows(&ta, xrows, H, nrows, 64, 64) &&
-           map_rows(&tb, ws + w.off_dgu, 2 * I, S_pad, 64, 64) &&
-           map_rows(&tl, ws + w.off_dgu_lo, 2 * I, S_pad, 64, 64);
+    case GK_W1_GRAD:  // accumulates dW_up^T: rows = the 2I columns of dW_up, columns = H
+      ok = map_rows(&ta, ws + w.off_dgu, 2 * I, S_pad, 64, 64) &&
+           map_rows(&tl, ws + w.off_dgu_lo, 2 * I, S_pad, 64, 64) &&
+           map_rows(&tb, xrows, H, nrows, 64, 64);
       has_lo = true;
-      a.m_tiles_w = cdiv(H, BM);
-      a.n_tiles_n = cdiv(2 * I, Traits<GK_W1_GRAD>::TN);
-      a.M = (int)H;
-      a.N = (int)(2 * I);
+      a.m_tiles_w = cdiv(2 * I, BM);
+      a.n_tiles_n = cdiv(H, Traits<GK_W1_GRAD>::TN);
+      a.M = (int)(2 * I);
+      a.N = (int)H;
       a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
       a.ld0 = 2 * I;
       a.out_expert_stride = H * 2 * I;
@@ -1108,10 +989,11 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
     // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_64B;
-    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N], bf16 or fp32 (128-byte swizzle)
+    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N] ([E][N][M] transposed), bf16 or fp32
       a.wgrad_f32 = c.wgrad_f32 ? 1 : 0;
       const uint64_t es = a.wgrad_f32 ? 4 : 2;
-      const uint64_t d3[3] = {(uint64_t)a.N, (uint64_t)a.M, (uint64_t)E};
+      const bool tr = Traits<KIND>::TRANSPOSED_OUT;
+      const uint64_t d3[3] = {(uint64_t)(tr ? a.M : a.N), (uint64_t)(tr ? a.N : a.M), (uint64_t)E};
       const uint64_t s3[2] = {(uint64_t)a.ld0 * es, (uint64_t)a.out_expert_stride * es};
       const uint32_t b3[3] = {32, 32, 1};
       if (!make_map(&em.out, a.out0, 3, d3, s3, b3,
