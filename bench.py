@@ -74,6 +74,8 @@ def workload_of(args):
     w = synth.BY_NAME[args.workload]
     if args.tokens:
         w = dataclasses.replace(w, T=int(args.tokens))
+    if args.experts:
+        w = dataclasses.replace(w, E=int(args.experts))
     return w
 
 
@@ -482,6 +484,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (smaller profiling cases)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the workload's expert count (profiling captures: fewer tokens "
+                         "with the same rows per expert)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--shared-intermediate", type=int, default=0,
                     help="add a shared expert of this intermediate size (0: none)")
