@@ -31,8 +31,8 @@ METRIC = "MoE-FFN fwd+bwd tokens/s and TFLOPS (% of GB300 BF16 dense peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # algorithmic FLOPs per slot of each GEMM stage (routed work only, no padding)
-GEMM_FLOPS_PER_SLOT = {"gemm1_swiglu": 4, "gemm2": 2, "act_grad": 2, "w2_grad": 2,
-                       "input_grad": 4, "w1_grad": 4}  # x H*I
+GEMM_FLOPS_PER_SLOT = {"gemm1_swiglu": 4, "gemm2": 2, "gemm1_gemm2": 6, "act_grad": 2,
+                       "w2_grad": 2, "input_grad": 4, "w1_grad": 4}  # x H*I
 
 
 def load_peaks():

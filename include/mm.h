@@ -82,6 +82,13 @@ typedef struct mm_dims {
  * accumulation into fp32 "main grad" buffers with one rounding per addition. */
 #define MM_FLAG_FP32_WEIGHT_GRADS 0x4u
 
+/* mm_forward flag: run GEMM1 + SwiGLU and GEMM2 in one persistent launch in which a row block's
+ * GEMM2 tiles start as soon as all of its GEMM1 tiles have stored their h rows (per-row-block
+ * ready counters in the workspace, bounded waits; the RFC's event-counter release of dependent
+ * tiles, §5.1) instead of two stream-ordered launches. Results are identical bit for bit; on a
+ * GB300 both take the same time, so the default is the two launches. */
+#define MM_FLAG_FUSED_FORWARD_GEMMS 0x8u
+
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
  * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is
@@ -211,7 +218,7 @@ int mm_abi_version(void);
  * CUDA events on its stream. mm_timing_read synchronises those events, writes for each stage
  * (up to max_stages) the summed milliseconds and the number of launches since the last read,
  * clears them, and returns the number of stages (MM_NUM_STAGES). mm_stage_name names a stage. */
-#define MM_NUM_STAGES 15
+#define MM_NUM_STAGES 16
 mm_status mm_timing_enable(int on);
 int mm_timing_read(double* ms, int64_t* launches, int max_stages);
 const char* mm_stage_name(int stage);

@@ -26,7 +26,8 @@ MM_FLAG_VALIDATE_IDS = 0x1
 MM_FLAG_TEST_STALL = 0x80000000
 MM_FLAG_ACCUMULATE_WEIGHT_GRADS = 0x2
 MM_FLAG_FP32_WEIGHT_GRADS = 0x4
-MM_NUM_STAGES = 15
+MM_FLAG_FUSED_FORWARD_GEMMS = 0x8
+MM_NUM_STAGES = 16
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT",

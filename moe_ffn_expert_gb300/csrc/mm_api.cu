@@ -80,7 +80,8 @@ cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
 const char* kStageNames[ST_COUNT] = {
     "route_count", "route_scan",  "route_rank", "gather_x",   "gemm1_swiglu",
     "gemm2",       "combine_y",   "gather_dy",  "act_grad",   "d_topk",
-    "w2_grad",     "input_grad",  "combine_dx", "w1_grad",    "shared_expert"};
+    "w2_grad",     "input_grad",  "combine_dx", "w1_grad",    "shared_expert",
+    "gemm1_gemm2"};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -177,6 +178,7 @@ bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows) {
   p.off_poff = take((d.E + 1) * sizeof(int32_t));
   p.off_chunk = take((size_t)p.n_chunks * d.E * sizeof(int32_t));
   p.off_tile_expert = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
+  p.off_ready = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
   p.off_row_of_slot = take((size_t)p.S * sizeof(int32_t));
   p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
   p.off_w_row = take((size_t)p.S_pad * sizeof(float));
@@ -296,10 +298,18 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
              stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
-  MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
-  c.kind = GK_GEMM2;
-  c.inject_stall = 0;
-  MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
+  if (flags & MM_FLAG_FUSED_FORWARD_GEMMS) {
+    // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored
+    MM_TRY(cudaMemsetAsync(ws + w.off_ready, 0, (size_t)(w.S_pad / BM) * sizeof(int32_t), st));
+    c.kind = GK_FWD_FUSED;
+    MM_TRY(timed(ST_FWD_GEMMS, st, [&] { return launch_gemm(w, ws, c, st); }));
+    c.inject_stall = 0;
+  } else {
+    MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
+    c.kind = GK_GEMM2;
+    c.inject_stall = 0;
+    MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
+  }
   const void* extra = nullptr;
   const void* extra_lo = nullptr;
   if (p.shared) {  // the shared expert: identity routing over all tokens, weight 1

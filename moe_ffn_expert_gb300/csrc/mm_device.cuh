@@ -69,6 +69,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Cross-CTA release/acquire of a counter in global memory, and the proxy fence that orders a
+// thread's generic-proxy view of global memory with its async-proxy (TMA) accesses.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits (bounded by limit_ns of %globaltimer) until *p >= target; false if the limit ran out.
+__device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t limit_ns) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(p) >= target) return true;
+    }
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------------ TMA (bulk tensor copies)
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -64,6 +64,7 @@ struct alignas(128) EpiMaps {
   CUtensorMap dgu_hi, dgu_lo, hw_hi, hw_lo;
   CUtensorMap out;  // the bf16 output of GEMM2, INPUT_GRAD and the weight gradients
   CUtensorMap out_lo;  // its lo part (GEMM2 / INPUT_GRAD with split_out)
+  CUtensorMap a2, b2;  // the fused forward's second GEMM: h rows and W_down
 };
 
 static_assert(offsetof(EpiMaps, out_lo) == offsetof(EpiMaps, out) + sizeof(CUtensorMap),
@@ -101,14 +102,19 @@ struct Args {
   int accumulate;  // weight gradients: reduce-add into the output
   int split_out;   // GEMM2 / INPUT_GRAD: store the output as bf16 hi and lo planes
   int wgrad_f32;   // weight gradients: fp32 output (else bf16)
+  // fused forward: GEMM2 column tiles, reduction blocks, window of row tiles, ready counters
+  int n2, k2, win;
+  int* ready;
+  int ready_target;
 };
 
 template <int KIND>
 struct Traits {
   static constexpr bool WGRAD = (KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
   static constexpr bool A_MN = WGRAD;
-  static constexpr bool B_MN =
-      (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
+  static constexpr bool FUSED = (KIND == GK_FWD_FUSED);
+  static constexpr bool B_MN = (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || FUSED ||
+                                KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
   // The weight gradients' split operand (bf16 hi + lo, two MMAs per k-step into one fp32
   // accumulator) is always A: W2Grad computes (w h)^T dy_rows with A = w h; W1Grad computes the
   // transpose dW_up^T = [d_gate|d_up]^T x_rows with A = [d_gate|d_up] and its epilogue stores the
@@ -131,9 +137,11 @@ struct Traits {
   static constexpr int STAGES = (GU_STAGING || WGRAD) ? 3 : 4;
   // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
   // buffers) and store it with TMA
-  static constexpr bool OUT_STAGING = (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD);
-  // GEMM1 copies its outputs out through a 4 KB per-warp buffer with coalesced stores
-  static constexpr bool ROW_STAGING = (KIND == GK_GEMM1_SWIGLU);
+  static constexpr bool OUT_STAGING =
+      (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD || FUSED);
+  // GEMM1 copies its outputs out through a 4 KB per-warp buffer with coalesced stores (the
+  // fused forward uses the same 4 KB for both of its epilogues)
+  static constexpr bool ROW_STAGING = (KIND == GK_GEMM1_SWIGLU || FUSED);
   static constexpr int EPI_BYTES = GU_STAGING    ? NUM_EPI_WARPS * (GU_CHUNK_BYTES + OUT_CHUNK_BYTES)
                                    : OUT_STAGING ? NUM_EPI_WARPS * 2 * OUT_TILE_BYTES
                                    : ROW_STAGING ? NUM_EPI_WARPS * 4096
@@ -144,12 +152,61 @@ struct Traits {
 
 struct Tile {
   int e, m0, n0, kiters, row0;
+  int part;  // fused forward: 0 = GEMM1 + SwiGLU tile, 1 = GEMM2 tile
 };
 
 template <int KIND>
 __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   Tile t;
-  if constexpr (Traits<KIND>::WGRAD) {
+  t.part = 0;
+  if constexpr (Traits<KIND>::FUSED) {
+    // Order: GEMM1 tiles of row-tile window 0, then for each later window w its GEMM1 tiles
+    // followed by window w-1's GEMM2 tiles, then the last window's GEMM2 tiles. Every GEMM2
+    // tile of a row block comes after all of that block's GEMM1 tiles, and about a window of
+    // GEMM1 work separates them.
+    const int nm = __ldg(a.hdr + HDR_NUM_MTILES);
+    const int W = a.win, n1 = a.n_tiles_n, n2 = a.n2;
+    const int nw = (nm + W - 1) / W;
+    const int mL = nm - (nw - 1) * W;  // row tiles of the last window
+    const int A = W * n1, B = W * n2;
+    int i = tile, w, part, r;
+    const int first = (nw == 1 ? mL : W) * n1;
+    if (i < first) {
+      w = 0, part = 0, r = i;
+    } else {
+      i -= first;
+      const int full_pairs = nw >= 2 ? nw - 2 : 0;
+      if (i < full_pairs * (A + B)) {
+        const int p = i / (A + B), q = i - p * (A + B);
+        if (q < A)
+          w = p + 1, part = 0, r = q;
+        else
+          w = p, part = 1, r = q - A;
+      } else {
+        i -= full_pairs * (A + B);
+        if (nw >= 2 && i < mL * n1) {
+          w = nw - 1, part = 0, r = i;
+        } else {
+          if (nw >= 2) i -= mL * n1;
+          if (nw >= 2 && i < B) {
+            w = nw - 2, part = 1, r = i;
+          } else {
+            if (nw >= 2) i -= B;
+            w = nw - 1, part = 1, r = i;
+          }
+        }
+      }
+    }
+    const int n = part ? n2 : n1;
+    const int mt = w * W + r / n;
+    const int nt = r - (r / n) * n;
+    t.part = part;
+    t.e = __ldg(a.tile_expert + mt);
+    t.m0 = mt * BM;
+    t.n0 = part ? nt * BN : nt * (BN / 2);
+    t.row0 = t.m0;
+    t.kiters = part ? a.k2 : a.k_iters;
+  } else if constexpr (Traits<KIND>::WGRAD) {
     const int per_e = a.m_tiles_w * a.n_tiles_n;
     t.e = tile / per_e;
     const int rem = tile - t.e * per_e;
@@ -569,8 +626,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = TR::WGRAD ? a.E * a.m_tiles_w * a.n_tiles_n
-                              : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
+  const int total = TR::WGRAD   ? a.E * a.m_tiles_w * a.n_tiles_n
+                    : TR::FUSED ? a.hdr[HDR_NUM_MTILES] * (a.n_tiles_n + a.n2)
+                                : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -588,6 +646,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     if constexpr (TR::A_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
     if constexpr (TR::OUT_STAGING) tma_prefetch_desc(&em.out);
+    if constexpr (TR::FUSED) {
+      tma_prefetch_desc(&em.a2);
+      tma_prefetch_desc(&em.b2);
+    }
     if constexpr (TR::GU_STAGING) {
       tma_prefetch_desc(&em.dgu_hi);
       tma_prefetch_desc(&em.dgu_lo);
@@ -611,6 +673,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode_tile<KIND>(a, tile);
+        if constexpr (TR::FUSED) {
+          // a GEMM2 tile waits until every GEMM1 tile of its row block has stored its h rows
+          // (each of their epilogue warps counts once), then orders those generic-proxy writes
+          // before its TMA reads
+          if (t.part == 1) {
+            if (!wait_counter(a.ready + t.m0 / BM, a.ready_target, tmo)) {
+              set_status(a.status, MM_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();
+          }
+        }
         for (int kb = 0; kb < t.kiters; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, tmo)) {
@@ -629,10 +704,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d(sa + TR::A_LO_OFF + MN_BLOCK_BYTES, &tmL, full_bar(s), t.m0 + 64,
                           t.row0 + k0);
             }
+          } else if constexpr (TR::FUSED) {
+            tma_load_2d(sa, t.part ? &em.a2 : &tmA, full_bar(s), k0, t.m0);
           } else {
             tma_load_2d(sa, &tmA, full_bar(s), k0, t.m0);
           }
-          if constexpr (KIND == GK_GEMM1_SWIGLU) {
+          if constexpr (TR::FUSED) {
+            if (t.part == 0) {
+              tma_load_3d(sb + 0 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0, k0, t.e);
+              tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
+              tma_load_3d(sb + 2 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0, k0, t.e);
+              tma_load_3d(sb + 3 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0 + 64, k0, t.e);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d(sb + j * MN_BLOCK_BYTES, &em.b2, full_bar(s), t.n0 + 64 * j, k0, t.e);
+            }
+          } else if constexpr (KIND == GK_GEMM1_SWIGLU) {
             tma_load_3d(sb + 0 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0, k0, t.e);
             tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
             tma_load_3d(sb + 2 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0, k0, t.e);
@@ -729,6 +817,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
+      if constexpr (TR::FUSED) {
+        if (t.part == 0) {
+          // the staging buffer may still be read by this warp's TMA stores of a GEMM2 tile
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw), acce_bar(buf));
+          // this warp's h (and gate|up) stores are visible device-wide, then it counts once
+          __threadfence();
+          fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) atomicAdd(a.ready + t.m0 / BM, 1);
+        } else {
+          staged_store_tile<GK_GEMM2>(a, t, tacc, q, hf, lane, &em.out, sbuf,
+                                      smem_raw + (sbuf - raw), chunk_no);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce_bar(buf));
+        }
+        ++acc_it;
+        continue;
+      }
       if constexpr (TR::ROW_STAGING) {  // releases the accumulator itself
         gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw), acce_bar(buf));
         ++acc_it;
@@ -891,6 +1000,28 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.ld1 = I;
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
+    case GK_FWD_FUSED:
+      ok = map_rows(&ta, xrows, H, nrows, 64, BM) &&
+           map_experts(&tb, c.w_up, 2 * I, H, E, 64, 64) &&
+           map_rows(&em.a2, ws + w.off_h, I, S_pad, 64, BM) &&
+           map_experts(&em.b2, c.w_down, H, I, E, 64, 64);
+      a.n_tiles_n = cdiv(I, BN / 2);
+      a.k_iters = cdiv(H, BK);
+      a.n2 = cdiv(H, BN);
+      a.k2 = cdiv(I, BK);
+      // GEMM1 windows of 128 row tiles (~5 waves of GEMM1 tiles) between a row block's GEMM1
+      // and GEMM2 tiles: windows of 8 or 32 row tiles, which interleave the two GEMMs more
+      // finely, were 27 % and 6 % slower on a GB300; 128 and one window were equal to two launches
+      a.win = 128;
+      a.ready = reinterpret_cast<int*>(ws + w.off_ready);
+      a.ready_target = NUM_EPI_WARPS * a.n_tiles_n;
+      a.N = (int)I;
+      a.out0 = ws + w.off_gu;  // fp32
+      a.ld0 = 2 * I;
+      a.out1 = bf(w.off_h);
+      a.ld1 = I;
+      tiles_max = m_tiles_max * (a.n_tiles_n + a.n2);
+      break;
     case GK_GEMM2:
       ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, BM) &&
            map_experts(&tb, c.w_down, H, I, E, 64, 64);
@@ -985,11 +1116,18 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   if (!ok) return cudaErrorInvalidValue;
   if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
   if (!has_em) em.dgu_hi = em.dgu_lo = em.hw_hi = em.hw_lo = ta;  // unused but initialised
+  if constexpr (!Traits<KIND>::FUSED) em.a2 = em.b2 = ta;                // unused but initialised
   if constexpr (Traits<KIND>::OUT_STAGING) {
     // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_64B;
-    if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N] ([E][N][M] transposed), bf16 or fp32
+    if constexpr (Traits<KIND>::FUSED) {  // GEMM2's o rows [S_pad][H]
+      const uint64_t d2[2] = {(uint64_t)H, (uint64_t)S_pad};
+      const uint64_t s2[1] = {(uint64_t)H * 2};
+      const uint32_t b2[2] = {32, 32};
+      if (!make_map(&em.out, ws + w.off_o, 2, d2, s2, b2, BF, SW)) return cudaErrorInvalidValue;
+      em.out_lo = em.out;  // unused but initialised
+    } else if constexpr (Traits<KIND>::WGRAD) {  // [E][M][N] ([E][N][M] transposed), bf16 or fp32
       a.wgrad_f32 = c.wgrad_f32 ? 1 : 0;
       const uint64_t es = a.wgrad_f32 ? 4 : 2;
       const bool tr = Traits<KIND>::TRANSPOSED_OUT;
@@ -1032,6 +1170,7 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
     case GK_INPUT_GRAD: return run<GK_INPUT_GRAD>(w, ws, c, st);
     case GK_W2_GRAD: return run<GK_W2_GRAD>(w, ws, c, st);
     case GK_W1_GRAD: return run<GK_W1_GRAD>(w, ws, c, st);
+    case GK_FWD_FUSED: return run<GK_FWD_FUSED>(w, ws, c, st);
   }
   return cudaErrorInvalidValue;
 }

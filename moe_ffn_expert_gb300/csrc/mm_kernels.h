@@ -39,6 +39,8 @@ enum GemmKind {
   GK_INPUT_GRAD = 3,    // dx_slot = dgu W_up[e]^T
   GK_W2_GRAD = 4,       // dW_down[e] = hw_e^T dy_slot_e
   GK_W1_GRAD = 5,       // dW_up[e] = x_slot_e^T dgu_e
+  GK_FWD_FUSED = 6,     // GEMM1 + SwiGLU and GEMM2 in one launch, GEMM2 row blocks released by
+                        // ready counters that GEMM1's epilogue increments
 };
 
 struct GemmCall {

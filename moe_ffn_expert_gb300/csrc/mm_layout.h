@@ -42,7 +42,8 @@ enum Stage {
   ST_INPUT_GRAD,
   ST_COMBINE_DX,
   ST_W1_GRAD,
-  ST_SHARED,  // every launch of the shared expert (forward and backward)
+  ST_SHARED,     // every launch of the shared expert (forward and backward)
+  ST_FWD_GEMMS,  // the fused GEMM1 + SwiGLU -> GEMM2 launch
   ST_COUNT
 };
 static_assert(ST_COUNT == MM_NUM_STAGES, "stage table");
@@ -54,6 +55,7 @@ struct Workspace {
   int64_t n_chunks;     // routing chunks of ROUTE_CHUNK slots
   int64_t n_act_tiles;  // rows of the d_topk partials: 2 column halves x ceil(I / BN) tiles
   size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
+  size_t off_ready;  // int32 [S_pad / BM] fused forward: GEMM1 epilogue warps done per row tile
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
   size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
   size_t off_gu;       // fp32 [S_pad, 2I]  gate|up accumulators (kept for the backward)

@@ -108,3 +108,34 @@ def test_torch_entry_point_tokens_per_expert():
     with pytest.raises(_abi.MMError):
         hyper_mega_moe(inp["x"], inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"],
                        tokens_per_expert=bad)
+
+
+@pytest.mark.parametrize("T,H,I,E,K", [(1, 64, 64, 1, 1),        # one row tile
+                                       (1000, 256, 72, 7, 3),    # ragged I, a few row tiles
+                                       (4096, 512, 256, 16, 4),  # two windows of row tiles
+                                       (9000, 256, 128, 40, 6)])  # four windows, ragged last
+def test_fused_forward_gemms_equal_two_launches(T, H, I, E, K):
+    """The one-launch forward (GEMM2 row blocks released by ready counters) and the two-launch
+    forward compute the same tiles with the same arithmetic: y is identical bit for bit, and so
+    is everything the backward derives from the saved activations."""
+    w = synth.small("fused", T, H, I, E, K, seed=T)
+    inp = make_inputs(w)
+    a = run_layer(inp, flags=_abi.MM_FLAG_FUSED_FORWARD_GEMMS)
+    b = run_layer(inp)
+    assert a["status"] == _abi.MM_OK and b["status"] == _abi.MM_OK
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_fused_forward_bounded_waits_end_the_call():
+    """With the stall hook the fused launch's withheld hand-off leaves one row block's ready
+    counter short: the GEMM2 tiles waiting on it give up after the bound, the call reports
+    MM_ERR_TIMEOUT, and the next fused call on the same workspace is clean."""
+    w = synth.small("fstall", 2000, 256, 128, 8, 4, seed=3)
+    inp = make_inputs(w)
+    fused = _abi.MM_FLAG_FUSED_FORWARD_GEMMS
+    bad = run_layer(inp, flags=fused | _abi.MM_FLAG_TEST_STALL, backward=False)
+    assert bad["status"] == _abi.MM_ERR_TIMEOUT
+    good = run_layer(inp, flags=fused, ws=bad["ws"], backward=False)
+    assert good["status"] == _abi.MM_OK
+    assert torch.equal(good["y"], run_layer(inp, backward=False)["y"])
