@@ -222,7 +222,7 @@ def run_gpu(args):
 
     def fwd(bf=bufs0):
         args_f = (bf["x"].data_ptr(), bf["ids"].data_ptr(), bf["tw"].data_ptr(), wu.data_ptr(),
-                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, st, 0)
+                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, st, args.fwd_flags)
         if I_s:
             _abi.check(_abi.mm_forward_ex(d, opt, *args_f), "fwd")
         else:
@@ -386,6 +386,7 @@ def run_gpu(args):
                                + (f" shared I_s={I_s}" if I_s else ""), "T": T, "H": H, "I": I,
                    "E": E, "K": K, "routing": w.routing, "seed": w.seed,
                    **({"shared_I": I_s} if I_s else {}),
+                   **({"forward_flags": hex(args.fwd_flags)} if args.fwd_flags else {}),
                    "l2": "inputs larger than L2: 1.2 GB of expert weights and 0.6 GB of slot rows per step",
                    "parallelism": "single GPU" if world == 1 else f"{world} independent replicas"},
         "tflops": round(tflops, 2),
@@ -516,6 +517,9 @@ def main(argv=None):
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (profiling captures: fewer tokens "
                          "with the same rows per expert)")
+    ap.add_argument("--fwd-flags", type=lambda v: int(v, 0), default=0,
+                    help="mm_forward flags, e.g. 0x8 (one-launch forward GEMMs), 0x10 (combine in "
+                         "GEMM2's epilogue)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--shared-intermediate", type=int, default=0,
                     help="add a shared expert of this intermediate size (0: none)")

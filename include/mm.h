@@ -89,6 +89,13 @@ typedef struct mm_dims {
  * GB300 both take the same time, so the default is the two launches. */
 #define MM_FLAG_FUSED_FORWARD_GEMMS 0x8u
 
+/* mm_forward flag: fold the weighted combine into GEMM2's epilogue instead of running it as its
+ * own kernel. Each epilogue warp, after its o rows are stored and visible, counts each row's token
+ * once per 128-column chunk (counters in the workspace); the warp that brings a token's count to K
+ * sums that token's K rows of the chunk in slot order and writes y (the RFC's per-token arrival
+ * counting at Combine, §2.1, §5.1). y is identical bit for bit to the separate combine's. */
+#define MM_FLAG_FUSED_COMBINE 0x10u
+
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
  * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is

@@ -179,6 +179,7 @@ bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows) {
   p.off_chunk = take((size_t)p.n_chunks * d.E * sizeof(int32_t));
   p.off_tile_expert = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
   p.off_ready = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
+  p.off_cnt = take((size_t)d.T * ((d.H + 127) / 128) * sizeof(int32_t));
   p.off_row_of_slot = take((size_t)p.S * sizeof(int32_t));
   p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
   p.off_w_row = take((size_t)p.S_pad * sizeof(float));
@@ -298,18 +299,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
              stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
-  if (flags & MM_FLAG_FUSED_FORWARD_GEMMS) {
-    // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored
-    MM_TRY(cudaMemsetAsync(ws + w.off_ready, 0, (size_t)(w.S_pad / BM) * sizeof(int32_t), st));
-    c.kind = GK_FWD_FUSED;
-    MM_TRY(timed(ST_FWD_GEMMS, st, [&] { return launch_gemm(w, ws, c, st); }));
-    c.inject_stall = 0;
-  } else {
-    MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
-    c.kind = GK_GEMM2;
-    c.inject_stall = 0;
-    MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
-  }
+  // the shared expert first: its output rows must exist before a combine reads them
   const void* extra = nullptr;
   const void* extra_lo = nullptr;
   if (p.shared) {  // the shared expert: identity routing over all tokens, weight 1
@@ -324,9 +314,31 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
     extra = wss + p.ws_s.off_o;
     extra_lo = wss + p.ws_s.off_o_lo;
   }
-  MM_TRY(timed(ST_COMBINE_Y, st, [&] {
-    return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo);
-  }));
+  const bool fuse_combine = (flags & MM_FLAG_FUSED_COMBINE) != 0;
+  if (fuse_combine) {  // GEMM2's epilogue sums y; its per-(token, chunk) counters start at zero
+    MM_TRY(cudaMemsetAsync(ws + w.off_cnt, 0,
+                           (size_t)w.T * ((w.H + 127) / 128) * sizeof(int32_t), st));
+    c.comb_y = y;
+    c.comb_w = topk_weights;
+    c.comb_extra = extra;
+    c.comb_extra_lo = extra_lo;
+  }
+  if (flags & MM_FLAG_FUSED_FORWARD_GEMMS) {
+    // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored
+    MM_TRY(cudaMemsetAsync(ws + w.off_ready, 0, (size_t)(w.S_pad / BM) * sizeof(int32_t), st));
+    c.kind = GK_FWD_FUSED;
+    MM_TRY(timed(ST_FWD_GEMMS, st, [&] { return launch_gemm(w, ws, c, st); }));
+    c.inject_stall = 0;
+  } else {
+    MM_TRY(timed(ST_GEMM1_SWIGLU, st, [&] { return launch_gemm(w, ws, c, st); }));
+    c.kind = fuse_combine ? GK_GEMM2_COMBINE : GK_GEMM2;
+    c.inject_stall = 0;
+    MM_TRY(timed(ST_GEMM2, st, [&] { return launch_gemm(w, ws, c, st); }));
+  }
+  if (!fuse_combine)
+    MM_TRY(timed(ST_COMBINE_Y, st, [&] {
+      return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo);
+    }));
   return MM_OK;
 }
 

@@ -106,6 +106,17 @@ struct Args {
   int n2, k2, win;
   int* ready;
   int ready_target;
+  // GEMM2 with the combine fused into its epilogue (y[t] summed by the last of its K slots)
+  int fuse_combine;
+  int* cnt;                       // [T][comb_nch] slots stored so far per 128-column chunk
+  const int32_t* slot_of_row;
+  const int32_t* row_of_slot;
+  const float* comb_w;            // routing weights [T][K]
+  const __nv_bfloat16* comb_o;    // o rows [S_pad][H]
+  const __nv_bfloat16* comb_extra;     // optional row per token added with weight 1 (hi)
+  const __nv_bfloat16* comb_extra_lo;  // and its lo part
+  __nv_bfloat16* comb_y;          // [T][H]
+  int comb_K, comb_H, comb_nch;
 };
 
 template <int KIND>
@@ -113,7 +124,8 @@ struct Traits {
   static constexpr bool WGRAD = (KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
   static constexpr bool A_MN = WGRAD;
   static constexpr bool FUSED = (KIND == GK_FWD_FUSED);
-  static constexpr bool B_MN = (KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || FUSED ||
+  static constexpr bool GEMM2_LIKE = (KIND == GK_GEMM2 || KIND == GK_GEMM2_COMBINE);
+  static constexpr bool B_MN = (KIND == GK_GEMM1_SWIGLU || GEMM2_LIKE || FUSED ||
                                 KIND == GK_W2_GRAD || KIND == GK_W1_GRAD);
   // The weight gradients' split operand (bf16 hi + lo, two MMAs per k-step into one fp32
   // accumulator) is always A: W2Grad computes (w h)^T dy_rows with A = w h; W1Grad computes the
@@ -138,7 +150,7 @@ struct Traits {
   // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
   // buffers) and store it with TMA
   static constexpr bool OUT_STAGING =
-      (KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD || WGRAD || FUSED);
+      (GEMM2_LIKE || KIND == GK_INPUT_GRAD || WGRAD || FUSED);
   // GEMM1 copies its outputs out through a 4 KB per-warp buffer with coalesced stores (the
   // fused forward uses the same 4 KB for both of its epilogues)
   static constexpr bool ROW_STAGING = (KIND == GK_GEMM1_SWIGLU || FUSED);
@@ -601,6 +613,77 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, 
   }
 }
 
+// Combine fused into GEMM2's epilogue, for one warp's 32 rows x 128 columns (chunk j of H)
+// after its o stores: the warp waits for them to complete, makes them visible device-wide, and
+// counts each real row's token once for chunk j. The lane that brings a token's count to K holds
+// its last slot; the warp then sums that token's K rows of chunk j in slot order (fp32, weights,
+// then the optional extra rows) and stores y, with the separate combine kernel's arithmetic.
+__device__ __forceinline__ void fused_combine_warp(const Args& a, const Tile& t, int q, int hf,
+                                                   int lane) {
+  if (lane == 0) bulk_wait_all();
+  __syncwarp();
+  fence_proxy_async_global();
+  __threadfence();
+  const int j = (t.n0 >> 7) + hf;  // 128-column chunk
+  if (j >= a.comb_nch) return;     // this column half lies past H
+  const int K = a.comb_K, H = a.comb_H;
+  const int s = __ldg(a.slot_of_row + t.m0 + q * 32 + lane);
+  int tok = -1;
+  bool last = false;
+  if (s >= 0) {
+    tok = s / K;
+    last = atomicAdd(a.cnt + (size_t)tok * a.comb_nch + j, 1) == K - 1;
+  }
+  unsigned m = __ballot_sync(0xffffffffu, last);
+  if (m == 0) return;
+  __threadfence();  // the other slots' rows, counted before ours, are visible
+  const int col = j * 128 + lane * 4;
+  while (m) {
+    const int src = __ffs(m) - 1;
+    m &= m - 1;
+    const int tk = __shfl_sync(0xffffffffu, tok, src);
+    if (col < H) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int k0 = 0; k0 < K; k0 += 8) {  // eight slots' loads in flight at a time
+        uint2 v[8];
+        float wk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k0 + k < K) {
+            const size_t sk = (size_t)tk * K + k0 + k;
+            wk[k] = a.comb_w ? __ldg(a.comb_w + sk) : 1.0f;
+            v[k] = __ldcg(reinterpret_cast<const uint2*>(
+                a.comb_o + (size_t)__ldg(a.row_of_slot + sk) * H + col));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k0 + k < K) {
+            acc[0] += wk[k] * bf16_lo(v[k].x);
+            acc[1] += wk[k] * bf16_hi(v[k].x);
+            acc[2] += wk[k] * bf16_lo(v[k].y);
+            acc[3] += wk[k] * bf16_hi(v[k].y);
+          }
+        }
+      }
+      const __nv_bfloat16* ex[2] = {a.comb_extra, a.comb_extra_lo};
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (ex[x] != nullptr) {
+          const uint2 e = __ldg(reinterpret_cast<const uint2*>(ex[x] + (size_t)tk * H + col));
+          acc[0] += 1.0f * bf16_lo(e.x);
+          acc[1] += 1.0f * bf16_hi(e.x);
+          acc[2] += 1.0f * bf16_lo(e.y);
+          acc[3] += 1.0f * bf16_hi(e.y);
+        }
+      }
+      *reinterpret_cast<uint2*>(a.comb_y + (size_t)tk * H + col) =
+          make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    }
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -725,7 +808,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
             tma_load_3d(sb + 2 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0, k0, t.e);
             tma_load_3d(sb + 3 * MN_BLOCK_BYTES, &tmB, full_bar(s), a.I + t.n0 + 64, k0, t.e);
-          } else if constexpr (KIND == GK_GEMM2) {
+          } else if constexpr (TR::GEMM2_LIKE) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               tma_load_3d(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, k0, t.e);
@@ -834,6 +917,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acce_bar(buf));
+          if (a.fuse_combine) fused_combine_warp(a, t, q, hf, lane);
         }
         ++acc_it;
         continue;
@@ -849,6 +933,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce_bar(buf));
+      if constexpr (KIND == GK_GEMM2_COMBINE) fused_combine_warp(a, t, q, hf, lane);
       ++acc_it;
     }
     if constexpr (TR::OUT_STAGING) {
@@ -981,6 +1066,20 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.timeout_ns = c.timeout_ns;
   a.inject_stall = c.inject_stall;
   a.accumulate = c.accumulate;
+  if (c.comb_y != nullptr) {  // GEMM2 (or the fused forward) with the combine in its epilogue
+    a.fuse_combine = 1;
+    a.cnt = reinterpret_cast<int*>(ws + w.off_cnt);
+    a.slot_of_row = reinterpret_cast<const int32_t*>(ws + w.off_slot_of_row);
+    a.row_of_slot = reinterpret_cast<const int32_t*>(ws + w.off_row_of_slot);
+    a.comb_w = c.comb_w;
+    a.comb_o = reinterpret_cast<const __nv_bfloat16*>(ws + w.off_o);
+    a.comb_extra = reinterpret_cast<const __nv_bfloat16*>(c.comb_extra);
+    a.comb_extra_lo = reinterpret_cast<const __nv_bfloat16*>(c.comb_extra_lo);
+    a.comb_y = reinterpret_cast<__nv_bfloat16*>(c.comb_y);
+    a.comb_K = (int)w.K;
+    a.comb_H = (int)w.H;
+    a.comb_nch = (int)((w.H + 127) / 128);
+  }
 
   CUtensorMap ta, tb, tl;
   EpiMaps em;
@@ -1023,6 +1122,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       tiles_max = m_tiles_max * (a.n_tiles_n + a.n2);
       break;
     case GK_GEMM2:
+    case GK_GEMM2_COMBINE:
       ok = map_rows(&ta, ws + w.off_h, I, S_pad, 64, BM) &&
            map_experts(&tb, c.w_down, H, I, E, 64, 64);
       a.n_tiles_n = cdiv(H, BN);
@@ -1166,6 +1266,7 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
   switch (c.kind) {
     case GK_GEMM1_SWIGLU: return run<GK_GEMM1_SWIGLU>(w, ws, c, st);
     case GK_GEMM2: return run<GK_GEMM2>(w, ws, c, st);
+    case GK_GEMM2_COMBINE: return run<GK_GEMM2_COMBINE>(w, ws, c, st);
     case GK_ACT_GRAD: return run<GK_ACT_GRAD>(w, ws, c, st);
     case GK_INPUT_GRAD: return run<GK_INPUT_GRAD>(w, ws, c, st);
     case GK_W2_GRAD: return run<GK_W2_GRAD>(w, ws, c, st);

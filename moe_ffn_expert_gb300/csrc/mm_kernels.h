@@ -41,6 +41,7 @@ enum GemmKind {
   GK_W1_GRAD = 5,       // dW_up[e] = x_slot_e^T dgu_e
   GK_FWD_FUSED = 6,     // GEMM1 + SwiGLU and GEMM2 in one launch, GEMM2 row blocks released by
                         // ready counters that GEMM1's epilogue increments
+  GK_GEMM2_COMBINE = 7, // GEMM2 with the weighted combine into y in its epilogue
 };
 
 struct GemmCall {
@@ -55,6 +56,12 @@ struct GemmCall {
   int* status;         // if set: the status word errors are recorded in
   int split_out;       // GEMM2 / INPUT_GRAD: write o as bf16 hi (off_o) + lo (off_o_lo) rows
   int wgrad_f32;       // weight gradients: fp32 output arrays (else bf16)
+  // GEMM2 / fused forward: when comb_y is set, the weighted combine into comb_y runs in the
+  // epilogue (the per-(token, 128-column chunk) counters at off_cnt must be zero)
+  void* comb_y = nullptr;
+  const float* comb_w = nullptr;
+  const void* comb_extra = nullptr;
+  const void* comb_extra_lo = nullptr;
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);

@@ -56,6 +56,7 @@ struct Workspace {
   int64_t n_act_tiles;  // rows of the d_topk partials: 2 column halves x ceil(I / BN) tiles
   size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
   size_t off_ready;  // int32 [S_pad / BM] fused forward: GEMM1 epilogue warps done per row tile
+  size_t off_cnt;    // int32 [T][ceil(H / 128)] fused combine: slots stored per token and chunk
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
   size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
   size_t off_gu;       // fp32 [S_pad, 2I]  gate|up accumulators (kept for the backward)

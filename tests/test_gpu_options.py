@@ -139,3 +139,31 @@ def test_fused_forward_bounded_waits_end_the_call():
     good = run_layer(inp, flags=fused, ws=bad["ws"], backward=False)
     assert good["status"] == _abi.MM_OK
     assert torch.equal(good["y"], run_layer(inp, backward=False)["y"])
+
+
+@pytest.mark.parametrize("T,H,I,E,K", [(1, 64, 64, 1, 1),
+                                       (1000, 136, 72, 7, 3),    # H past the last 128 columns
+                                       (300, 256, 128, 8, 16),   # two batches of 8 slots
+                                       (4096, 512, 256, 16, 4)])
+def test_fused_combine_equals_combine_kernel(T, H, I, E, K):
+    """MM_FLAG_FUSED_COMBINE (the last of a token's K slots sums y inside GEMM2's epilogue) gives
+    y identical bit for bit to the separate combine kernel, alone and with the one-launch
+    forward; the backward is unaffected."""
+    w = synth.small("fcomb", T, H, I, E, K, seed=T + 1)
+    inp = make_inputs(w)
+    ref = run_layer(inp)
+    for flags in (_abi.MM_FLAG_FUSED_COMBINE,
+                  _abi.MM_FLAG_FUSED_COMBINE | _abi.MM_FLAG_FUSED_FORWARD_GEMMS):
+        out = run_layer(inp, flags=flags)
+        assert out["status"] == _abi.MM_OK
+        for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+            assert torch.equal(out[k], ref[k]), (flags, k)
+
+
+def test_fused_combine_with_a_shared_expert():
+    w = synth.small("fcomb_se", 700, 256, 128, 6, 2, seed=4)
+    inp = make_inputs(w)
+    sh = (synth.shared_up(w, 192, device="cuda"), synth.shared_down(w, 192, device="cuda"))
+    ref = run_layer(inp, shared=sh, backward=False)
+    out = run_layer(inp, shared=sh, flags=_abi.MM_FLAG_FUSED_COMBINE, backward=False)
+    assert out["status"] == _abi.MM_OK and torch.equal(out["y"], ref["y"])
