@@ -100,6 +100,20 @@ def test_workload_sampled_parity(name, n_tokens, experts):
     torch.cuda.empty_cache()
 
 
+def test_two_million_slots_sampled_parity():
+    """The largest layer in the tests: 2^21 slots (T=262144, K=8), a 13 GB workspace, row and
+    element offsets far past 2^31 bytes. Routing is checked bit for bit, y/dx/d_topk on sampled
+    tokens and the weight gradients of two experts (32k rows each) against the oracle."""
+    w = synth.small("huge", 262144, 512, 128, 64, 8, seed=11)
+    inp = make_inputs(w)
+    out = run_layer(inp)
+    assert out["status"] == _abi.MM_OK
+    _check_routing(out, inp["topk_ids"], w.E)
+    _check_sampled(inp, out, 24, [0, 63])
+    del out, inp
+    torch.cuda.empty_cache()
+
+
 def test_device_generator_matches_host():
     w = synth.small("g", 3, 64, 16, 5, 2)
     assert torch.equal(synth.w_up(w, device="cuda").cpu(), synth.w_up(w))
