@@ -2,11 +2,15 @@
 //
 // Forward (RFC "HyperParallel Multicore HyperMegaMoE fused forward/backward operator", §2.1):
 //   status clear -> route count -> route scan -> route rank -> gather x rows ->
-//   GEMM1 + SwiGLU -> GEMM2 -> weighted combine into y.
+//   [shared expert GEMM1 + GEMM2] -> GEMM1 + SwiGLU -> GEMM2 -> weighted combine into y
+//   (GEMM1 and GEMM2 in one launch with MM_FLAG_FUSED_FORWARD_GEMMS; the combine inside GEMM2
+//   with MM_FLAG_FUSED_COMBINE).
 // Backward (§2.2): gather dy rows -> act_grad + SwiGLU backward -> d_topk_weights ->
-//   W2Grad -> input_grad -> combine dx -> W1Grad.
+//   W2Grad -> input_grad -> [shared expert act_grad, W2Grad, input_grad] ->
+//   combine dx (side stream) || W1Grad -> [shared expert W1Grad].
 // The host never waits on the device here (except the optional id pre-check); the caller's
-// stream orders everything. The two-phase size query / execute split mirrors §2.3.
+// stream orders everything (the side stream is forked from it and joined back within the
+// call). The two-phase size query / execute split mirrors §2.3.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdarg.h>

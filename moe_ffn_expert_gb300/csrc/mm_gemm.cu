@@ -1,25 +1,27 @@
 // Grouped GEMMs of the MoE-FFN layer on the sm_103a tensor cores (tcgen05 + TMEM), fed by TMA.
 //
-// One persistent, warp-specialised kernel template serves all six products of the layer
-// (RFC "HyperParallel Multicore HyperMegaMoE fused forward/backward operator", §2.1 GMM1/GMM2,
-// §2.2 act_grad, input_grad, W2Grad and W1Grad):
+// One persistent, warp-specialised kernel template serves all products of the layer (RFC
+// "HyperParallel Multicore HyperMegaMoE fused forward/backward operator", §2.1 GMM1/GMM2, §2.2
+// act_grad, input_grad, W2Grad and W1Grad), every one on 128 x 256 accumulator tiles:
 //
-//   kind         A (rows x red.)          B (red. x cols)              epilogue
-//   GEMM1        x_slot [rows,H]  K-maj   W_up[e]   [H,2I]  N-major    gu = [gate|up], h = silu(gate)*up
-//   GEMM2        h      [rows,I]  K-maj   W_down[e] [I,H]   N-major    o (bf16)
-//   ACT_GRAD     dy_slot[rows,H]  K-maj   W_down[e]^T       K-major    SwiGLU backward: dgu, hw, <g,h>
-//   INPUT_GRAD   dgu    [rows,2I] K-maj   W_up[e]^T         K-major    dx_slot (bf16)
-//   W2_GRAD      hw_e^T [I,M_e]   M-maj   dy_slot_e [M_e,H] N-major    dW_down[e] (bf16)
-//   W1_GRAD      x_slot_e^T[H,M_e] M-maj  dgu_e [M_e,2I]    N-major    dW_up[e] (bf16)
+//   kind          A (rows x red.)            B (red. x cols)              epilogue
+//   GEMM1         x_slot [rows,H]  K-maj     W_up[e]   [H,2I]  N-major    gu = [gate|up] (fp32), h
+//   GEMM2         h      [rows,I]  K-maj     W_down[e] [I,H]   N-major    o (bf16; hi + lo if split)
+//   ACT_GRAD      dy_slot[rows,H]  K-maj     W_down[e]^T       K-major    SwiGLU backward: dgu, hw, <g,h>
+//   INPUT_GRAD    dgu    [rows,2I] K-maj     W_up[e]^T         K-major    dx_slot (bf16)
+//   W2_GRAD       hw_e^T [I,M_e]   M-maj x2  dy_slot_e [M_e,H] N-major    dW_down[e]
+//   W1_GRAD       dgu_e^T[2I,M_e]  M-maj x2  x_slot_e [M_e,H]  N-major    dW_up[e] (stored transposed)
+//   FWD_FUSED     GEMM1 and GEMM2 tiles in one launch (GEMM2 row blocks released by counters)
+//   GEMM2_COMBINE GEMM2 whose epilogue also sums y for the tokens whose last slot it stores
 //
 // Precision of the weight gradients. They reduce over all rows of an expert (hundreds to
 // thousands), so a bf16 rounding of every row of an operand would leave errors of ~0.5% of the
 // gradient's rms. The forward therefore keeps the gate|up accumulators in fp32, and the
 // act_grad epilogue writes w*h and [d_gate|d_up] as two bf16 planes, hi = bf16(v) and
-// lo = bf16(v - hi), which together carry ~16 mantissa bits. W2_GRAD issues two MMAs per
-// k-step (hw_hi and hw_lo against the same dy tile), W1_GRAD two (x against dgu_hi and dgu_lo),
-// both accumulating into one fp32 accumulator; their column tiles are 128 wide so every
-// stage still holds 48 KB.
+// lo = bf16(v - hi), which together carry ~16 mantissa bits. Both weight gradients put that pair
+// on the A side ("x2" above) and issue two MMAs per k-step (hi and lo against the same B tile)
+// into one fp32 accumulator; W1_GRAD therefore computes dW_up^T and its epilogue transposes.
+// Their stages hold A hi, A lo and B: 64 KB, three of them.
 //
 // Row-grouped kinds walk 128-row tiles of the expert-sorted (padded) row buffers; each tile
 // belongs to one expert, whose weight slab is the third coordinate of a 3-D tensor map.
@@ -27,14 +29,14 @@
 // the expert's padded rows (pad rows are zero, an expert with no rows gets a zero tile).
 //
 // Warp roles (320 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
-//   warp 0      one thread issues TMA loads into a 4-stage shared-memory ring (mbarrier per
-//               stage, transaction-count completion);
+//   warp 0      one thread issues TMA loads into a 4-stage (3 for act_grad and the weight
+//               gradients) shared-memory ring (mbarrier per stage, transaction-count completion);
 //   warp 1      allocates 2*BN TMEM columns (two 128xBN fp32 accumulators); one thread issues
 //               tcgen05.mma (128xBNx16 per instruction) and tcgen05.commit's the stage and
 //               accumulator barriers;
 //   warps 2-9   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
-//               i.e. one tile row per thread; warps w and w+4 take one column half each), apply
-//               the kind's epilogue, store to global memory,
+//               32 tile rows; warps w and w+4 take one column half each), apply the kind's
+//               epilogue through per-warp shared-memory staging (TMA or coalesced stores), and
 //               release the accumulator so the next tile's MMAs overlap this epilogue.
 // All operand tiles use the 128-byte swizzle; every mbarrier wait is bounded by %globaltimer and
 // a wait that runs out records MM_ERR_TIMEOUT, stops the role and still frees TMEM.
