@@ -220,9 +220,10 @@ def run_gpu(args):
 
     bufs0 = dict(x=x, ids=ids, tw=tw, dy=dy, y=y, dx=dx, dtk=dtk)
 
-    def fwd(bf=bufs0):
+    def fwd(bf=bufs0, extra_flags=0):
         args_f = (bf["x"].data_ptr(), bf["ids"].data_ptr(), bf["tw"].data_ptr(), wu.data_ptr(),
-                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, st, args.fwd_flags)
+                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, st,
+                  args.fwd_flags | extra_flags)
         if I_s:
             _abi.check(_abi.mm_forward_ex(d, opt, *args_f), "fwd")
         else:
@@ -283,6 +284,7 @@ def run_gpu(args):
     # ---- forward alone and backward alone (short extra passes)
     n_part = max(3, min(args.steps, 10))
     fwd_ms = timed(fwd, n_part) / n_part
+    infer_ms = timed(lambda: fwd(extra_flags=_abi.MM_FLAG_FORWARD_ONLY), n_part) / n_part
     fwd()
     bwd_ms = timed(bwd, n_part) / n_part
 
@@ -394,6 +396,10 @@ def run_gpu(args):
                               "sustained": round(tflops / peak_sus, 4), "peaks": peak_src},
         "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(T / (fwd_ms / 1e3), 1),
                 "tflops": round(flops["fwd"] / (fwd_ms / 1e3) / 1e12, 2)},
+        "fwd_inference": {"ms": round(infer_ms, 4),
+                          "tokens_per_s": round(T / (infer_ms / 1e3), 1),
+                          "tflops": round(flops["fwd"] / (infer_ms / 1e3) / 1e12, 2),
+                          "note": "mm_forward with MM_FLAG_FORWARD_ONLY (no gate|up kept)"},
         "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(T / (bwd_ms / 1e3), 1),
                 "tflops": round(flops["bwd"] / (bwd_ms / 1e3) / 1e12, 2)},
         "first_call_ms": round(first_ms, 3),

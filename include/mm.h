@@ -96,6 +96,11 @@ typedef struct mm_dims {
  * counting at Combine, §2.1, §5.1). y is identical bit for bit to the separate combine's. */
 #define MM_FLAG_FUSED_COMBINE 0x10u
 
+/* mm_forward flag: a forward with no backward to follow (inference). GEMM1 stores h only, not
+ * the fp32 gate|up activations a backward needs. An mm_backward on that workspace records
+ * MM_ERR_INVALID_ARG in the status word and its GEMMs do nothing (outputs unspecified). */
+#define MM_FLAG_FORWARD_ONLY 0x20u
+
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
  * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is

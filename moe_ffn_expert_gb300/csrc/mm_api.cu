@@ -303,6 +303,11 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
              stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
+  if (flags & MM_FLAG_FORWARD_ONLY) {  // no gate|up kept; a backward from here is refused
+    c.skip_gu = 1;
+    MM_TRY(cudaMemsetAsync(ws + w.off_hdr + HDR_NO_BACKWARD * sizeof(int32_t), 1,
+                           sizeof(int32_t), st));
+  }
   // the shared expert first: its output rows must exist before a combine reads them
   const void* extra = nullptr;
   const void* extra_lo = nullptr;
@@ -311,6 +316,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
     GemmCall cs{GK_GEMM1_SWIGLU, se->up_proj_weight, se->down_proj_weight, nullptr,
                 c.timeout_ns, 0, 0, x, reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS,
                 1};  // its output is added with weight 1: kept as a bf16 hi + lo pair
+    cs.skip_gu = c.skip_gu;
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_shared_tables(p.ws_s, wss, st); }));
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
     cs.kind = GK_GEMM2;

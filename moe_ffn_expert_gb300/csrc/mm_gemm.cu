@@ -119,6 +119,7 @@ struct Args {
   const __nv_bfloat16* comb_extra_lo;  // and its lo part
   __nv_bfloat16* comb_y;          // [T][H]
   int comb_K, comb_H, comb_nch;
+  int skip_gu;  // GEMM1: forward only, gate|up are not stored
 };
 
 template <int KIND>
@@ -337,14 +338,16 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
       u[j] = __uint_as_float(ub[j]);
       h[j] = g[j] * sigmoidf_(g[j]) * u[j];
     }
-    stage_row_f32(stage, lane, g);
-    __syncwarp();
-    copy_out_f32(stage, lane, gu, row0, a.ld0, n, a.I);
-    __syncwarp();
-    stage_row_f32(stage, lane, u);
-    __syncwarp();
-    copy_out_f32(stage, lane, gu + a.I, row0, a.ld0, n, a.I);
-    __syncwarp();
+    if (!a.skip_gu) {  // gate|up are kept only for a backward
+      stage_row_f32(stage, lane, g);
+      __syncwarp();
+      copy_out_f32(stage, lane, gu, row0, a.ld0, n, a.I);
+      __syncwarp();
+      stage_row_f32(stage, lane, u);
+      __syncwarp();
+      copy_out_f32(stage, lane, gu + a.I, row0, a.ld0, n, a.I);
+      __syncwarp();
+    }
     stage_row_bf16(stage, lane, h);
     __syncwarp();
     copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I);
@@ -693,8 +696,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
            const Args a) {
   using TR = Traits<KIND>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform)
-  if (__syncthreads_or(a.hdr[HDR_STATUS] != 0)) return;
+  // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform); the status
+  // word is the call's (the shared expert's launches point at the routed layout's word too)
+  if (__syncthreads_or(*a.status != 0)) return;
+  if constexpr (KIND == GK_ACT_GRAD) {
+    // the forward on this workspace kept no gate|up (forward-only): no backward from it
+    if (__syncthreads_or(a.hdr[HDR_NO_BACKWARD] != 0)) {
+      if (threadIdx.x == 0) set_status(a.status, MM_ERR_INVALID_ARG);
+      return;
+    }
+  }
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   constexpr int STAGES = TR::STAGES;
@@ -1068,6 +1079,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   a.timeout_ns = c.timeout_ns;
   a.inject_stall = c.inject_stall;
   a.accumulate = c.accumulate;
+  a.skip_gu = c.skip_gu;
   if (c.comb_y != nullptr) {  // GEMM2 (or the fused forward) with the combine in its epilogue
     a.fuse_combine = 1;
     a.cnt = reinterpret_cast<int*>(ws + w.off_cnt);

@@ -58,6 +58,7 @@ struct GemmCall {
   int wgrad_f32;       // weight gradients: fp32 output arrays (else bf16)
   // GEMM2 / fused forward: when comb_y is set, the weighted combine into comb_y runs in the
   // epilogue (the per-(token, 128-column chunk) counters at off_cnt must be zero)
+  int skip_gu = 0;     // GEMM1 / fused forward: do not store gate|up (forward only)
   void* comb_y = nullptr;
   const float* comb_w = nullptr;
   const void* comb_extra = nullptr;

@@ -23,6 +23,7 @@ enum HeaderWord {
   HDR_STATUS = 0,      // mm_status of the call (0 = OK)
   HDR_NUM_MTILES = 1,  // number of BM-row tiles over all experts (padded rows / BM)
   HDR_BAD_SLOT = 2,    // first slot seen with an invalid expert id (diagnostics)
+  HDR_NO_BACKWARD = 3, // nonzero: the forward kept no gate|up (MM_FLAG_FORWARD_ONLY)
   HDR_WORDS = 64
 };
 

@@ -278,9 +278,8 @@ __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts
                                                        int32_t* row_of_slot, int T) {
   const int Tp = (T + BM - 1) / BM * BM;
   const int r = blockIdx.x * 256 + threadIdx.x;
+  if (r < HDR_WORDS) hdr[r] = r == HDR_NUM_MTILES ? Tp / BM : 0;  // every header word
   if (r == 0) {
-    hdr[HDR_STATUS] = 0;
-    hdr[HDR_NUM_MTILES] = Tp / BM;
     counts[0] = T;
     offsets[0] = 0;
     offsets[1] = T;

@@ -167,3 +167,38 @@ def test_fused_combine_with_a_shared_expert():
     ref = run_layer(inp, shared=sh, backward=False)
     out = run_layer(inp, shared=sh, flags=_abi.MM_FLAG_FUSED_COMBINE, backward=False)
     assert out["status"] == _abi.MM_OK and torch.equal(out["y"], ref["y"])
+
+
+def test_accumulate_with_a_shared_expert():
+    """With MM_FLAG_ACCUMULATE_WEIGHT_GRADS (fp32 outputs: one exact fp32 add per element) the
+    shared expert's gradients are added into their buffers like the routed ones."""
+    w, inp = _inputs(T=260, E=6, seed=43, empty_last=False)
+    sh = (synth.shared_up(w, 128, device="cuda"), synth.shared_down(w, 128, device="cuda"))
+    ref = run_layer(inp, shared=sh, bwd_flags=F32)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    bases = {k: torch.randn(ref[k].shape, generator=g, device="cuda")
+             for k in ("dW_up", "dW_down", "dS_up", "dS_down")}
+    out = run_layer(inp, shared=sh, bwd_flags=F32 | ACC, d_up=bases["dW_up"].clone(),
+                    d_down=bases["dW_down"].clone(), ds_up=bases["dS_up"].clone(),
+                    ds_down=bases["dS_down"].clone())
+    assert out["status"] == _abi.MM_OK
+    for k, base in bases.items():
+        assert torch.equal(out[k], base + ref[k]), k
+
+
+def test_forward_only_keeps_y_and_refuses_a_backward():
+    """MM_FLAG_FORWARD_ONLY skips the gate|up save: y is unchanged bit for bit (with and without a
+    shared expert), a backward on that workspace reports MM_ERR_INVALID_ARG, and a normal forward
+    on the same workspace then allows the backward again."""
+    w, inp = _inputs(T=500, E=6, seed=47, empty_last=False)
+    sh = (synth.shared_up(w, 64, device="cuda"), synth.shared_down(w, 64, device="cuda"))
+    for shared in (None, sh):
+        ref = run_layer(inp, shared=shared)
+        assert ref["status"] == _abi.MM_OK
+        out = run_layer(inp, shared=shared, flags=_abi.MM_FLAG_FORWARD_ONLY)
+        assert torch.equal(out["y"], ref["y"])
+        assert out["status"] == _abi.MM_ERR_INVALID_ARG
+        again = run_layer(inp, shared=shared, ws=out["ws"])
+        assert again["status"] == _abi.MM_OK
+        for k in ("y", "dx", "dW_up", "dW_down"):
+            assert torch.equal(again[k], ref[k]), k
