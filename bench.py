@@ -271,8 +271,19 @@ def run_gpu(args):
     sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else uuid).start()
     _abi.mm_timing_read()
     _abi.mm_timing_enable(True)
-    elapsed = timed(step, args.steps)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    step_i = [0]
+
+    def step_marked():  # one event per step boundary: the per-step median and minimum
+        if step_i[0] == 0:
+            step_ev[0].record(stream)
+        step()
+        step_i[0] += 1
+        step_ev[step_i[0]].record(stream)
+
+    elapsed = timed(step_marked, args.steps)
     _abi.mm_timing_enable(False)
+    per_step = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
     stages = _abi.mm_timing_read()
     clocks = sampler.stop()
     if _abi.mm_get_status(ws.data_ptr(), st) != _abi.MM_OK:
@@ -367,6 +378,25 @@ def run_gpu(args):
     top_flops = GEMM_FLOPS_PER_SLOT[top] * hi * S
     achieved = top_flops / (avg_ms / 1e3) / 1e12
 
+    # HBM-bound stages: algorithmic bytes per launch / event-timed duration, against the measured
+    # copy bandwidth (routing, dispatch and combine rows; act_grad's row planes and weights)
+    Hb, Ib = 2 * H, 2 * I
+    algo_bytes = {
+        "gather_x": 2 * S * Hb, "gather_dy": 2 * S * Hb,
+        "combine_y": S * Hb + T * Hb + 8 * S, "combine_dx": S * Hb + T * Hb + 4 * S,
+        "act_grad": S * (20 * I + Hb) + E * I * Hb,
+    }
+    hbm_peak = peaks["hbm_gbs"]
+    hbm_stages = {}
+    for k, nbytes_k in algo_bytes.items():
+        ms_k, n_k = stages.get(k, (0.0, 0))
+        if n_k:
+            gbs = nbytes_k / (ms_k / n_k / 1e3) / 1e9
+            hbm_stages[k] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 3),
+                             "bytes_per_launch": int(nbytes_k)}
+    hbm_stages["note"] = ("algorithmic bytes / average launch time, against the measured copy "
+                          "bandwidth; combine_dx runs beside w1_grad on a second stream")
+
     # CPU baseline: the oracle on a bounded sample of this workload
     cpu = (cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 and not I_s
            else None)
@@ -403,7 +433,10 @@ def run_gpu(args):
         "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(T / (bwd_ms / 1e3), 1),
                 "tflops": round(flops["bwd"] / (bwd_ms / 1e3) / 1e12, 2)},
         "first_call_ms": round(first_ms, 3),
+        "step_ms": {"median": round(per_step[len(per_step) // 2], 4), "min": round(per_step[0], 4),
+                    "max": round(per_step[-1], 4)},
         "stages_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
+        "hbm_stages": hbm_stages,
         "roofline": {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
                      "peak_kind": f"bf16 sustained ({peak_src})",

@@ -347,7 +347,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   }
   if (!fuse_combine)
     MM_TRY(timed(ST_COMBINE_Y, st, [&] {
-      return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo);
+      return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo, true);
     }));
   return MM_OK;
 }

@@ -23,7 +23,7 @@ cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, vo
 // plus extra[t] (weight 1) when extra is not null.
 cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
                            void* out, cudaStream_t st, const void* extra = nullptr,
-                           const void* extra_lo = nullptr);
+                           const void* extra_lo = nullptr, bool row_table = false);
 // Identity routing tables of the shared expert's sub-workspace (ws points at its base).
 cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st);
 // d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]].

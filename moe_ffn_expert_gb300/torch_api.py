@@ -136,8 +136,10 @@ class HyperMegaMoEFunction(torch.autograd.Function):
         # with a caller histogram the id and histogram checks are waited for, so that a mismatch
         # raises here instead of leaving y unspecified
         flags = _abi.MM_FLAG_VALIDATE_IDS if tpe is not None else 0
+        if not any(ctx.needs_input_grad):  # inference (no_grad or no input needs a gradient)
+            flags |= _abi.MM_FLAG_FORWARD_ONLY
         y = forward(ws, x, ids, w, wu, wd, flags=flags, shared=shared, tokens_per_expert=tpe)
-        ctx.ws = ws
+        ctx.ws = ws if any(ctx.needs_input_grad) else None
         ctx.wdtype = topk_weights.dtype
         ctx.has_shared = shared is not None
         ctx.save_for_backward(x, ids, w, wu, wd, *(shared or ()))

@@ -202,3 +202,11 @@ def test_forward_only_keeps_y_and_refuses_a_backward():
         assert again["status"] == _abi.MM_OK
         for k in ("y", "dx", "dW_up", "dW_down"):
             assert torch.equal(again[k], ref[k]), k
+
+
+def test_torch_entry_point_under_no_grad_runs_forward_only():
+    from moe_ffn_expert_gb300.torch_api import hyper_mega_moe
+    w, inp = _inputs(seed=53)
+    with torch.no_grad():
+        y = hyper_mega_moe(inp["x"], inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"])
+    assert torch.equal(y, run_layer(inp, backward=False)["y"])
