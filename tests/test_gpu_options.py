@@ -192,10 +192,12 @@ def test_forward_only_keeps_y_and_refuses_a_backward():
     on the same workspace then allows the backward again."""
     w, inp = _inputs(T=500, E=6, seed=47, empty_last=False)
     sh = (synth.shared_up(w, 64, device="cuda"), synth.shared_down(w, 64, device="cuda"))
-    for shared in (None, sh):
+    fo = _abi.MM_FLAG_FORWARD_ONLY
+    for shared, flags in ((None, fo), (sh, fo), (None, fo | _abi.MM_FLAG_FUSED_FORWARD_GEMMS),
+                          (None, fo | _abi.MM_FLAG_FUSED_COMBINE)):
         ref = run_layer(inp, shared=shared)
         assert ref["status"] == _abi.MM_OK
-        out = run_layer(inp, shared=shared, flags=_abi.MM_FLAG_FORWARD_ONLY)
+        out = run_layer(inp, shared=shared, flags=flags)
         assert torch.equal(out["y"], ref["y"])
         assert out["status"] == _abi.MM_ERR_INVALID_ARG
         again = run_layer(inp, shared=shared, ws=out["ws"])

@@ -137,6 +137,8 @@ def _custom(T, H, I, E, K, ids=None, seed=3):
     (130, 256, 128, 2, 1),    # one expert gets 129+ rows: tail tile
     (64, 512, 256, 64, 16),   # K = 16
     (40, 64, 32, 1024, 4),    # E = 1024
+    (1, 8, 8, 16, 16),        # the smallest H and I (one 16-byte row), one token in 16 experts
+    (5, 24, 16, 3, 3),        # H and I below one 64-wide block: every tile is mostly padding
 ])
 def test_edge_shapes(T, H, I, E, K):
     w, inp = _custom(T, H, I, E, K)
