@@ -440,7 +440,12 @@ def run_gpu(args):
         "roofline": {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
                      "peak_kind": f"bf16 sustained ({peak_src})",
-                     "traffic": profiled_traffic(top, w.name)},
+                     "traffic": profiled_traffic(top, w.name),
+                     **({"executed_tflops": round(2 * achieved, 2),
+                         "executed_note": "the weight gradients issue two MMAs per k-step (bf16 hi "
+                                          "and lo planes of the split operand): twice the "
+                                          "algorithmic FLOPs"}
+                        if top in ("w1_grad", "w2_grad") else {})},
         "gpu_launches": launches,
         "e2e": {"value": round(e2e_tokens / (e2e_max / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
