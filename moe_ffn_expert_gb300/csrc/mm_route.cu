@@ -42,16 +42,21 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
   __syncwarp();
   const int s0 = chunk * ROUTE_CHUNK;
   const int s1 = min(S, s0 + ROUTE_CHUNK);
-  for (int base = s0; base < s1; base += 32) {
-    const int s = base + lane;
-    int e = -1;
-    if (s < s1) {
-      e = __ldg(ids + s);
-      if (e < 0 || e >= E) {
-        set_status(hdr + HDR_STATUS, MM_ERR_BAD_EXPERT_ID);
-        atomicCAS(hdr + HDR_BAD_SLOT, 0, s + 1);
-        e = -1;
-      }
+  constexpr int PER_LANE = ROUTE_CHUNK / 32;
+  int ev[PER_LANE];  // all of the chunk's ids in flight at once
+#pragma unroll
+  for (int j = 0; j < PER_LANE; ++j) {
+    const int s = s0 + j * 32 + lane;
+    ev[j] = s < s1 ? __ldg(ids + s) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < PER_LANE; ++j) {
+    const int s = s0 + j * 32 + lane;
+    int e = ev[j];
+    if (s < s1 && (e < 0 || e >= E)) {
+      set_status(hdr + HDR_STATUS, MM_ERR_BAD_EXPERT_ID);
+      atomicCAS(hdr + HDR_BAD_SLOT, 0, s + 1);
+      e = -1;
     }
     const unsigned m = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(m) - 1) cnt[e] += __popc(m);
@@ -60,6 +65,10 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
   for (int i = lane; i < E; i += 32) chunk_cnt[(size_t)chunk * E + i] = cnt[i];
 }
 
+// One CTA of 1024 threads. Each expert gets P = 1024 / E threads (a power of two, 1 to 32, all
+// in one warp), each owning a contiguous range of the chunk histograms: they sum their ranges,
+// the expert totals are scanned across experts (plain and padded to BM rows), and each thread
+// then turns its range into running padded-row bases, so the chunk loop is split P ways.
 __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restrict__ chunk_cnt,
                                                      int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ offsets,
@@ -70,14 +79,34 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks) {
   __shared__ int wsum[32], wsum_p[32];
+  __shared__ int tot_s[1024], po_s[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (hdr[HDR_STATUS] != 0) {  // bad ids: schedule nothing downstream
     if (tid == 0) hdr[HDR_NUM_MTILES] = 0;
     return;
   }
-  int c = 0;
-  if (tid < E)
-    for (int k = 0; k < n_chunks; ++k) c += chunk_cnt[(size_t)k * E + tid];
+  int P = 1;  // threads per expert
+  while (P < 32 && P * 2 * E <= 1024) P *= 2;
+  const int e = tid / P, j = tid - (tid / P) * P;
+  const bool active = e < E;
+  const int L = (n_chunks + P - 1) / P;  // chunks per thread
+  const int k0 = min(n_chunks, j * L), k1 = min(n_chunks, k0 + L);
+  int seg = 0;
+  if (active)
+    for (int k = k0; k < k1; ++k) seg += chunk_cnt[(size_t)k * E + e];
+  // inclusive scan of seg within the expert's group of P lanes (P divides 32)
+  int incl = seg;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (d < P && j >= d) incl += y;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, (lane / P) * P + P - 1);
+  if (active && j == 0) tot_s[e] = total;
+  __syncthreads();
+
+  // scan of the expert totals (plain and padded), one thread per expert
+  const int c = tid < E ? tot_s[tid] : 0;
   // a caller's histogram is only compared, never used for addressing
   if (tpe != nullptr && tid < E && __ldg(tpe + tid) != c)
     set_status(hdr + HDR_STATUS, MM_ERR_TOKENS_PER_EXPERT);
@@ -114,25 +143,33 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
     wsum_p[lane] = v - v0;
   }
   __syncthreads();
-  if (tid >= E) return;
-  const int off = a - c + wsum[warp];
-  const int po = b - pc + wsum_p[warp];
-  counts[tid] = c;
-  offsets[tid] = off;
-  poff[tid] = po;
-  if (tid == E - 1) {
-    offsets[E] = off + c;
-    poff[E] = po + pc;
-    hdr[HDR_NUM_MTILES] = (po + pc) / BM;
+  if (tid < E) {
+    const int off = a - c + wsum[warp];
+    const int po = b - pc + wsum_p[warp];
+    counts[tid] = c;
+    offsets[tid] = off;
+    poff[tid] = po;
+    po_s[tid] = po;
+    if (tid == E - 1) {
+      offsets[E] = off + c;
+      poff[E] = po + pc;
+      hdr[HDR_NUM_MTILES] = (po + pc) / BM;
+    }
   }
-  int run = po;  // chunk histograms -> running padded-row base of each chunk
-  for (int k = 0; k < n_chunks; ++k) {
-    const int v = chunk_cnt[(size_t)k * E + tid];
-    chunk_cnt[(size_t)k * E + tid] = run;
+  __syncthreads();
+  if (!active) return;
+  // chunk histograms -> running padded-row base of each chunk (this thread's range)
+  const int po = po_s[e];
+  int run = po + incl - seg;
+  for (int k = k0; k < k1; ++k) {
+    const int v = chunk_cnt[(size_t)k * E + e];
+    chunk_cnt[(size_t)k * E + e] = run;
     run += v;
   }
-  for (int t = po / BM; t < (po + pc) / BM; ++t) tile_expert[t] = tid;
-  for (int r = po + c; r < po + pc; ++r) {
+  // the expert's row tiles and pad-row markers, split over its P threads
+  const int pcount = (total + BM - 1) / BM * BM;
+  for (int t = po / BM + j; t < (po + pcount) / BM; t += P) tile_expert[t] = e;
+  for (int r = po + total + j; r < po + pcount; r += P) {
     slot_of_row[r] = -1;
     w_row[r] = 0.0f;
   }
@@ -157,9 +194,19 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
   const unsigned lt = (1u << lane) - 1u;
   const int s0 = chunk * ROUTE_CHUNK;
   const int s1 = min(S, s0 + ROUTE_CHUNK);
-  for (int base = s0; base < s1; base += 32) {
-    const int s = base + lane;
-    const int e = s < s1 ? __ldg(ids + s) : -1;
+  constexpr int PER_LANE = ROUTE_CHUNK / 32;
+  int ev[PER_LANE];
+  float wv[PER_LANE];
+#pragma unroll
+  for (int j = 0; j < PER_LANE; ++j) {
+    const int s = s0 + j * 32 + lane;
+    ev[j] = s < s1 ? __ldg(ids + s) : -1;
+    wv[j] = s < s1 ? __ldg(topk_w + s) : 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < PER_LANE; ++j) {
+    const int s = s0 + j * 32 + lane;
+    const int e = ev[j];
     const unsigned m = __match_any_sync(0xffffffffu, e);
     int row = 0;
     if (e >= 0) row = cnt[e] + __popc(m & lt);
@@ -169,7 +216,7 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
     if (e >= 0) {
       row_of_slot[s] = row;
       slot_of_row[row] = s;
-      w_row[row] = __ldg(topk_w + s);
+      w_row[row] = wv[j];
     }
   }
 }
