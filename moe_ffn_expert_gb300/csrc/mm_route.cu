@@ -92,8 +92,10 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   const int L = (n_chunks + P - 1) / P;  // chunks per thread
   const int k0 = min(n_chunks, j * L), k1 = min(n_chunks, k0 + L);
   int seg = 0;
-  if (active)
+  if (active) {
+#pragma unroll 8
     for (int k = k0; k < k1; ++k) seg += chunk_cnt[(size_t)k * E + e];
+  }
   // inclusive scan of seg within the expert's group of P lanes (P divides 32)
   int incl = seg;
 #pragma unroll
@@ -161,7 +163,18 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   // chunk histograms -> running padded-row base of each chunk (this thread's range)
   const int po = po_s[e];
   int run = po + incl - seg;
-  for (int k = k0; k < k1; ++k) {
+  int k = k0;
+  for (; k + 8 <= k1; k += 8) {  // eight loads in flight, then the running sums
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = chunk_cnt[(size_t)(k + i) * E + e];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      chunk_cnt[(size_t)(k + i) * E + e] = run;
+      run += v[i];
+    }
+  }
+  for (; k < k1; ++k) {
     const int v = chunk_cnt[(size_t)k * E + e];
     chunk_cnt[(size_t)k * E + e] = run;
     run += v;
