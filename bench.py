@@ -232,7 +232,8 @@ def run_gpu(args):
     def bwd(bf=bufs0):
         args_b = (bf["dy"].data_ptr(), bf["x"].data_ptr(), bf["ids"].data_ptr(),
                   bf["tw"].data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(), nbytes,
-                  bf["dx"].data_ptr(), bf["dtk"].data_ptr(), du.data_ptr(), dd.data_ptr(), st, 0)
+                  bf["dx"].data_ptr(), bf["dtk"].data_ptr(), du.data_ptr(), dd.data_ptr(), st,
+                  args.bwd_flags)
         if I_s:
             _abi.check(_abi.mm_backward_ex(d, opt, *args_b), "bwd")
         else:
@@ -419,6 +420,7 @@ def run_gpu(args):
                    "E": E, "K": K, "routing": w.routing, "seed": w.seed,
                    **({"shared_I": I_s} if I_s else {}),
                    **({"forward_flags": hex(args.fwd_flags)} if args.fwd_flags else {}),
+                   **({"backward_flags": hex(args.bwd_flags)} if args.bwd_flags else {}),
                    "l2": "inputs larger than L2: 1.2 GB of expert weights and 0.6 GB of slot rows per step",
                    "parallelism": "single GPU" if world == 1 else f"{world} independent replicas"},
         "tflops": round(tflops, 2),
@@ -564,6 +566,8 @@ def main(argv=None):
     ap.add_argument("--fwd-flags", type=lambda v: int(v, 0), default=0,
                     help="mm_forward flags, e.g. 0x8 (one-launch forward GEMMs), 0x10 (combine in "
                          "GEMM2's epilogue)")
+    ap.add_argument("--bwd-flags", type=lambda v: int(v, 0), default=0,
+                    help="mm_backward flags, e.g. 0x40 (paired row tiles for input_grad)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--shared-intermediate", type=int, default=0,
                     help="add a shared expert of this intermediate size (0: none)")

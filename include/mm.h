@@ -101,6 +101,12 @@ typedef struct mm_dims {
  * MM_ERR_INVALID_ARG in the status word and its GEMMs do nothing (outputs unspecified). */
 #define MM_FLAG_FORWARD_ONLY 0x20u
 
+/* mm_forward / mm_backward flag: run GEMM1, GEMM2 (forward) and input_grad (backward) in clusters
+ * of two CTAs that take two row tiles of the same expert and share its weight tile, each CTA
+ * loading half of it into both CTAs' shared memory (TMA multicast). Results are identical bit for
+ * bit. */
+#define MM_FLAG_PAIRED_TILES 0x40u
+
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one
  * accumulator hand-off (first tile of its first CTA) and every device wait of the call is bounded
  * by 50 ms instead of 2 s. The call then ends with MM_ERR_TIMEOUT in the status word (and y is

@@ -184,6 +184,7 @@ bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows) {
   p.off_tile_expert = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
   p.off_ready = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
   p.off_cnt = take((size_t)d.T * ((d.H + 127) / 128) * sizeof(int32_t));
+  p.off_pair_tile = take((size_t)(p.S_pad / BM) * sizeof(int32_t));
   p.off_row_of_slot = take((size_t)p.S * sizeof(int32_t));
   p.off_slot_of_row = take((size_t)p.S_pad * sizeof(int32_t));
   p.off_w_row = take((size_t)p.S_pad * sizeof(float));
@@ -303,6 +304,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
              stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
+  c.paired = (flags & MM_FLAG_PAIRED_TILES) ? 1 : 0;
   if (flags & MM_FLAG_FORWARD_ONLY) {  // no gate|up kept; a backward from here is refused
     c.skip_gu = 1;
     MM_TRY(cudaMemsetAsync(ws + w.off_hdr + HDR_NO_BACKWARD * sizeof(int32_t), 1,
@@ -395,7 +397,9 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   c.kind = GK_INPUT_GRAD;
   c.d_w = nullptr;
   c.accumulate = 0;
+  c.paired = (flags & MM_FLAG_PAIRED_TILES) ? 1 : 0;
   MM_TRY(timed(ST_INPUT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  c.paired = 0;
   const void* extra = nullptr;
   const void* extra_lo = nullptr;
   char* wss = ws + p.base_s;

@@ -72,7 +72,8 @@ struct alignas(128) EpiMaps {
 static_assert(offsetof(EpiMaps, out_lo) == offsetof(EpiMaps, out) + sizeof(CUtensorMap),
               "the split output's lo map follows its hi map");
 
-constexpr int OUT_TILE_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16 of staged output (64-byte rows)
+constexpr int OUT_TILE_BYTES = 32 * 32 * 2;
+constexpr int B_HALF_ROWS = BN / 2;  // paired INPUT_GRAD: rows of B each CTA of a pair loads  // 32 rows x 32 bf16 of staged output (64-byte rows)
 static_assert(BK == 64, "one 128-byte swizzle row per k-block");
 
 struct Args {
@@ -120,6 +121,7 @@ struct Args {
   __nv_bfloat16* comb_y;          // [T][H]
   int comb_K, comb_H, comb_nch;
   int skip_gu;  // GEMM1: forward only, gate|up are not stored
+  const int32_t* pair_tile;  // paired launches: first row tile of each pair (~tile: no second)
 };
 
 template <int KIND>
@@ -689,12 +691,38 @@ __device__ __forceinline__ void fused_combine_warp(const Args& a, const Tile& t,
   }
 }
 
+// Paired launches (row-grouped GEMM1, GEMM2, INPUT_GRAD): clusters of two CTAs take two row
+// tiles of the same expert and the same column tile, so their B tiles (the expert's weights)
+// are the same: each CTA loads half of B multicast to both, halving the weight traffic into
+// shared memory. A stage is refilled only after both CTAs' MMAs have released it (each MMA
+// commit arrives on both CTAs' empty barriers). When an expert has an odd number of row tiles
+// its last pair's second tile is not the expert's: that CTA runs the MMAs (its A rows are other
+// rows of the buffer or zero-filled past it) and stores nothing.
 template <int KIND>
+__device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
+  const int p = unit / a.n_tiles_n;
+  const int nt = unit - p * a.n_tiles_n;
+  const int pt = __ldg(a.pair_tile + p);
+  const int mt0 = pt >= 0 ? pt : ~pt;
+  valid = rank == 0 || pt >= 0;
+  Tile t;
+  t.part = 0;
+  t.e = __ldg(a.tile_expert + mt0);
+  t.m0 = (mt0 + (int)rank) * BM;
+  t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
+  t.row0 = t.m0;
+  t.kiters = a.k_iters;
+  return t;
+}
+
+template <int KIND, bool PAIRED = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmL, const __grid_constant__ EpiMaps em,
            const Args a) {
   using TR = Traits<KIND>;
+  static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD,
+                "paired launches: row-grouped GEMM1, GEMM2 and INPUT_GRAD"); 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform); the status
   // word is the call's (the shared expert's launches point at the routed layout's word too)
@@ -722,14 +750,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = TR::WGRAD   ? a.E * a.m_tiles_w * a.n_tiles_n
+  const int total = PAIRED      ? a.hdr[HDR_NUM_MPAIRS] * a.n_tiles_n
+                    : TR::WGRAD ? a.E * a.m_tiles_w * a.n_tiles_n
                     : TR::FUSED ? a.hdr[HDR_NUM_MTILES] * (a.n_tiles_n + a.n2)
                                 : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
+  // work units of this CTA: tile (or pair) first, first + step, ...
+  const uint32_t rank = PAIRED ? cluster_ctarank() : 0u;
+  const int first = PAIRED ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int step = PAIRED ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto tile_at = [&](int unit, bool& valid) -> Tile {
+    if constexpr (PAIRED) {
+      return decode_pair<KIND>(a, unit, rank, valid);
+    } else {
+      valid = true;
+      return decode_tile<KIND>(a, unit);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), PAIRED ? 2 : 1);  // paired: both CTAs' MMAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -760,6 +801,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // paired: both CTAs' barriers are initialised before either multicasts into the other
+  if constexpr (PAIRED) cluster_sync();
   const uint32_t tmem_base = *tmem_holder_ptr;
   const uint64_t tmo = a.timeout_ns;
 
@@ -767,8 +810,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile<KIND>(a, tile);
+      for (int tile = first; tile < total && ok; tile += step) {
+        bool tile_ok;
+        const Tile t = tile_at(tile, tile_ok);
+        (void)tile_ok;
         if constexpr (TR::FUSED) {
           // a GEMM2 tile waits until every GEMM1 tile of its row block has stored its h rows
           // (each of their epilogue warps counts once), then orders those generic-proxy writes
@@ -805,7 +850,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tma_load_2d(sa, &tmA, full_bar(s), k0, t.m0);
           }
-          if constexpr (TR::FUSED) {
+          if constexpr (PAIRED) {
+            // this CTA's half of the shared B tile, multicast to both CTAs of the pair
+            constexpr uint16_t kBoth = 0x3;
+            if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
+              const int c0 = (rank ? a.I : 0) + t.n0;
+              tma_load_3d_mc(sb + (2 * rank + 0) * MN_BLOCK_BYTES, &tmB, full_bar(s), c0, k0, t.e,
+                             kBoth);
+              tma_load_3d_mc(sb + (2 * rank + 1) * MN_BLOCK_BYTES, &tmB, full_bar(s), c0 + 64, k0,
+                             t.e, kBoth);
+            } else if constexpr (KIND == GK_GEMM2) {  // rank r: column blocks 2r and 2r + 1
+#pragma unroll
+              for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
+                tma_load_3d_mc(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, k0, t.e,
+                               kBoth);
+            } else {  // INPUT_GRAD, K-major B of 256 rows: rank r loads rows 128r..128r+127
+              tma_load_3d_mc(sb + rank * (B_HALF_ROWS * 128), &tmB, full_bar(s), k0,
+                             t.n0 + B_HALF_ROWS * (int)rank, t.e, kBoth);
+            }
+          } else if constexpr (TR::FUSED) {
             if (t.part == 0) {
               tma_load_3d(sb + 0 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0, k0, t.e);
               tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
@@ -834,13 +897,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      if constexpr (PAIRED) {
+        // both CTAs' releases of every stage's last use have landed on this CTA's barriers
+        // before it may leave (the peer's MMA commits arrive here asynchronously)
+        for (int s = 0; s < STAGES && ok; ++s) {
+          if (it <= (uint32_t)s) break;
+          const uint32_t last = (it - 1 - s) / STAGES;  // index of stage s's last use
+          if (!mbar_wait(empty_bar(s), last & 1u, tmo)) set_status(a.status, MM_ERR_TIMEOUT);
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile<KIND>(a, tile);
+      for (int tile = first; tile < total && ok; tile += step) {
+        bool tile_ok;
+        const Tile t = tile_at(tile, tile_ok);
+        (void)tile_ok;
         if (t.kiters == 0) continue;
         const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), aph ^ 1u, tmo)) {
@@ -871,7 +945,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (TR::A_SPLIT)
               umma_bf16(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, TR::IDESC, 1u);
           }
-          umma_commit(empty_bar(s));
+          if constexpr (PAIRED)
+            umma_commit_mc(empty_bar(s), 0x3);  // both CTAs' producers wait on this stage
+          else
+            umma_commit(empty_bar(s));
         }
         if (!ok) break;
         // (test hook: CTA 0 withholds its first hand-off, so its epilogue's wait runs out)
@@ -892,8 +969,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sbuf = epi_base + (warp - 2) * 2 * OUT_TILE_BYTES;  // output staging
     uint32_t chunk_no = 0;
     uint32_t acc_it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode_tile<KIND>(a, tile);
+    for (int tile = first; tile < total; tile += step) {
+      bool tile_ok;
+      const Tile t = tile_at(tile, tile_ok);
       if (t.kiters == 0) {
         if constexpr (TR::WGRAD) {
           if (!a.accumulate)  // adding zero changes nothing
@@ -913,6 +991,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
+      if (!tile_ok) {  // a pair's second tile outside the expert: nothing to store
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+        ++acc_it;
+        continue;
+      }
       if constexpr (TR::FUSED) {
         if (t.part == 0) {
           // the staging buffer may still be read by this warp's TMA stores of a GEMM2 tile
@@ -957,6 +1042,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // paired: the peer may still commit onto this CTA's barriers until it is done too
+  if constexpr (PAIRED) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -1038,7 +1125,7 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KIND>
+template <int KIND, bool PAIRED>
 cudaError_t set_smem_attr() {
   static uint64_t done_mask = 0;
   int dev = 0;
@@ -1046,7 +1133,7 @@ cudaError_t set_smem_attr() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(k_gemm<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(k_gemm<KIND, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)Traits<KIND>::SMEM);
   if (e == cudaSuccess) done_mask |= bit;
   return e;
@@ -1054,9 +1141,9 @@ cudaError_t set_smem_attr() {
 
 inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-template <int KIND>
+template <int KIND, bool PAIRED = false>
 cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
-  cudaError_t err = set_smem_attr<KIND>();
+  cudaError_t err = set_smem_attr<KIND, PAIRED>();
   if (err != cudaSuccess) return err;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorNoDevice;
@@ -1187,9 +1274,9 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
     }
-    case GK_INPUT_GRAD:
+    case GK_INPUT_GRAD:  // paired: each CTA loads half of B's rows
       ok = map_rows(&ta, ws + w.off_dgu, 2 * I, S_pad, 64, BM) &&
-           map_experts(&tb, c.w_up, 2 * I, H, E, 64, BN);
+           map_experts(&tb, c.w_up, 2 * I, H, E, 64, PAIRED ? B_HALF_ROWS : BN);
       a.n_tiles_n = cdiv(H, BN);
       a.k_iters = cdiv(2 * I, BK);
       a.N = (int)H;
@@ -1269,20 +1356,50 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   } else {
     em.out = em.out_lo = ta;  // unused but initialised
   }
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
-  k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
-  return cudaGetLastError();
+  if constexpr (PAIRED) {
+    // clusters of two CTAs over pairs of row tiles: as many clusters as fit at once (a
+    // persistent grid must not wait for SMs), at most one per pair-column unit
+    a.pair_tile = reinterpret_cast<const int32_t*>(ws + w.off_pair_tile);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Traits<KIND>::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(nsm & ~1));
+    int max_clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm<KIND, true>, &cfg);
+    if (err != cudaSuccess) return err;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int64_t units = (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
+    const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, k_gemm<KIND, true>, ta, tb, tl, em, a);
+  } else {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
+    k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
+  const bool paired = c.paired && c.rows == nullptr;  // expert-sorted rows only
   switch (c.kind) {
-    case GK_GEMM1_SWIGLU: return run<GK_GEMM1_SWIGLU>(w, ws, c, st);
-    case GK_GEMM2: return run<GK_GEMM2>(w, ws, c, st);
+    case GK_GEMM1_SWIGLU:
+      return paired ? run<GK_GEMM1_SWIGLU, true>(w, ws, c, st) : run<GK_GEMM1_SWIGLU>(w, ws, c, st);
+    case GK_GEMM2:
+      return paired ? run<GK_GEMM2, true>(w, ws, c, st) : run<GK_GEMM2>(w, ws, c, st);
     case GK_GEMM2_COMBINE: return run<GK_GEMM2_COMBINE>(w, ws, c, st);
     case GK_ACT_GRAD: return run<GK_ACT_GRAD>(w, ws, c, st);
-    case GK_INPUT_GRAD: return run<GK_INPUT_GRAD>(w, ws, c, st);
+    case GK_INPUT_GRAD:
+      return paired ? run<GK_INPUT_GRAD, true>(w, ws, c, st) : run<GK_INPUT_GRAD>(w, ws, c, st);
     case GK_W2_GRAD: return run<GK_W2_GRAD>(w, ws, c, st);
     case GK_W1_GRAD: return run<GK_W1_GRAD>(w, ws, c, st);
     case GK_FWD_FUSED: return run<GK_FWD_FUSED>(w, ws, c, st);

@@ -59,6 +59,8 @@ struct GemmCall {
   // GEMM2 / fused forward: when comb_y is set, the weighted combine into comb_y runs in the
   // epilogue (the per-(token, 128-column chunk) counters at off_cnt must be zero)
   int skip_gu = 0;     // GEMM1 / fused forward: do not store gate|up (forward only)
+  int paired = 0;      // GEMM1 / GEMM2 / INPUT_GRAD on expert-sorted rows: clusters of two CTAs
+                       // sharing the weight tile of two row tiles (multicast loads)
   void* comb_y = nullptr;
   const float* comb_w = nullptr;
   const void* comb_extra = nullptr;

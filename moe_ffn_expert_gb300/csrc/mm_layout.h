@@ -24,6 +24,7 @@ enum HeaderWord {
   HDR_NUM_MTILES = 1,  // number of BM-row tiles over all experts (padded rows / BM)
   HDR_BAD_SLOT = 2,    // first slot seen with an invalid expert id (diagnostics)
   HDR_NO_BACKWARD = 3, // nonzero: the forward kept no gate|up (MM_FLAG_FORWARD_ONLY)
+  HDR_NUM_MPAIRS = 4,  // pairs of row tiles of one expert (the paired GEMMs' work units)
   HDR_WORDS = 64
 };
 
@@ -58,6 +59,8 @@ struct Workspace {
   size_t off_hdr, off_counts, off_offsets, off_poff, off_chunk, off_tile_expert;
   size_t off_ready;  // int32 [S_pad / BM] fused forward: GEMM1 epilogue warps done per row tile
   size_t off_cnt;    // int32 [T][ceil(H / 128)] fused combine: slots stored per token and chunk
+  size_t off_pair_tile;  // int32 [S_pad / BM] first row tile of each pair; ~tile if the pair's
+                         // second tile belongs to another expert
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
   size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
   size_t off_gu;       // fp32 [S_pad, 2I]  gate|up accumulators (kept for the backward)

@@ -76,10 +76,11 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      int32_t* __restrict__ tile_expert,
                                                      int32_t* __restrict__ slot_of_row,
                                                      float* __restrict__ w_row,
+                                                     int32_t* __restrict__ pair_tile,
                                                      const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks) {
-  __shared__ int wsum[32], wsum_p[32];
-  __shared__ int tot_s[1024], po_s[1024];
+  __shared__ int wsum[32], wsum_p[32], wsum_q[32];
+  __shared__ int tot_s[1024], po_s[1024], qo_s[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (hdr[HDR_STATUS] != 0) {  // bad ids: schedule nothing downstream
     if (tid == 0) hdr[HDR_NUM_MTILES] = 0;
@@ -113,49 +114,60 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   if (tpe != nullptr && tid < E && __ldg(tpe + tid) != c)
     set_status(hdr + HDR_STATUS, MM_ERR_TOKENS_PER_EXPERT);
   const int pc = (c + BM - 1) / BM * BM;
-  int a = c, b = pc;  // inclusive warp scans
+  const int pq = (pc / BM + 1) / 2;  // pairs of row tiles
+  int a = c, b = pc, q = pq;  // inclusive warp scans
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const int ya = __shfl_up_sync(0xffffffffu, a, d);
     const int yb = __shfl_up_sync(0xffffffffu, b, d);
+    const int yq = __shfl_up_sync(0xffffffffu, q, d);
     if (lane >= d) {
       a += ya;
       b += yb;
+      q += yq;
     }
   }
   if (lane == 31) {
     wsum[warp] = a;
     wsum_p[warp] = b;
+    wsum_q[warp] = q;
   }
   __syncthreads();
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
     int u = lane < nw ? wsum[lane] : 0, v = lane < nw ? wsum_p[lane] : 0;
-    const int u0 = u, v0 = v;
+    int z = lane < nw ? wsum_q[lane] : 0;
+    const int u0 = u, v0 = v, z0 = z;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int yu = __shfl_up_sync(0xffffffffu, u, d);
       const int yv = __shfl_up_sync(0xffffffffu, v, d);
+      const int yz = __shfl_up_sync(0xffffffffu, z, d);
       if (lane >= d) {
         u += yu;
         v += yv;
+        z += yz;
       }
     }
     wsum[lane] = u - u0;  // exclusive prefix of warp totals
     wsum_p[lane] = v - v0;
+    wsum_q[lane] = z - z0;
   }
   __syncthreads();
   if (tid < E) {
     const int off = a - c + wsum[warp];
     const int po = b - pc + wsum_p[warp];
+    const int qo = q - pq + wsum_q[warp];
     counts[tid] = c;
     offsets[tid] = off;
     poff[tid] = po;
     po_s[tid] = po;
+    qo_s[tid] = qo;
     if (tid == E - 1) {
       offsets[E] = off + c;
       poff[E] = po + pc;
       hdr[HDR_NUM_MTILES] = (po + pc) / BM;
+      hdr[HDR_NUM_MPAIRS] = qo + pq;
     }
   }
   __syncthreads();
@@ -179,9 +191,14 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
     chunk_cnt[(size_t)k * E + e] = run;
     run += v;
   }
-  // the expert's row tiles and pad-row markers, split over its P threads
+  // the expert's row tiles, row-tile pairs and pad-row markers, split over its P threads
   const int pcount = (total + BM - 1) / BM * BM;
   for (int t = po / BM + j; t < (po + pcount) / BM; t += P) tile_expert[t] = e;
+  const int ntile = pcount / BM, qo = qo_s[e];
+  for (int i = j; i < (ntile + 1) / 2; i += P) {
+    const int t0 = po / BM + 2 * i;
+    pair_tile[qo + i] = 2 * i + 1 < ntile ? t0 : ~t0;
+  }
   for (int r = po + total + j; r < po + pcount; r += P) {
     slot_of_row[r] = -1;
     w_row[r] = 0.0f;
@@ -413,8 +430,8 @@ cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* token
       region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
       region<int32_t>(ws, w.off_counts), region<int32_t>(ws, w.off_offsets),
       region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_tile_expert),
-      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row), tokens_per_expert,
-      (int)w.E, (int)w.n_chunks);
+      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
+      region<int32_t>(ws, w.off_pair_tile), tokens_per_expert, (int)w.E, (int)w.n_chunks);
   return cudaGetLastError();
 }
 

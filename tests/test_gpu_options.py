@@ -212,3 +212,30 @@ def test_torch_entry_point_under_no_grad_runs_forward_only():
     with torch.no_grad():
         y = hyper_mega_moe(inp["x"], inp["topk_ids"], inp["topk_weights"], inp["w_up"], inp["w_down"])
     assert torch.equal(y, run_layer(inp, backward=False)["y"])
+
+
+@pytest.mark.parametrize("T,H,I,E,K", [(1, 64, 64, 1, 1),       # one row tile: its pair's second is empty
+                                       (1000, 136, 72, 7, 3),   # ragged H and I, odd tile counts
+                                       (3000, 512, 256, 16, 4),
+                                       (300, 256, 128, 40, 2)])  # many experts with one tile
+def test_paired_tiles_equal_single_tiles(T, H, I, E, K):
+    """MM_FLAG_PAIRED_TILES (clusters of two CTAs sharing the weight tile of two row tiles of one
+    expert, multicast loads) gives outputs identical bit for bit to the one-CTA launches."""
+    w = synth.small("pair", T, H, I, E, K, seed=T + 7)
+    inp = make_inputs(w)
+    ref = run_layer(inp)
+    pt = _abi.MM_FLAG_PAIRED_TILES
+    out = run_layer(inp, flags=pt, bwd_flags=pt)
+    assert out["status"] == _abi.MM_OK
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+        assert torch.equal(out[k], ref[k]), k
+
+
+def test_paired_tiles_on_the_skew_workload():
+    w = synth.BY_NAME["skew"]
+    inp = make_inputs(w)
+    ref = run_layer(inp)
+    pt = _abi.MM_FLAG_PAIRED_TILES
+    out = run_layer(inp, flags=pt, bwd_flags=pt)
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
+        assert torch.equal(out[k], ref[k]), k
