@@ -238,6 +238,9 @@ int mm_abi_version(void);
  * clears them, and returns the number of stages (MM_NUM_STAGES). mm_stage_name names a stage. */
 #define MM_NUM_STAGES 16
 mm_status mm_timing_enable(int on);
+/* Restricts the timer to the stages whose bit (1 << stage) is set in stage_mask (default: all),
+ * so that a timed run can bracket only the kernel it reports on. */
+mm_status mm_timing_select(uint32_t stage_mask);
 int mm_timing_read(double* ms, int64_t* launches, int max_stages);
 const char* mm_stage_name(int stage);
 

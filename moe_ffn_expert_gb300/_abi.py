@@ -91,6 +91,7 @@ def _lib():
         "mm_abi_version": (ctypes.c_int, []),
         "mm_last_error_detail": (ctypes.c_char_p, []),
         "mm_timing_enable": (st, [ctypes.c_int]),
+        "mm_timing_select": (st, [ctypes.c_uint32]),
         "mm_timing_read": (ctypes.c_int, [_P, _P, ctypes.c_int]),
         "mm_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -183,6 +184,17 @@ def mm_abi_version() -> int:
 
 def mm_timing_enable(on: bool) -> int:
     return int(_lib().mm_timing_enable(1 if on else 0))
+
+
+def mm_timing_select(stage_mask: int) -> int:
+    return int(_lib().mm_timing_select(stage_mask & 0xFFFFFFFF))
+
+
+def stage_index(name: str) -> int:
+    for i in range(MM_NUM_STAGES):
+        if _lib().mm_stage_name(i).decode() == name:
+            return i
+    raise KeyError(name)
 
 
 def mm_timing_read() -> dict:

@@ -50,6 +50,7 @@ struct TimerRecord {
 };
 struct Timer {
   bool on = false;
+  uint32_t mask = 0xFFFFFFFFu;  // stages that are bracketed while on
   std::vector<TimerRecord> pending;
   std::vector<cudaEvent_t> pool;
   cudaEvent_t get() {
@@ -67,7 +68,7 @@ Timer g_timer;
 
 template <typename F>
 cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
-  if (!g_timer.on) return launch();
+  if (!g_timer.on || !((g_timer.mask >> stage) & 1u)) return launch();
   cudaEvent_t a = g_timer.get(), b = g_timer.get();
   if (a) cudaEventRecord(a, st);
   cudaError_t e = launch();
@@ -530,6 +531,11 @@ mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts, i
 
 mm_status mm_timing_enable(int on) {
   g_timer.on = on != 0;
+  return MM_OK;
+}
+
+mm_status mm_timing_select(uint32_t stage_mask) {
+  g_timer.mask = stage_mask;
   return MM_OK;
 }
 
