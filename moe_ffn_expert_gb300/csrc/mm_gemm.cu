@@ -80,6 +80,7 @@ struct Args {
   const int* hdr;
   const int32_t* tile_expert;
   const int32_t* poff;
+  const int32_t* counts;  // weight-gradient kinds: rows of each expert (without padding)
   int* status;
   int n_tiles_n;   // column tiles
   int k_iters;     // row-grouped kinds: reduction blocks of BK
@@ -169,6 +170,7 @@ struct Traits {
 
 struct Tile {
   int e, m0, n0, kiters, row0;
+  int klast;  // 16-deep MMA steps issued for the last reduction block (BK / 16 unless trimmed)
   int part;  // fused forward: 0 = GEMM1 + SwiGLU tile, 1 = GEMM2 tile
 };
 
@@ -176,6 +178,7 @@ template <int KIND>
 __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   Tile t;
   t.part = 0;
+  t.klast = BK / 16;
   if constexpr (Traits<KIND>::FUSED) {
     // Order: GEMM1 tiles of row-tile window 0, then for each later window w its GEMM1 tiles
     // followed by window w-1's GEMM2 tiles, then the last window's GEMM2 tiles. Every GEMM2
@@ -232,7 +235,11 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
     t.m0 = mt * BM;
     t.n0 = nt * Traits<KIND>::TN;
     t.row0 = __ldg(a.poff + t.e);
-    t.kiters = (__ldg(a.poff + t.e + 1) - t.row0) / BK;
+    // the reduction runs over the expert's rows only: whole blocks of BK rows, then as many
+    // 16-row MMA steps as the last block needs (its pad rows are zero and add nothing)
+    const int rows = __ldg(a.counts + t.e);
+    t.kiters = (rows + BK - 1) / BK;
+    if (t.kiters > 0) t.klast = (rows - (t.kiters - 1) * BK + 15) / 16;
   } else {
     const int mt = tile / a.n_tiles_n;
     const int nt = tile - mt * a.n_tiles_n;
@@ -707,6 +714,7 @@ __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t ra
   valid = rank == 0 || pt >= 0;
   Tile t;
   t.part = 0;
+  t.klast = BK / 16;
   t.e = __ldg(a.tile_expert + mt0);
   t.m0 = (mt0 + (int)rank) * BM;
   t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
@@ -932,8 +940,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + TR::B_OFF;
+          const int nk = kb == t.kiters - 1 ? t.klast : BK / 16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nk) break;
             // k-step offsets: 16 elements = 32 B along a K-major row, 16 k-rows = 2 KB MN-major
             const uint32_t ka = TR::A_MN ? kk * 2048 : kk * 32;
             const uint32_t kbo = TR::B_MN ? kk * 2048 : kk * 32;
@@ -1160,6 +1170,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   const int64_t nrows = c.rows ? w.T : S_pad;
   a.tile_expert = reinterpret_cast<const int32_t*>(ws + w.off_tile_expert);
   a.poff = reinterpret_cast<const int32_t*>(ws + w.off_poff);
+  a.counts = reinterpret_cast<const int32_t*>(ws + w.off_counts);
   a.E = (int)E;
   a.I = (int)I;
   a.S_pad = S_pad;
