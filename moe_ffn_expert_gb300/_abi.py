@@ -30,6 +30,7 @@ MM_FLAG_FUSED_FORWARD_GEMMS = 0x8
 MM_FLAG_FUSED_COMBINE = 0x10
 MM_FLAG_FORWARD_ONLY = 0x20
 MM_FLAG_PAIRED_TILES = 0x40
+MM_FLAG_SINGLE_CTA_TILES = 0x100
 MM_NUM_STAGES = 16
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",

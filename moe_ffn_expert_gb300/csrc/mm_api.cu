@@ -266,6 +266,12 @@ static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, cons
   return MM_OK;
 }
 
+// CTA-pair form of the row-grouped GEMMs: 0 one CTA per tile, 1 pairs sharing the weight tile by
+// multicast loads, 2 (default) pairs sharing one M = 256 MMA.
+static int pair_mode(uint32_t flags) {
+  return (flags & MM_FLAG_SINGLE_CTA_TILES) ? 0 : (flags & MM_FLAG_PAIRED_TILES) ? 1 : 2;
+}
+
 static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32_t* tpe,
                               const void* x,
                               const int32_t* topk_ids, const float* topk_weights,
@@ -305,7 +311,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   const bool stall = (flags & MM_FLAG_TEST_STALL) != 0;
   GemmCall c{GK_GEMM1_SWIGLU, up_proj_weight, down_proj_weight, nullptr,
              stall ? kTestTimeoutNs : kDefaultTimeoutNs, stall ? 1 : 0, 0, nullptr, nullptr};
-  c.paired = (flags & MM_FLAG_PAIRED_TILES) ? 1 : 0;
+  c.paired = pair_mode(flags);
   if (flags & MM_FLAG_FORWARD_ONLY) {  // no gate|up kept; a backward from here is refused
     c.skip_gu = 1;
     MM_TRY(cudaMemsetAsync(ws + w.off_hdr + HDR_NO_BACKWARD * sizeof(int32_t), 1,
@@ -389,16 +395,22 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
              nullptr, nullptr};
   const int accumulate = (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) ? 1 : 0;
   c.wgrad_f32 = (flags & MM_FLAG_FP32_WEIGHT_GRADS) ? 1 : 0;
+  // CTA pairs: input_grad in either form; the weight gradients as pair MMAs only, and only when
+  // the experts average 512 rows or more (on short reductions the pair's lockstep costs more
+  // than its halved operand traffic saves)
+  const int pair = pair_mode(flags);
+  const int wgrad_pair = (pair == 2 && w.S >= 512 * w.E) ? 2 : 0;
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;
   c.d_w = d_down_proj_weight;
   c.accumulate = accumulate;
+  c.paired = wgrad_pair;
   MM_TRY(timed(ST_W2_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.kind = GK_INPUT_GRAD;
   c.d_w = nullptr;
   c.accumulate = 0;
-  c.paired = (flags & MM_FLAG_PAIRED_TILES) ? 1 : 0;
+  c.paired = pair;
   MM_TRY(timed(ST_INPUT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   c.paired = 0;
   const void* extra = nullptr;
@@ -434,6 +446,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   c.kind = GK_W1_GRAD;
   c.d_w = d_up_proj_weight;
   c.accumulate = accumulate;
+  c.paired = wgrad_pair;
   const cudaError_t e_w1 = timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); });
   MM_TRY(cudaEventRecord(side->join, side->s));  // the join is enqueued whatever happened above
   MM_TRY(cudaStreamWaitEvent(st, side->join, 0));

@@ -72,8 +72,8 @@ struct alignas(128) EpiMaps {
 static_assert(offsetof(EpiMaps, out_lo) == offsetof(EpiMaps, out) + sizeof(CUtensorMap),
               "the split output's lo map follows its hi map");
 
-constexpr int OUT_TILE_BYTES = 32 * 32 * 2;
-constexpr int B_HALF_ROWS = BN / 2;  // paired INPUT_GRAD: rows of B each CTA of a pair loads  // 32 rows x 32 bf16 of staged output (64-byte rows)
+constexpr int OUT_TILE_BYTES = 32 * 32 * 2;  // 32 rows x 32 bf16 of staged output (64-byte rows)
+constexpr int B_HALF_ROWS = BN / 2;          // a CTA of a pair loads half of B's N extent
 static_assert(BK == 64, "one 128-byte swizzle row per k-block");
 
 struct Args {
@@ -166,6 +166,14 @@ struct Traits {
                                                  : 0;
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
   static_assert(SMEM <= 232448, "shared memory budget");
+  // a CTA of a pair MMA (M = 256 over two CTAs) holds its A rows (hi and lo) and half of B's
+  // columns per stage: 32 KB six deep (four beside act_grad's staging), 48 KB four deep for the
+  // weight gradients
+  static constexpr int PAIR_STAGE_BYTES = B_OFF + B_BYTES / 2;
+  static constexpr int PAIR_STAGES = (WGRAD || GU_STAGING) ? 4 : 6;
+  static constexpr size_t PAIR_SMEM =
+      (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
+  static_assert(PAIR_SMEM <= 232448, "pair-MMA shared memory budget");
 };
 
 struct Tile {
@@ -325,7 +333,7 @@ __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __
 // accumulator is released (`acce`) right after the last TMEM read, before the last stores.
 __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile& t, uint32_t tacc,
                                                       int q, int hf, int lane, uint8_t* stage,
-                                                      uint32_t acce) {
+                                                      uint32_t acce, bool acce_cluster = false) {
   const int64_t row0 = (int64_t)t.m0 + q * 32;
   float* gu = reinterpret_cast<float*>(a.out0);
 #pragma unroll 1
@@ -337,7 +345,12 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
     if (c == 2 * hf + 1) {  // last TMEM read of this warp for the tile
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce);
+      if (lane == 0) {
+        if (acce_cluster)
+          mbar_arrive_cluster(acce);
+        else
+          mbar_arrive(acce);
+      }
     }
     const int n = t.n0 + c * 32;
     float g[32], u[32], h[32];
@@ -707,6 +720,19 @@ __device__ __forceinline__ void fused_combine_warp(const Args& a, const Tile& t,
 // rows of the buffer or zero-filled past it) and stores nothing.
 template <int KIND>
 __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
+  if constexpr (Traits<KIND>::WGRAD) {
+    // unit = (expert, pair of weight row tiles, column tile); rank r takes row tile 2p + r
+    const int mp = (a.m_tiles_w + 1) / 2;
+    const int per_e = mp * a.n_tiles_n;
+    const int e = unit / per_e;
+    const int rem = unit - e * per_e;
+    const int p = rem / a.n_tiles_n;
+    const int nt = rem - p * a.n_tiles_n;
+    Tile t = decode_tile<KIND>(a, (e * a.m_tiles_w + 2 * p) * a.n_tiles_n + nt);
+    t.m0 += (int)rank * BM;
+    valid = t.m0 < a.M;
+    return t;
+  }
   const int p = unit / a.n_tiles_n;
   const int nt = unit - p * a.n_tiles_n;
   const int pt = __ldg(a.pair_tile + p);
@@ -723,18 +749,22 @@ __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t ra
   return t;
 }
 
-template <int KIND, bool PAIRED = false>
+// PAIR: 0 = one CTA per tile; 1 = clusters of two CTAs, each with its own MMA on its own row tile,
+// sharing the weight tile by multicast loads; 2 = clusters of two CTAs sharing one M = 256 MMA
+// (tcgen05 .cta_group::2): each CTA holds its 128 rows of A and half of B's columns, the even CTA
+// issues the MMAs, each CTA's tensor memory receives its own 128 accumulator rows.
+template <int KIND, int PAIR = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmL, const __grid_constant__ EpiMaps em,
            const Args a) {
   using TR = Traits<KIND>;
-  static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD,
-                "paired launches: row-grouped GEMM1, GEMM2 and INPUT_GRAD"); 
+  constexpr bool PAIRED = PAIR != 0;
+  constexpr bool MMA2 = PAIR == 2;
+  static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
+                    (MMA2 && TR::WGRAD),
+                "paired launches: GEMM1, GEMM2 and INPUT_GRAD; pair MMAs also the weight gradients");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform); the status
-  // word is the call's (the shared expert's launches point at the routed layout's word too)
-  if (__syncthreads_or(*a.status != 0)) return;
   if constexpr (KIND == GK_ACT_GRAD) {
     // the forward on this workspace kept no gate|up (forward-only): no backward from it
     if (__syncthreads_or(a.hdr[HDR_NO_BACKWARD] != 0)) {
@@ -744,8 +774,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
-  constexpr int STAGES = TR::STAGES;
-  constexpr uint32_t STAGE_BYTES = TR::STAGE_BYTES;
+  constexpr int STAGES = MMA2 ? TR::PAIR_STAGES : TR::STAGES;
+  constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(2 * BM, TR::TN, TR::A_MN ? 1 : 0, TR::B_MN ? 1 : 0);
+  constexpr uint32_t STAGE_BYTES = MMA2 ? TR::PAIR_STAGE_BYTES : TR::STAGE_BYTES;
   const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // act_grad gate|up staging
   const uint32_t bars = epi_base + TR::EPI_BYTES;
   auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -757,9 +788,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile uint32_t* tmem_holder_ptr =
       reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
 
+  // an earlier kernel of this call failed (a CTA-wide vote keeps the exit uniform); the status
+  // word is the call's (the shared expert's launches point at the routed layout's word too).
+  // The two CTAs of a pair take the same decision (two words at the end of the barrier area):
+  // neither may leave while the other waits for it at a cluster barrier or in the pair's
+  // tensor-memory allocation.
+  int failed_before = __syncthreads_or(*a.status != 0);
+  if constexpr (PAIRED) {
+    const uint32_t flag = bars + BAR_BYTES - 8;
+    volatile uint32_t* flag_ptr = reinterpret_cast<volatile uint32_t*>(smem_raw + (flag - raw));
+    if (threadIdx.x == 0) flag_ptr[0] = (uint32_t)failed_before;
+    cluster_sync();
+    if (threadIdx.x == 0) flag_ptr[1] = ld_shared_cluster(mapa_shared(flag, cluster_ctarank() ^ 1u));
+    cluster_sync();  // the peer has read this CTA's flag before either may leave
+    failed_before = (int)(flag_ptr[0] | flag_ptr[1]);
+  }
+  if (failed_before) return;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = PAIRED      ? a.hdr[HDR_NUM_MPAIRS] * a.n_tiles_n
-                    : TR::WGRAD ? a.E * a.m_tiles_w * a.n_tiles_n
+  const int total = (PAIRED && TR::WGRAD) ? a.E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+                    : PAIRED                ? a.hdr[HDR_NUM_MPAIRS] * a.n_tiles_n
+                    : TR::WGRAD             ? a.E * a.m_tiles_w * a.n_tiles_n
                     : TR::FUSED ? a.hdr[HDR_NUM_MTILES] * (a.n_tiles_n + a.n2)
                                 : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
   // work units of this CTA: tile (or pair) first, first + step, ...
@@ -778,11 +827,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIRED ? 2 : 1);  // paired: both CTAs' MMAs release a stage
+      mbar_init(empty_bar(s), PAIR == 1 ? 2 : 1);  // PAIR 1: both CTAs' MMAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), NUM_EPI_WARPS);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (a pair MMA's even CTA: per epilogue warp of both CTAs)
+      mbar_init(acce_bar(b), MMA2 ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     }
     if constexpr (TR::GU_STAGING)
       for (int ew = 0; ew < NUM_EPI_WARPS; ++ew) mbar_init(gu_bar(ew), 1);
@@ -803,8 +853,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TR::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (MMA2) {
+      tmem_alloc_pair(tmem_holder, TR::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, TR::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -843,8 +898,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + TR::B_OFF;
-          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
           const int k0 = kb * BK;
+          if constexpr (MMA2) {
+            // both CTAs' bytes complete on the even CTA's barrier; only it posts their count
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+            const uint32_t fb = mapa_shared(full_bar(s), 0);
+            if constexpr (TR::WGRAD) {  // this CTA's 128 rows of A (MN-major), hi and lo
+              tma_load_2d_pair(sa, &tmA, fb, t.m0, t.row0 + k0);
+              tma_load_2d_pair(sa + MN_BLOCK_BYTES, &tmA, fb, t.m0 + 64, t.row0 + k0);
+              tma_load_2d_pair(sa + TR::A_LO_OFF, &tmL, fb, t.m0, t.row0 + k0);
+              tma_load_2d_pair(sa + TR::A_LO_OFF + MN_BLOCK_BYTES, &tmL, fb, t.m0 + 64,
+                               t.row0 + k0);
+            } else {
+              tma_load_2d_pair(sa, &tmA, fb, k0, t.m0);  // this CTA's 128 rows of A
+            }
+            // this CTA's half of B's columns (its MMA share), in its own shared memory
+            if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
+              const int c0 = (rank ? a.I : 0) + t.n0;
+              tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
+              tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, k0, t.e);
+            } else if constexpr (KIND == GK_GEMM2) {  // rank r: column blocks 2r and 2r + 1
+              const int c0 = t.n0 + 128 * (int)rank;
+              tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
+              tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, k0, t.e);
+            } else if constexpr (TR::WGRAD) {  // rank r: column blocks 2r and 2r + 1 of the rows
+              const int c0 = t.n0 + 128 * (int)rank;
+              tma_load_2d_pair(sb, &tmB, fb, c0, t.row0 + k0);
+              tma_load_2d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, t.row0 + k0);
+            } else {  // INPUT_GRAD, K-major B: rank r loads rows 128r..128r+127
+              tma_load_3d_pair(sb, &tmB, fb, k0, t.n0 + B_HALF_ROWS * (int)rank, t.e);
+            }
+            continue;
+          }
+          mbar_arrive_expect_tx(full_bar(s), STAGE_BYTES);
           if constexpr (TR::A_MN) {
             tma_load_2d(sa, &tmA, full_bar(s), t.m0, t.row0 + k0);
             tma_load_2d(sa + MN_BLOCK_BYTES, &tmA, full_bar(s), t.m0 + 64, t.row0 + k0);
@@ -916,7 +1002,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!MMA2 || rank == 0)) {  // a pair MMA is issued by the even CTA alone
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int tile = first; tile < total && ok; tile += step) {
@@ -951,18 +1037,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t lbo_b = TR::B_MN ? MN_BLOCK_BYTES : 16;
             const uint64_t ad = sdesc_sw128(sa + ka, lbo_a, 1024);
             const uint64_t bd = sdesc_sw128(sb + kbo, lbo_b, 1024);
-            umma_bf16(d, ad, bd, TR::IDESC, (kb | kk) != 0 ? 1u : 0u);
-            if constexpr (TR::A_SPLIT)
-              umma_bf16(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, TR::IDESC, 1u);
+            if constexpr (MMA2) {
+              umma_bf16_pair(d, ad, bd, PAIR_IDESC, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (TR::A_SPLIT)
+                umma_bf16_pair(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, PAIR_IDESC,
+                               1u);
+            } else {
+              umma_bf16(d, ad, bd, TR::IDESC, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (TR::A_SPLIT)
+                umma_bf16(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, TR::IDESC, 1u);
+            }
           }
-          if constexpr (PAIRED)
+          if constexpr (MMA2)
+            umma_commit_pair_mc(empty_bar(s), 0x3);  // both CTAs' producers refill this stage
+          else if constexpr (PAIRED)
             umma_commit_mc(empty_bar(s), 0x3);  // both CTAs' producers wait on this stage
           else
             umma_commit(empty_bar(s));
         }
         if (!ok) break;
         // (test hook: CTA 0 withholds its first hand-off, so its epilogue's wait runs out)
-        if (!(a.inject_stall && blockIdx.x == 0 && acc_it == 0)) umma_commit(accf_bar(buf));
+        if (!(a.inject_stall && blockIdx.x == 0 && acc_it == 0)) {
+          if constexpr (MMA2)
+            umma_commit_pair_mc(accf_bar(buf), 0x3);  // both CTAs' epilogues
+          else
+            umma_commit(accf_bar(buf));
+        }
         ++acc_it;
       }
     }
@@ -978,13 +1078,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int hf = (warp - 2) >> 2;  // column half of the tile
     const uint32_t sbuf = epi_base + (warp - 2) * 2 * OUT_TILE_BYTES;  // output staging
     uint32_t chunk_no = 0;
+    // hands accumulator `b` back to the MMA issuer (for a pair MMA: the even CTA's barrier)
+    auto release_acc = [&](uint32_t b) {
+      if constexpr (MMA2)
+        mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+      else
+        mbar_arrive(acce_bar(b));
+    };
     uint32_t acc_it = 0;
     for (int tile = first; tile < total; tile += step) {
       bool tile_ok;
       const Tile t = tile_at(tile, tile_ok);
       if (t.kiters == 0) {
         if constexpr (TR::WGRAD) {
-          if (!a.accumulate)  // adding zero changes nothing
+          if (!a.accumulate && tile_ok)  // adding zero changes nothing
             staged_store_tile<KIND>(a, t, 0u, q, hf, lane, &em.out, sbuf,
                                     smem_raw + (sbuf - raw), chunk_no, true);
         }
@@ -1004,7 +1111,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!tile_ok) {  // a pair's second tile outside the expert: nothing to store
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar(buf));
+        if (lane == 0) release_acc(buf);
         ++acc_it;
         continue;
       }
@@ -1031,7 +1138,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       if constexpr (TR::ROW_STAGING) {  // releases the accumulator itself
-        gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw), acce_bar(buf));
+        gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw),
+                              MMA2 ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf), MMA2);
         ++acc_it;
         continue;
       }
@@ -1040,7 +1148,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 chunk_no);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));
+      if (lane == 0) release_acc(buf);
       if constexpr (KIND == GK_GEMM2_COMBINE) fused_combine_warp(a, t, q, hf, lane);
       ++acc_it;
     }
@@ -1057,7 +1165,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TR::TMEM_COLS);
+    if constexpr (MMA2)
+      tmem_dealloc_pair(tmem_base, TR::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TR::TMEM_COLS);
   }
 }
 
@@ -1135,7 +1246,14 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int KIND, bool PAIRED>
+// Dynamic shared memory of a launch: the stage ring, the epilogue's buffers, alignment slack
+// and the barriers.
+template <int KIND, int PAIR>
+constexpr size_t smem_bytes() {
+  return PAIR == 2 ? Traits<KIND>::PAIR_SMEM : Traits<KIND>::SMEM;
+}
+
+template <int KIND, int PAIR>
 cudaError_t set_smem_attr() {
   static uint64_t done_mask = 0;
   int dev = 0;
@@ -1143,17 +1261,18 @@ cudaError_t set_smem_attr() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (done_mask & bit) return cudaSuccess;
-  e = cudaFuncSetAttribute(k_gemm<KIND, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Traits<KIND>::SMEM);
+  e = cudaFuncSetAttribute(k_gemm<KIND, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes<KIND, PAIR>());
   if (e == cudaSuccess) done_mask |= bit;
   return e;
 }
 
 inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-template <int KIND, bool PAIRED = false>
+template <int KIND, int PAIR = 0>
 cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
-  cudaError_t err = set_smem_attr<KIND, PAIRED>();
+  constexpr bool PAIRED = PAIR != 0;
+  cudaError_t err = set_smem_attr<KIND, PAIR>();
   if (err != cudaSuccess) return err;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorNoDevice;
@@ -1378,19 +1497,21 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = Traits<KIND>::SMEM;
+    cfg.dynamicSmemBytes = smem_bytes<KIND, PAIR>();
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(nsm & ~1));
     int max_clusters = 0;
-    err = cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm<KIND, true>, &cfg);
+    err = cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm<KIND, PAIR>, &cfg);
     if (err != cudaSuccess) return err;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int64_t units = (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
+    const int64_t units = Traits<KIND>::WGRAD
+                              ? E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+                              : (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
     cfg.gridDim = dim3((unsigned)(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, k_gemm<KIND, true>, ta, tb, tl, em, a);
+    return cudaLaunchKernelEx(&cfg, k_gemm<KIND, PAIR>, ta, tb, tl, em, a);
   } else {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
     k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
@@ -1401,18 +1522,26 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
-  const bool paired = c.paired && c.rows == nullptr;  // expert-sorted rows only
+  const int pair = c.rows == nullptr ? c.paired : 0;  // expert-sorted rows only
   switch (c.kind) {
     case GK_GEMM1_SWIGLU:
-      return paired ? run<GK_GEMM1_SWIGLU, true>(w, ws, c, st) : run<GK_GEMM1_SWIGLU>(w, ws, c, st);
+      return pair == 2   ? run<GK_GEMM1_SWIGLU, 2>(w, ws, c, st)
+             : pair == 1 ? run<GK_GEMM1_SWIGLU, 1>(w, ws, c, st)
+                         : run<GK_GEMM1_SWIGLU>(w, ws, c, st);
     case GK_GEMM2:
-      return paired ? run<GK_GEMM2, true>(w, ws, c, st) : run<GK_GEMM2>(w, ws, c, st);
+      return pair == 2   ? run<GK_GEMM2, 2>(w, ws, c, st)
+             : pair == 1 ? run<GK_GEMM2, 1>(w, ws, c, st)
+                         : run<GK_GEMM2>(w, ws, c, st);
     case GK_GEMM2_COMBINE: return run<GK_GEMM2_COMBINE>(w, ws, c, st);
     case GK_ACT_GRAD: return run<GK_ACT_GRAD>(w, ws, c, st);
     case GK_INPUT_GRAD:
-      return paired ? run<GK_INPUT_GRAD, true>(w, ws, c, st) : run<GK_INPUT_GRAD>(w, ws, c, st);
-    case GK_W2_GRAD: return run<GK_W2_GRAD>(w, ws, c, st);
-    case GK_W1_GRAD: return run<GK_W1_GRAD>(w, ws, c, st);
+      return pair == 2   ? run<GK_INPUT_GRAD, 2>(w, ws, c, st)
+             : pair == 1 ? run<GK_INPUT_GRAD, 1>(w, ws, c, st)
+                         : run<GK_INPUT_GRAD>(w, ws, c, st);
+    case GK_W2_GRAD:
+      return pair == 2 ? run<GK_W2_GRAD, 2>(w, ws, c, st) : run<GK_W2_GRAD>(w, ws, c, st);
+    case GK_W1_GRAD:
+      return pair == 2 ? run<GK_W1_GRAD, 2>(w, ws, c, st) : run<GK_W1_GRAD>(w, ws, c, st);
     case GK_FWD_FUSED: return run<GK_FWD_FUSED>(w, ws, c, st);
   }
   return cudaErrorInvalidValue;

@@ -59,8 +59,9 @@ struct GemmCall {
   // GEMM2 / fused forward: when comb_y is set, the weighted combine into comb_y runs in the
   // epilogue (the per-(token, 128-column chunk) counters at off_cnt must be zero)
   int skip_gu = 0;     // GEMM1 / fused forward: do not store gate|up (forward only)
-  int paired = 0;      // GEMM1 / GEMM2 / INPUT_GRAD on expert-sorted rows: clusters of two CTAs
-                       // sharing the weight tile of two row tiles (multicast loads)
+  int paired = 0;      // GEMM1 / GEMM2 / INPUT_GRAD on expert-sorted rows, clusters of two CTAs
+                       // over two row tiles of one expert: 1 = each CTA its own MMA, the weight
+                       // tile shared by multicast loads; 2 = one M = 256 MMA of the pair
   void* comb_y = nullptr;
   const float* comb_w = nullptr;
   const void* comb_extra = nullptr;

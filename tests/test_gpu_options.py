@@ -214,28 +214,56 @@ def test_torch_entry_point_under_no_grad_runs_forward_only():
     assert torch.equal(y, run_layer(inp, backward=False)["y"])
 
 
-@pytest.mark.parametrize("T,H,I,E,K", [(1, 64, 64, 1, 1),       # one row tile: its pair's second is empty
-                                       (1000, 136, 72, 7, 3),   # ragged H and I, odd tile counts
-                                       (3000, 512, 256, 16, 4),
-                                       (300, 256, 128, 40, 2)])  # many experts with one tile
-def test_paired_tiles_equal_single_tiles(T, H, I, E, K):
-    """MM_FLAG_PAIRED_TILES (clusters of two CTAs sharing the weight tile of two row tiles of one
-    expert, multicast loads) gives outputs identical bit for bit to the one-CTA launches."""
+SINGLE = _abi.MM_FLAG_SINGLE_CTA_TILES
+
+
+@pytest.mark.parametrize("T,H,I,E,K", [(1, 64, 64, 1, 1),        # one row tile: its pair's second is empty
+                                       (1000, 136, 72, 7, 3),    # ragged H and I, odd tile counts
+                                       (3000, 512, 256, 16, 4),  # weight gradients paired too
+                                       (300, 256, 128, 40, 2),   # many experts with one tile
+                                       (2000, 136, 72, 3, 2),    # paired weight gradients, ragged:
+                                       (1500, 200, 200, 2, 1)])  # odd weight row tiles, B halves past N
+@pytest.mark.parametrize("flags", [0, _abi.MM_FLAG_PAIRED_TILES])
+def test_paired_tiles_equal_single_tiles(T, H, I, E, K, flags):
+    """The default pair MMAs (two row tiles of one expert, or two weight row tiles, as one
+    M = 256 tcgen05 MMA of a CTA pair) and MM_FLAG_PAIRED_TILES (two CTAs sharing the weight tile
+    by multicast loads) give outputs identical bit for bit to one CTA per tile."""
     w = synth.small("pair", T, H, I, E, K, seed=T + 7)
     inp = make_inputs(w)
-    ref = run_layer(inp)
-    pt = _abi.MM_FLAG_PAIRED_TILES
-    out = run_layer(inp, flags=pt, bwd_flags=pt)
-    assert out["status"] == _abi.MM_OK
+    ref = run_layer(inp, flags=SINGLE, bwd_flags=SINGLE)
+    out = run_layer(inp, flags=flags, bwd_flags=flags)
+    assert out["status"] == _abi.MM_OK and ref["status"] == _abi.MM_OK
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(out[k], ref[k]), k
 
 
-def test_paired_tiles_on_the_skew_workload():
+@pytest.mark.parametrize("flags", [0, _abi.MM_FLAG_PAIRED_TILES])
+def test_paired_tiles_on_the_skew_workload(flags):
     w = synth.BY_NAME["skew"]
     inp = make_inputs(w)
-    ref = run_layer(inp)
-    pt = _abi.MM_FLAG_PAIRED_TILES
-    out = run_layer(inp, flags=pt, bwd_flags=pt)
+    ref = run_layer(inp, flags=SINGLE, bwd_flags=SINGLE)
+    out = run_layer(inp, flags=flags, bwd_flags=flags)
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(out[k], ref[k]), k
+
+
+@pytest.mark.parametrize("bwd", [0, F32, F32 | ACC, ACC])
+def test_pair_mma_weight_grads_output_forms(bwd):
+    """Pair-MMA weight gradients (2048 rows per expert) in bf16, fp32, fp32 accumulated and bf16
+    accumulated equal the one-CTA ones bit for bit, including an expert with no slot."""
+    w, inp = _inputs(T=4096, H=256, I=128, E=5, K=2, seed=31)
+    base = {}
+    if bwd & ACC:
+        g = torch.Generator(device="cuda").manual_seed(5)
+        dt = torch.float32 if bwd & F32 else torch.bfloat16
+        base = {"d_up": torch.randn(inp["w_up"].shape, generator=g, device="cuda").to(dt),
+                "d_down": torch.randn(inp["w_down"].shape, generator=g, device="cuda").to(dt)}
+    ref = run_layer(inp, flags=SINGLE, bwd_flags=bwd | SINGLE,
+                    **{k: v.clone() for k, v in base.items()})
+    out = run_layer(inp, bwd_flags=bwd, **{k: v.clone() for k, v in base.items()})
+    assert out["status"] == _abi.MM_OK
+    for k in ("dW_up", "dW_down", "dx", "d_topk_weights"):
+        assert torch.equal(out[k], ref[k]), k
+    if not bwd & ACC:
+        assert torch.count_nonzero(out["dW_up"][-1]) == 0
+        assert torch.count_nonzero(out["dW_down"][-1]) == 0
