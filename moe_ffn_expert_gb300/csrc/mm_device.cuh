@@ -124,9 +124,11 @@ __device__ __forceinline__ uint32_t ld_shared_cluster(uint32_t cluster_addr) {
   return v;
 }
 
-// Arrives (release, cluster scope) on an mbarrier of this or another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+// Arrives on an mbarrier of another CTA of the cluster, ordering no memory accesses (relaxed):
+// for hand-offs whose data is not in memory, such as tensor-memory reads already completed with
+// tcgen05.wait::ld and fenced with tcgen05.fence::before_thread_sync.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
 

@@ -333,7 +333,7 @@ __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __
 // accumulator is released (`acce`) right after the last TMEM read, before the last stores.
 __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile& t, uint32_t tacc,
                                                       int q, int hf, int lane, uint8_t* stage,
-                                                      uint32_t acce, bool acce_cluster = false) {
+                                                      uint32_t acce, bool acce_remote = false) {
   const int64_t row0 = (int64_t)t.m0 + q * 32;
   float* gu = reinterpret_cast<float*>(a.out0);
 #pragma unroll 1
@@ -346,8 +346,8 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (acce_cluster)
-          mbar_arrive_cluster(acce);
+        if (acce_remote)  // the odd CTA of a pair MMA: the even CTA's barrier
+          mbar_arrive_remote_relaxed(acce);
         else
           mbar_arrive(acce);
       }
@@ -1078,10 +1078,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int hf = (warp - 2) >> 2;  // column half of the tile
     const uint32_t sbuf = epi_base + (warp - 2) * 2 * OUT_TILE_BYTES;  // output staging
     uint32_t chunk_no = 0;
-    // hands accumulator `b` back to the MMA issuer (for a pair MMA: the even CTA's barrier)
+    // hands accumulator `b` back to the MMA issuer (for the odd CTA of a pair MMA: the even
+    // CTA's barrier; its tensor-memory reads are complete, so the arrive orders nothing else)
     auto release_acc = [&](uint32_t b) {
-      if constexpr (MMA2)
-        mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+      if (MMA2 && rank != 0)
+        mbar_arrive_remote_relaxed(mapa_shared(acce_bar(b), 0));
       else
         mbar_arrive(acce_bar(b));
     };
@@ -1139,7 +1140,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if constexpr (TR::ROW_STAGING) {  // releases the accumulator itself
         gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw),
-                              MMA2 ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf), MMA2);
+                              (MMA2 && rank != 0) ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf),
+                              MMA2 && rank != 0);
         ++acc_it;
         continue;
       }
