@@ -220,19 +220,19 @@ def run_gpu(args):
 
     bufs0 = dict(x=x, ids=ids, tw=tw, dy=dy, y=y, dx=dx, dtk=dtk)
 
-    def fwd(bf=bufs0, extra_flags=0):
+    def fwd(bf=bufs0, extra_flags=0, s=None):
         args_f = (bf["x"].data_ptr(), bf["ids"].data_ptr(), bf["tw"].data_ptr(), wu.data_ptr(),
-                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, st,
+                  wd.data_ptr(), bf["y"].data_ptr(), ws.data_ptr(), nbytes, s or st,
                   args.fwd_flags | extra_flags)
         if I_s:
             _abi.check(_abi.mm_forward_ex(d, opt, *args_f), "fwd")
         else:
             _abi.check(_abi.mm_forward(d, *args_f), "fwd")
 
-    def bwd(bf=bufs0):
+    def bwd(bf=bufs0, s=None):
         args_b = (bf["dy"].data_ptr(), bf["x"].data_ptr(), bf["ids"].data_ptr(),
                   bf["tw"].data_ptr(), wu.data_ptr(), wd.data_ptr(), ws.data_ptr(), nbytes,
-                  bf["dx"].data_ptr(), bf["dtk"].data_ptr(), du.data_ptr(), dd.data_ptr(), st,
+                  bf["dx"].data_ptr(), bf["dtk"].data_ptr(), du.data_ptr(), dd.data_ptr(), s or st,
                   args.bwd_flags)
         if I_s:
             _abi.check(_abi.mm_backward_ex(d, opt, *args_b), "bwd")
@@ -299,6 +299,30 @@ def run_gpu(args):
     infer_ms = timed(lambda: fwd(extra_flags=_abi.MM_FLAG_FORWARD_ONLY), n_part) / n_part
     fwd()
     bwd_ms = timed(bwd, n_part) / n_part
+
+    # ---- the same step captured once as a CUDA graph and replayed (no per-launch host work)
+    graph = None
+    try:
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):  # one eager step on the capture stream first
+            fwd(s=gs.cuda_stream)
+            bwd(s=gs.cuda_stream)
+        gs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=gs):
+            fwd(s=gs.cuda_stream)
+            bwd(s=gs.cuda_stream)
+        g.replay()
+        n_graph = max(3, min(args.steps, 20))
+        graph_ms = timed(g.replay, n_graph) / n_graph
+        if _abi.mm_get_status(ws.data_ptr(), st) != _abi.MM_OK:
+            raise RuntimeError("device status error after the graph replays")
+        graph = {"ms_per_step": round(graph_ms, 4), "tokens_per_s": round(T / (graph_ms / 1e3), 1),
+                 "note": "one fwd+bwd step captured once as a CUDA graph, replayed "
+                         f"{n_graph} times (per-stage timer off)"}
+    except Exception as exc:  # reported, not fatal: the headline does not depend on it
+        graph = {"error": f"{type(exc).__name__}: {exc}"[:200]}
 
     # ---- end to end: host buffers in, results out, copies inside the timed region
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
@@ -434,6 +458,7 @@ def run_gpu(args):
                           "note": "mm_forward with MM_FLAG_FORWARD_ONLY (no gate|up kept)"},
         "bwd": {"ms": round(bwd_ms, 4), "tokens_per_s": round(T / (bwd_ms / 1e3), 1),
                 "tflops": round(flops["bwd"] / (bwd_ms / 1e3) / 1e12, 2)},
+        "graph": graph,
         "first_call_ms": round(first_ms, 3),
         "step_ms": {"median": round(per_step[len(per_step) // 2], 4), "min": round(per_step[0], 4),
                     "max": round(per_step[-1], 4)},

@@ -42,6 +42,7 @@
 // a wait that runs out records MM_ERR_TIMEOUT, stops the role and still frees TMEM.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mm_device.cuh"
@@ -1504,9 +1505,19 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(nsm & ~1));
-    int max_clusters = 0;
-    err = cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm<KIND, PAIR>, &cfg);
+    // clusters that fit at once, queried once per device (a launch inside a stream capture then
+    // makes no query)
+    static std::atomic<int> max_clusters_of[64];
+    int dev = 0;
+    err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int max_clusters = max_clusters_of[dev].load(std::memory_order_relaxed);
+    if (max_clusters == 0) {
+      err = cudaOccupancyMaxActiveClusters(&max_clusters, k_gemm<KIND, PAIR>, &cfg);
+      if (err != cudaSuccess) return err;
+      max_clusters_of[dev].store(max_clusters, std::memory_order_relaxed);
+    }
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int64_t units = Traits<KIND>::WGRAD
                               ? E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
