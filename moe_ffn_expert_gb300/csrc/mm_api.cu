@@ -326,6 +326,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
                 c.timeout_ns, 0, 0, x, reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS,
                 1};  // its output is added with weight 1: kept as a bf16 hi + lo pair
     cs.skip_gu = c.skip_gu;
+    cs.paired = c.paired;  // row tiles of its T rows pair like an expert's
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_shared_tables(p.ws_s, wss, st); }));
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
     cs.kind = GK_GEMM2;
@@ -418,6 +419,8 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   char* wss = ws + p.base_s;
   GemmCall cs{GK_ACT_GRAD, nullptr, nullptr, nullptr, kDefaultTimeoutNs, 0, 0, dy,
               reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS, 1, c.wgrad_f32};
+  // the shared expert is one expert of T rows: the same pair rules
+  const int shared_wgrad_pair = (pair == 2 && w.T >= 512) ? 2 : 0;
   if (p.shared) {  // shared expert: act_grad, W2Grad (rows = dy), input_grad
     cs.w_up = se->up_proj_weight;
     cs.w_down = se->down_proj_weight;
@@ -425,10 +428,12 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
     cs.kind = GK_W2_GRAD;
     cs.d_w = se->d_down_proj_weight;
     cs.accumulate = accumulate;
+    cs.paired = shared_wgrad_pair;
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
     cs.kind = GK_INPUT_GRAD;
     cs.d_w = nullptr;
     cs.accumulate = 0;
+    cs.paired = pair;
     cs.rows = nullptr;
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
     extra = wss + p.ws_s.off_o;
@@ -457,6 +462,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
     cs.d_w = se->d_up_proj_weight;
     cs.accumulate = accumulate;
     cs.rows = x;
+    cs.paired = shared_wgrad_pair;
     MM_TRY(timed(ST_SHARED, st, [&] { return launch_gemm(p.ws_s, wss, cs, st); }));
   }
   return MM_OK;

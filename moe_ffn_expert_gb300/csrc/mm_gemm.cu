@@ -1535,7 +1535,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
 }  // namespace
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
-  const int pair = c.rows == nullptr ? c.paired : 0;  // expert-sorted rows only
+  const int pair = c.paired;
   switch (c.kind) {
     case GK_GEMM1_SWIGLU:
       return pair == 2   ? run<GK_GEMM1_SWIGLU, 2>(w, ws, c, st)

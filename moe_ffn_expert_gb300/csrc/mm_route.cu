@@ -392,11 +392,15 @@ __global__ void __launch_bounds__(256) k_export_rows(const int32_t* __restrict__
 // padded row r is token r (r < T), the rows up to the next multiple of BM are pad rows.
 __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts, int32_t* offsets,
                                                        int32_t* poff, int32_t* tile_expert,
-                                                       int32_t* slot_of_row, float* w_row,
-                                                       int32_t* row_of_slot, int T) {
+                                                       int32_t* pair_tile, int32_t* slot_of_row,
+                                                       float* w_row, int32_t* row_of_slot, int T) {
   const int Tp = (T + BM - 1) / BM * BM;
+  const int nm = Tp / BM;
   const int r = blockIdx.x * 256 + threadIdx.x;
-  if (r < HDR_WORDS) hdr[r] = r == HDR_NUM_MTILES ? Tp / BM : 0;  // every header word
+  if (r < HDR_WORDS)  // every header word
+    hdr[r] = r == HDR_NUM_MTILES ? nm : r == HDR_NUM_MPAIRS ? (nm + 1) / 2 : 0;
+  // row tiles 2i and 2i + 1 form pair i (~2i when the second is past the last row tile)
+  if (r < (nm + 1) / 2) pair_tile[r] = 2 * r + 1 < nm ? 2 * r : ~(2 * r);
   if (r == 0) {
     counts[0] = T;
     offsets[0] = 0;
@@ -483,8 +487,9 @@ cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStrea
   k_shared_tables<<<div_up((w.T + BM - 1) / BM * BM, 256), 256, 0, st>>>(
       region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_counts),
       region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
-      region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
-      region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
+      region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
+      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
+      region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
   return cudaGetLastError();
 }
 

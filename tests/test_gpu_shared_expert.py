@@ -59,3 +59,18 @@ def test_shared_expert_torch_autograd():
     y.backward(inp["dy"])
     assert torch.equal(y.detach(), ref["y"]) and torch.equal(x.grad, ref["dx"])
     assert torch.equal(su_t.grad, ref["dS_up"]) and torch.equal(sd_t.grad, ref["dS_down"])
+
+
+@pytest.mark.parametrize("T,H,I,E,K,I_s", [(1200, 256, 128, 4, 2, 320),   # 10 row tiles; paired weight
+                                           # gradients with odd weight row tiles (320, 640 rows)
+                                           (333, 256, 128, 8, 3, 200)])   # 3 row tiles: a lone last one
+def test_shared_expert_pairs_equal_single_tiles(T, H, I, E, K, I_s):
+    """The shared expert's GEMMs as pair MMAs (its T rows tiled like an expert's) equal the
+    one-CTA launches bit for bit."""
+    w, inp, su, sd = _case(T, H, I, E, K, I_s, seed=13)
+    single = _abi.MM_FLAG_SINGLE_CTA_TILES
+    ref = run_layer(inp, shared=(su, sd), flags=single, bwd_flags=single)
+    out = run_layer(inp, shared=(su, sd))
+    assert out["status"] == _abi.MM_OK and ref["status"] == _abi.MM_OK
+    for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down", "dS_up", "dS_down"):
+        assert torch.equal(out[k], ref[k]), k
