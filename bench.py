@@ -420,7 +420,9 @@ def run_gpu(args):
             hbm_stages[k] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 3),
                              "bytes_per_launch": int(nbytes_k)}
     hbm_stages["note"] = ("algorithmic bytes / average launch time, against the measured copy "
-                          "bandwidth; combine_dx runs beside w1_grad on a second stream")
+                          "bandwidth; combine_dx runs beside w1_grad on a second stream; a gather "
+                          "reads each token row once per slot (K times), mostly from L2 when the "
+                          "token rows fit there, so its rate can pass the copy bandwidth")
 
     # CPU baseline: the oracle on a bounded sample of this workload
     cpu = (cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 and not I_s
