@@ -87,3 +87,19 @@ def test_stage_table():
     names = [_abi._lib().mm_stage_name(i).decode() for i in range(_abi.MM_NUM_STAGES)]
     assert names[0] == "route_count" and names[-1] == "gemm1_gemm2" and len(set(names)) == 16
     assert _abi.mm_timing_read() == {n: (0.0, 0) for n in names}
+
+
+def test_python_constants_match_the_header():
+    """Every MM_FLAG_* / MM_NUM_STAGES define and every status enumerator of include/mm.h has a
+    twin of the same name and value in the Python binding."""
+    import os
+    import re
+    text = open(os.path.join(os.path.dirname(_abi.__file__), os.pardir, "include", "mm.h")).read()
+    found = {}
+    for name, value in re.findall(r"#define\s+(MM_(?:FLAG_\w+|NUM_STAGES))\s+(0x[0-9a-fA-F]+|\d+)u?", text):
+        found[name] = int(value, 0)
+    for name, value in re.findall(r"\b(MM_(?:OK|ERR_\w+))\s*=\s*(\d+)", text):
+        found[name] = int(value)
+    assert len(found) >= 17
+    for name, value in found.items():
+        assert getattr(_abi, name) == value, name
