@@ -26,14 +26,24 @@
 // Row-grouped kinds walk 128-row tiles of the expert-sorted (padded) row buffers; each tile
 // belongs to one expert, whose weight slab is the third coordinate of a 3-D tensor map.
 // Weight-gradient kinds walk (expert, row tile, column tile) of the weight, reducing over
-// the expert's padded rows (pad rows are zero, an expert with no rows gets a zero tile).
+// the expert's rows (the last 64-row block trimmed to 16-row MMA steps; pad rows are zero, an
+// expert with no rows gets a zero tile).
+//
+// CTA pairs (template argument PAIR = 2, the default for GEMM1, GEMM2, INPUT_GRAD and long
+// weight gradients): two CTAs of a cluster share one 256 x 256 tcgen05.mma.cta_group::2 per
+// 16-deep step. Each holds its own 128 rows of A and half of B's columns (32 KB stages, six
+// deep; 48 KB and four deep for the split weight gradients), both CTAs' TMA loads complete on
+// the even CTA's stage barrier, the even CTA's MMA thread issues and multicasts its commits to
+// both CTAs, and each CTA's epilogue drains its own 128 accumulator rows. PAIR = 1 keeps one MMA
+// per CTA and only shares the weight tile by multicast loads.
 //
 // Warp roles (320 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
 //   warp 0      one thread issues TMA loads into a 4-stage (3 for act_grad and the weight
-//               gradients) shared-memory ring (mbarrier per stage, transaction-count completion);
+//               gradients; the pair counts above) shared-memory ring (mbarrier per stage,
+//               transaction-count completion);
 //   warp 1      allocates 2*BN TMEM columns (two 128xBN fp32 accumulators); one thread issues
-//               tcgen05.mma (128xBNx16 per instruction) and tcgen05.commit's the stage and
-//               accumulator barriers;
+//               tcgen05.mma (128xBNx16 per instruction; 256xBNx16 over a pair, from the even CTA)
+//               and tcgen05.commit's the stage and accumulator barriers;
 //   warps 2-9   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31,
 //               32 tile rows; warps w and w+4 take one column half each), apply the kind's
 //               epilogue through per-warp shared-memory staging (TMA or coalesced stores), and
