@@ -65,10 +65,11 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
   for (int i = lane; i < E; i += 32) chunk_cnt[(size_t)chunk * E + i] = cnt[i];
 }
 
-// One CTA of 1024 threads. Each expert gets P = 1024 / E threads (a power of two, 1 to 32, all
-// in one warp), each owning a contiguous range of the chunk histograms: they sum their ranges,
-// the expert totals are scanned across experts (plain and padded to BM rows), and each thread
-// then turns its range into running padded-row bases, so the chunk loop is split P ways.
+// One CTA of 1024 threads. Each expert gets P = 1024 / E threads (a power of two, 1 to 32), each
+// owning a contiguous range of the chunk histograms; thread tid serves expert tid % E, so a
+// warp reads 32 consecutive experts of one chunk (coalesced). The P threads of an expert sum
+// their ranges, the expert totals are scanned across experts (plain and padded to BM rows),
+// and each thread then turns its range into running padded-row bases.
 __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restrict__ chunk_cnt,
                                                      int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ offsets,
@@ -80,7 +81,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks) {
   __shared__ int wsum[32], wsum_p[32], wsum_q[32];
-  __shared__ int tot_s[1024], po_s[1024], qo_s[1024];
+  __shared__ int tot_s[1024], po_s[1024], qo_s[1024], seg_s[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (hdr[HDR_STATUS] != 0) {  // bad ids: schedule nothing downstream
     if (tid == 0) hdr[HDR_NUM_MTILES] = 0;
@@ -88,24 +89,27 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   }
   int P = 1;  // threads per expert
   while (P < 32 && P * 2 * E <= 1024) P *= 2;
-  const int e = tid / P, j = tid - (tid / P) * P;
-  const bool active = e < E;
+  const int e = tid % E, j = tid / E;
+  const bool active = j < P;
   const int L = (n_chunks + P - 1) / P;  // chunks per thread
   const int k0 = min(n_chunks, j * L), k1 = min(n_chunks, k0 + L);
   int seg = 0;
   if (active) {
 #pragma unroll 8
     for (int k = k0; k < k1; ++k) seg += chunk_cnt[(size_t)k * E + e];
+    seg_s[j * E + e] = seg;
   }
-  // inclusive scan of seg within the expert's group of P lanes (P divides 32)
-  int incl = seg;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, d);
-    if (d < P && j >= d) incl += y;
+  __syncthreads();
+  // this thread's exclusive prefix over the expert's earlier ranges, and the expert's total
+  int before = 0, total = 0;
+  if (active) {
+    for (int i = 0; i < P; ++i) {
+      const int v = seg_s[i * E + e];
+      before += i < j ? v : 0;
+      total += v;
+    }
+    if (j == 0) tot_s[e] = total;
   }
-  const int total = __shfl_sync(0xffffffffu, incl, (lane / P) * P + P - 1);
-  if (active && j == 0) tot_s[e] = total;
   __syncthreads();
 
   // scan of the expert totals (plain and padded), one thread per expert
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
   if (!active) return;
   // chunk histograms -> running padded-row base of each chunk (this thread's range)
   const int po = po_s[e];
-  int run = po + incl - seg;
+  int run = po + before;
   int k = k0;
   for (; k + 8 <= k1; k += 8) {  // eight loads in flight, then the running sums
     int v[8];
