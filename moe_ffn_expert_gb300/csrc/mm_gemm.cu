@@ -61,7 +61,7 @@
 namespace mm {
 namespace {
 
-constexpr int STAGE_BYTES = 48 * 1024;       // every kind: A (+A lo) and B (+B lo) tiles
+constexpr int STAGE_BYTES = 48 * 1024;       // one CTA per tile: A (128 x 64) and B (256 x 64)
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int MN_BLOCK_BYTES = 64 * BK * 2;  // one 64-wide MN block of an MN-major tile: 8 KB
 constexpr int NUM_EPI_WARPS = 8;             // two per TMEM lane quarter, one per column half
