@@ -110,6 +110,19 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Programmatic dependent launch. The library's kernels are launched with programmatic stream
+// serialization, so a kernel's CTAs may become resident while the stream's previous kernel is
+// still finishing. Every kernel calls pdl_wait() before its first access to global memory: it
+// returns once the previous kernels have completed and their writes are visible. The grouped
+// GEMMs call pdl_launch_dependents() when a CTA's work is done, which lets the next kernel's CTAs
+// take SMs as the GEMM's CTAs leave (the short kernels trigger by exiting). Without the launch
+// attribute both do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // The shared::cluster address of the variable at shared::cta address `addr` in CTA `rank` of the
 // cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {

@@ -772,6 +772,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using TR = Traits<KIND>;
   constexpr bool PAIRED = PAIR != 0;
   constexpr bool MMA2 = PAIR == 2;
+  pdl_wait();  // the stream's previous kernels are complete (see mm_device.cuh)
   static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
                     (MMA2 && TR::WGRAD),
                 "paired launches: GEMM1, GEMM2 and INPUT_GRAD; pair MMAs also the weight gradients");
@@ -1171,6 +1172,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  // this CTA's work is done: the next kernel may take its SM as soon as it leaves
+  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   // paired: the peer may still commit onto this CTA's barriers until it is done too
@@ -1504,11 +1507,13 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
     // persistent grid must not wait for SMs), at most one per pair-column unit
     a.pair_tile = reinterpret_cast<const int32_t*>(ws + w.off_pair_tile);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem_bytes<KIND, PAIR>();
     cfg.stream = st;
@@ -1534,11 +1539,13 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
                               : (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
     cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.numAttrs = 2;  // and programmatic stream serialization (the occupancy query had only the
+                       // cluster shape)
     return cudaLaunchKernelEx(&cfg, k_gemm<KIND, PAIR>, ta, tb, tl, em, a);
   } else {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
-    k_gemm<KIND><<<grid, NUM_THREADS, Traits<KIND>::SMEM, st>>>(ta, tb, tl, em, a);
-    return cudaGetLastError();
+    return launch_pdl(k_gemm<KIND, 0>, grid, NUM_THREADS, Traits<KIND>::SMEM, st, ta, tb, tl, em,
+                      a);
   }
 }
 

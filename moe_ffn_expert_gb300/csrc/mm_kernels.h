@@ -8,6 +8,24 @@
 
 namespace mm {
 
+// Launches `kernel` on `st` with programmatic stream serialization (see pdl_wait in
+// mm_device.cuh): the launch may overlap the end of the stream's previous kernel.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- routing, dispatch and combine (mm_route.cu)
 cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids, cudaStream_t st);
 // tokens_per_expert (optional, device int32 [E]): compared with the computed counts; a

@@ -33,6 +33,7 @@ const T* region(const char* ws, size_t off) {
 __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__ ids, int* hdr,
                                                      int32_t* __restrict__ chunk_cnt, int S, int E,
                                                      int n_chunks) {
+  pdl_wait();
   extern __shared__ int32_t cnt_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * 4 + warp;
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      int32_t* __restrict__ pair_tile,
                                                      const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks) {
+  pdl_wait();
   __shared__ int wsum[32], wsum_p[32], wsum_q[32];
   __shared__ int tot_s[1024], po_s[1024], qo_s[1024], seg_s[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ slot_of_row,
                                                     float* __restrict__ w_row, int S, int E,
                                                     int n_chunks) {
+  pdl_wait();
   extern __shared__ int32_t cnt_smem[];
   if (hdr[HDR_STATUS] != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
                                                      uint4* __restrict__ dst,
                                                      const int32_t* __restrict__ slot_of_row,
                                                      const int* hdr, int K, int vpr) {
+  pdl_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (hdr[HDR_STATUS] != 0 || row >= hdr[HDR_NUM_MTILES] * BM) return;
@@ -315,6 +319,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
                                                  const uint4* __restrict__ extra_lo,
                                                  uint4* __restrict__ out, const int* hdr, int T,
                                                  int K, int vpr) {
+  pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (hdr[HDR_STATUS] != 0 || t >= T) return;
@@ -367,6 +372,7 @@ __global__ void __launch_bounds__(256) k_d_topk(const float* __restrict__ p_part
                                                 const int32_t* __restrict__ row_of_slot,
                                                 float* __restrict__ d_topk, const int* hdr, int S,
                                                 int n_tiles, int64_t S_pad) {
+  pdl_wait();
   const int s = blockIdx.x * 256 + threadIdx.x;
   if (hdr[HDR_STATUS] != 0 || s >= S) return;
   const int r = row_of_slot[s];
@@ -398,6 +404,7 @@ __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts
                                                        int32_t* poff, int32_t* tile_expert,
                                                        int32_t* pair_tile, int32_t* slot_of_row,
                                                        float* w_row, int32_t* row_of_slot, int T) {
+  pdl_wait();
   const int Tp = (T + BM - 1) / BM * BM;
   const int nm = Tp / BM;
   const int r = blockIdx.x * 256 + threadIdx.x;
@@ -426,41 +433,36 @@ inline unsigned div_up(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b
 
 cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids, cudaStream_t st) {
   const unsigned grid = div_up(w.n_chunks, 4);
-  k_route_count<<<grid, 128, 4 * w.E * sizeof(int32_t), st>>>(
-      ids, region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk), (int)w.S, (int)w.E,
-      (int)w.n_chunks);
-  return cudaGetLastError();
+  return launch_pdl(k_route_count, grid, 128, 4 * w.E * sizeof(int32_t), st, ids,
+                    region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk), (int)w.S,
+                    (int)w.E, (int)w.n_chunks);
 }
 
 cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* tokens_per_expert,
                               cudaStream_t st) {
-  k_route_scan<<<1, 1024, 0, st>>>(
-      region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
-      region<int32_t>(ws, w.off_counts), region<int32_t>(ws, w.off_offsets),
-      region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_tile_expert),
-      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
-      region<int32_t>(ws, w.off_pair_tile), tokens_per_expert, (int)w.E, (int)w.n_chunks);
-  return cudaGetLastError();
+  return launch_pdl(k_route_scan, 1, 1024, 0, st, region<int>(ws, w.off_hdr),
+                    region<int32_t>(ws, w.off_chunk), region<int32_t>(ws, w.off_counts),
+                    region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
+                    region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
+                    region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_pair_tile),
+                    tokens_per_expert, (int)w.E, (int)w.n_chunks);
 }
 
 cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
                               cudaStream_t st) {
   const unsigned grid = div_up(w.n_chunks, 4);
-  k_route_rank<<<grid, 128, 4 * w.E * sizeof(int32_t), st>>>(
-      ids, topk_w, region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
-      region<int32_t>(ws, w.off_row_of_slot), region<int32_t>(ws, w.off_slot_of_row),
-      region<float>(ws, w.off_w_row), (int)w.S, (int)w.E, (int)w.n_chunks);
-  return cudaGetLastError();
+  return launch_pdl(k_route_rank, grid, 128, 4 * w.E * sizeof(int32_t), st, ids, topk_w,
+                    region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
+                    region<int32_t>(ws, w.off_row_of_slot), region<int32_t>(ws, w.off_slot_of_row),
+                    region<float>(ws, w.off_w_row), (int)w.S, (int)w.E, (int)w.n_chunks);
 }
 
 cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, void* dst,
                                cudaStream_t st) {
   const unsigned grid = div_up(w.S_pad, 8);
-  k_gather_rows<<<grid, 256, 0, st>>>(
-      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
-      region<int32_t>(ws, w.off_slot_of_row), region<int>(ws, w.off_hdr), (int)w.K,
-      (int)(w.H / 8));
-  return cudaGetLastError();
+  return launch_pdl(k_gather_rows, grid, 256, 0, st, reinterpret_cast<const uint4*>(src),
+                    reinterpret_cast<uint4*>(dst), region<int32_t>(ws, w.off_slot_of_row),
+                    region<int>(ws, w.off_hdr), (int)w.K, (int)(w.H / 8));
 }
 
 cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
@@ -468,33 +470,28 @@ cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const
                            const void* extra_lo, bool row_table) {
   const unsigned grid = div_up(w.T, 8);
   auto kern = row_table ? k_combine<true> : k_combine<false>;
-  kern<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(rows),
-                             region<int32_t>(ws, w.off_row_of_slot), weights,
-                             reinterpret_cast<const uint4*>(extra),
-                             reinterpret_cast<const uint4*>(extra_lo),
-                             reinterpret_cast<uint4*>(out), region<int>(ws, w.off_hdr), (int)w.T,
-                             (int)w.K, (int)(w.H / 8));
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, 256, 0, st, reinterpret_cast<const uint4*>(rows),
+                    region<int32_t>(ws, w.off_row_of_slot), weights,
+                    reinterpret_cast<const uint4*>(extra), reinterpret_cast<const uint4*>(extra_lo),
+                    reinterpret_cast<uint4*>(out), region<int>(ws, w.off_hdr), (int)w.T, (int)w.K,
+                    (int)(w.H / 8));
 }
 
 cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st) {
   const unsigned grid = div_up(w.S, 256);
-  k_d_topk<<<grid, 256, 0, st>>>(region<float>(ws, w.off_p_part),
-                                 region<int32_t>(ws, w.off_row_of_slot), d_topk,
-                                 region<int>(ws, w.off_hdr), (int)w.S, (int)w.n_act_tiles,
-                                 w.S_pad);
-  return cudaGetLastError();
+  return launch_pdl(k_d_topk, grid, 256, 0, st, region<float>(ws, w.off_p_part),
+                    region<int32_t>(ws, w.off_row_of_slot), d_topk, region<int>(ws, w.off_hdr),
+                    (int)w.S, (int)w.n_act_tiles, w.S_pad);
 }
 
 cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st) {
   const Workspace& w = ws_shared;
-  k_shared_tables<<<div_up((w.T + BM - 1) / BM * BM, 256), 256, 0, st>>>(
-      region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_counts),
-      region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
-      region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
-      region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
-      region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
-  return cudaGetLastError();
+  return launch_pdl(k_shared_tables, div_up((w.T + BM - 1) / BM * BM, 256), 256, 0, st,
+                    region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_counts),
+                    region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
+                    region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
+                    region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
+                    region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
 }
 
 cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out, cudaStream_t st) {
