@@ -103,3 +103,12 @@ def test_python_constants_match_the_header():
     assert len(found) >= 17
     for name, value in found.items():
         assert getattr(_abi, name) == value, name
+
+
+def test_c_example_builds_against_the_header(tmp_path):
+    """tests/c_abi/layer_step.c (a layer step through the C ABI alone) compiles with the host C
+    compiler against include/mm.h and links against libmm.so; it runs in the GPU tests."""
+    from c_abi_util import build_layer_step
+    exe = build_layer_step(str(tmp_path))
+    import os
+    assert os.access(exe, os.X_OK)
