@@ -18,7 +18,6 @@
 #include <string.h>
 
 #include <algorithm>
-#include <mutex>
 #include <vector>
 
 #include "mm_kernels.h"
@@ -109,23 +108,23 @@ mm_status cuda_fail(cudaError_t e, const char* what) {
     if (_e != cudaSuccess) return cuda_fail(_e, #expr); \
   } while (0)
 
-// A second stream per device, for work that may overlap the caller's stream inside one call,
-// with the two events that fork it from and join it back to the caller's stream. Created once per
-// device (non-blocking, highest priority, so its small grids are scheduled ahead of a persistent
-// GEMM's CTAs as soon as an SM has room).
+// A second stream per device and host thread, for work that may overlap the caller's stream
+// inside one call, with the two events that fork it from and join it back to the caller's
+// stream. Created once per device and thread (non-blocking, highest priority, so its small grids
+// are scheduled ahead of a persistent GEMM's CTAs as soon as an SM has room). One per thread, so
+// that calls from two host threads can never interleave their records of, and waits on, the same
+// events; a thread's own calls are sequential.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 cudaError_t side_stream(SideStream** out) {
-  static std::mutex mu;
-  static SideStream per_dev[64];
+  thread_local SideStream per_dev[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
   SideStream& ss = per_dev[dev];
   if (ss.s == nullptr) {
     int lo = 0, hi = 0;
