@@ -28,8 +28,10 @@
  * Ownership: the caller allocates every buffer, including the workspace. The library allocates
  * no device memory. All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  * stream) and nothing synchronises with the host, except mm_get_status, mm_routing_export
- * (host destination) and mm_forward with MM_FLAG_VALIDATE_IDS. The calls are not thread-safe
- * with respect to one another (the optional stage timer is process-global).
+ * (host destination) and mm_forward with MM_FLAG_VALIDATE_IDS. Host threads may call
+ * concurrently on different workspaces (mm_backward forks work onto a library stream of the
+ * calling thread and joins it back); the optional stage timer (mm_timing_*) is process-global
+ * and for use from one thread while no other thread calls the library.
  *
  * Errors: host-side checks (null or misaligned pointers, sizes out of range, workspace too
  * small) return an error before anything is enqueued. An expert id outside [0, E) can only be

@@ -1249,17 +1249,19 @@ bool map_experts(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, i
   return make_map(m, base, 3, dims, strides, box);
 }
 
+// The per-device values below are cached in atomics: host threads may call concurrently, and
+// a value computed twice is the same value.
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 // Dynamic shared memory of a launch: the stage ring, the epilogue's buffers, alignment slack
@@ -1271,15 +1273,15 @@ constexpr size_t smem_bytes() {
 
 template <int KIND, int PAIR>
 cudaError_t set_smem_attr() {
-  static uint64_t done_mask = 0;
+  static std::atomic<uint64_t> done_mask{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (done_mask & bit) return cudaSuccess;
+  if (done_mask.load(std::memory_order_relaxed) & bit) return cudaSuccess;
   e = cudaFuncSetAttribute(k_gemm<KIND, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_bytes<KIND, PAIR>());
-  if (e == cudaSuccess) done_mask |= bit;
+  if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_relaxed);
   return e;
 }
 
