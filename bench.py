@@ -471,6 +471,7 @@ def run_gpu(args):
                      "peak_kind": f"bf16 sustained ({peak_src})",
                      "traffic": profiled_traffic(top, w.name),
                      **({"executed_tflops": round(2 * achieved, 2),
+                         "executed_frac": round(2 * achieved / peak_sus, 4),
                          "executed_note": "the weight gradients issue two MMAs per k-step (bf16 hi "
                                           "and lo planes of the split operand): twice the "
                                           "algorithmic FLOPs"}
