@@ -400,6 +400,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   // than its halved operand traffic saves)
   const int pair = pair_mode(flags);
   const int wgrad_pair = (pair == 2 && w.S >= 512 * w.E) ? 2 : 0;
+  c.paired = pair == 2 ? 2 : 0;  // act_grad: pair MMAs or one CTA per tile
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;

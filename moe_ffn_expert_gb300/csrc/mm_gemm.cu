@@ -271,6 +271,44 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   return t;
 }
 
+// Work units of the paired launches. Row-grouped kinds: a unit is two row tiles of the same
+// expert and one column tile, so both CTAs need the same B tile (the expert's weights); CTA r of
+// the pair takes row tile mt0 + r. When an expert has an odd number of row tiles its last
+// pair's second tile is not the expert's: that CTA loads other rows of the buffer (or zeros
+// past it), takes part in the MMAs and stores nothing. Weight gradients: a unit is two 128-row
+// tiles of the weight (same expert, same column tile); a second tile past the weight's rows is
+// likewise computed and not stored.
+template <int KIND>
+__device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
+  if constexpr (Traits<KIND>::WGRAD) {
+    // unit = (expert, pair of weight row tiles, column tile); rank r takes row tile 2p + r
+    const int mp = (a.m_tiles_w + 1) / 2;
+    const int per_e = mp * a.n_tiles_n;
+    const int e = unit / per_e;
+    const int rem = unit - e * per_e;
+    const int p = rem / a.n_tiles_n;
+    const int nt = rem - p * a.n_tiles_n;
+    Tile t = decode_tile<KIND>(a, (e * a.m_tiles_w + 2 * p) * a.n_tiles_n + nt);
+    t.m0 += (int)rank * BM;
+    valid = t.m0 < a.M;
+    return t;
+  }
+  const int p = unit / a.n_tiles_n;
+  const int nt = unit - p * a.n_tiles_n;
+  const int pt = __ldg(a.pair_tile + p);
+  const int mt0 = pt >= 0 ? pt : ~pt;
+  valid = rank == 0 || pt >= 0;
+  Tile t;
+  t.part = 0;
+  t.klast = BK / 16;
+  t.e = __ldg(a.tile_expert + mt0);
+  t.m0 = (mt0 + (int)rank) * BM;
+  t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
+  t.row0 = t.m0;
+  t.kiters = a.k_iters;
+  return t;
+}
+
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   uint4 q;
   q.x = pack_bf16(v[0], v[1]);
@@ -438,13 +476,25 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
 // into the warp's staging buffer, and issues the next chunk's load as soon as the warp has read
 // the current one. Output: the warp writes the chunk's six 32x16 bf16 planes to its output
 // staging buffer and lane 0 stores them with TMA (the tensor maps clip columns past I).
+// PAIR = 2: the tiles are the CTA's halves of CTA-pair MMA tiles (units first, first + step, ..;
+// this CTA is `rank` of its pair); a half past the expert is consumed but stores nothing.
+template <int PAIR>
 __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorMap* tm_gu,
                                                   const EpiMaps* em, int total, uint32_t tmem_base,
                                                   uint32_t accf0, uint32_t accf1, uint32_t acce0,
                                                   uint32_t acce1, uint32_t gbar, uint32_t gbuf,
                                                   const uint8_t* gbuf_ptr, uint32_t obuf,
-                                                  uint8_t* obuf_ptr, int warp, int lane) {
+                                                  uint8_t* obuf_ptr, int warp, int lane, int first,
+                                                  int step, uint32_t rank) {
   constexpr int KIND = GK_ACT_GRAD;
+  auto tile_at = [&](int unit, bool& valid) -> Tile {
+    if constexpr (PAIR == 2) {
+      return decode_pair<KIND>(a, unit, rank, valid);
+    } else {
+      valid = true;
+      return decode_tile<KIND>(a, unit);
+    }
+  };
   constexpr int NC = BN / 32;      // 16-column chunks per column half
   const int q = warp & 3;          // TMEM lane quarter = rows 32q..32q+31 of the tile
   const int hf = (warp - 2) >> 2;  // column half
@@ -455,15 +505,16 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     while (ce > c0 && n0 + (ce - 1) * 16 >= a.I) --ce;
     return ce;
   };
-  int ld_tile = blockIdx.x, ld_c = c0;  // next (tile, chunk) to load
+  int ld_tile = first, ld_c = c0;  // next (unit, chunk) to load
   auto issue_next = [&]() {
-    while (ld_tile < total && ld_c >= chunk_end(decode_tile<KIND>(a, ld_tile).n0)) {
-      ld_tile += gridDim.x;
+    bool v;
+    while (ld_tile < total && ld_c >= chunk_end(tile_at(ld_tile, v).n0)) {
+      ld_tile += step;
       ld_c = c0;
     }
     if (ld_tile >= total) return;
     if (lane == 0) {
-      const Tile tn = decode_tile<KIND>(a, ld_tile);
+      const Tile tn = tile_at(ld_tile, v);
       fence_proxy_async_smem();  // the buffer's previous contents were read by the warp
       mbar_arrive_expect_tx(gbar, GU_CHUNK_BYTES);
       tma_load_2d(gbuf, tm_gu, gbar, tn.n0 + ld_c * 16, tn.m0 + q * 32);
@@ -475,8 +526,9 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   uint32_t acc_it = 0, used = 0;
   bool failed = false;
   uint8_t* out_row = obuf_ptr + lane * 32;
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const Tile t = decode_tile<KIND>(a, tile);
+  for (int tile = first; tile < total; tile += step) {
+    bool tile_ok;
+    const Tile t = tile_at(tile, tile_ok);
     const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
     int ok = 1;
     if (lane == 0) ok = mbar_wait(buf ? accf1 : accf0, aph, tmo) ? 1 : 0;
@@ -519,6 +571,7 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
       ++used;
       __syncwarp();
       issue_next();  // the staging buffer is free again: start the next chunk's load
+      if (!tile_ok) continue;  // a pair half past the expert: nothing to compute or store
       // the previous chunk's stores must have finished reading the output staging buffer
       if (lane == 0) bulk_wait_read_all();
       __syncwarp();
@@ -537,10 +590,15 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     }
     if (failed) break;
     // one partial per (column tile, half): the d_topk kernel sums them in a fixed order
-    a.p_part[(int64_t)(2 * (t.n0 / BN) + hf) * a.S_pad + row] = p;
+    if (tile_ok) a.p_part[(int64_t)(2 * (t.n0 / BN) + hf) * a.S_pad + row] = p;
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(buf ? acce1 : acce0);
+    if (lane == 0) {
+      if (PAIR == 2 && rank != 0)  // the odd CTA of a pair MMA: the even CTA's barrier
+        mbar_arrive_remote_relaxed(mapa_shared(buf ? acce1 : acce0, 0));
+      else
+        mbar_arrive(buf ? acce1 : acce0);
+    }
     ++acc_it;
   }
   if (lane == 0) bulk_wait_all();  // this warp's output stores are complete before it exits
@@ -722,43 +780,6 @@ __device__ __forceinline__ void fused_combine_warp(const Args& a, const Tile& t,
   }
 }
 
-// Paired launches (row-grouped GEMM1, GEMM2, INPUT_GRAD): clusters of two CTAs take two row
-// tiles of the same expert and the same column tile, so their B tiles (the expert's weights)
-// are the same: each CTA loads half of B multicast to both, halving the weight traffic into
-// shared memory. A stage is refilled only after both CTAs' MMAs have released it (each MMA
-// commit arrives on both CTAs' empty barriers). When an expert has an odd number of row tiles
-// its last pair's second tile is not the expert's: that CTA runs the MMAs (its A rows are other
-// rows of the buffer or zero-filled past it) and stores nothing.
-template <int KIND>
-__device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
-  if constexpr (Traits<KIND>::WGRAD) {
-    // unit = (expert, pair of weight row tiles, column tile); rank r takes row tile 2p + r
-    const int mp = (a.m_tiles_w + 1) / 2;
-    const int per_e = mp * a.n_tiles_n;
-    const int e = unit / per_e;
-    const int rem = unit - e * per_e;
-    const int p = rem / a.n_tiles_n;
-    const int nt = rem - p * a.n_tiles_n;
-    Tile t = decode_tile<KIND>(a, (e * a.m_tiles_w + 2 * p) * a.n_tiles_n + nt);
-    t.m0 += (int)rank * BM;
-    valid = t.m0 < a.M;
-    return t;
-  }
-  const int p = unit / a.n_tiles_n;
-  const int nt = unit - p * a.n_tiles_n;
-  const int pt = __ldg(a.pair_tile + p);
-  const int mt0 = pt >= 0 ? pt : ~pt;
-  valid = rank == 0 || pt >= 0;
-  Tile t;
-  t.part = 0;
-  t.klast = BK / 16;
-  t.e = __ldg(a.tile_expert + mt0);
-  t.m0 = (mt0 + (int)rank) * BM;
-  t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
-  t.row0 = t.m0;
-  t.kiters = a.k_iters;
-  return t;
-}
 
 // PAIR: 0 = one CTA per tile; 1 = clusters of two CTAs, each with its own MMA on its own row tile,
 // sharing the weight tile by multicast loads; 2 = clusters of two CTAs sharing one M = 256 MMA
@@ -774,8 +795,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr bool MMA2 = PAIR == 2;
   pdl_wait();  // the stream's previous kernels are complete (see mm_device.cuh)
   static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
-                    (MMA2 && TR::WGRAD),
-                "paired launches: GEMM1, GEMM2 and INPUT_GRAD; pair MMAs also the weight gradients");
+                    (MMA2 && (TR::WGRAD || KIND == GK_ACT_GRAD)),
+                "paired launches: GEMM1, GEMM2 and INPUT_GRAD; pair MMAs also act_grad and the "
+                "weight gradients");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if constexpr (KIND == GK_ACT_GRAD) {
     // the forward on this workspace kept no gate|up (forward-only): no backward from it
@@ -937,7 +959,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int c0 = t.n0 + 128 * (int)rank;
               tma_load_2d_pair(sb, &tmB, fb, c0, t.row0 + k0);
               tma_load_2d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, t.row0 + k0);
-            } else {  // INPUT_GRAD, K-major B: rank r loads rows 128r..128r+127
+            } else {  // INPUT_GRAD, ACT_GRAD, K-major B: rank r loads rows 128r..128r+127
               tma_load_3d_pair(sb, &tmB, fb, k0, t.n0 + B_HALF_ROWS * (int)rank, t.e);
             }
             continue;
@@ -1082,9 +1104,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp - 2;
     const uint32_t gbuf = epi_base + ew * GU_CHUNK_BYTES;
     const uint32_t obuf = epi_base + NUM_EPI_WARPS * GU_CHUNK_BYTES + ew * OUT_CHUNK_BYTES;
-    act_grad_epilogue(a, &tmL, &em, total, tmem_base, accf_bar(0), accf_bar(1), acce_bar(0),
-                      acce_bar(1), gu_bar(ew), gbuf, smem_raw + (gbuf - raw), obuf,
-                      smem_raw + (obuf - raw), warp, lane);
+    act_grad_epilogue<PAIR>(a, &tmL, &em, total, tmem_base, accf_bar(0), accf_bar(1),
+                            acce_bar(0), acce_bar(1), gu_bar(ew), gbuf, smem_raw + (gbuf - raw),
+                            obuf, smem_raw + (obuf - raw), warp, lane, first, step, rank);
   } else {
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int hf = (warp - 2) >> 2;  // column half of the tile
@@ -1388,7 +1410,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       const uint64_t gstr[1] = {(uint64_t)(2 * I) * 4};
       const uint32_t gbox[2] = {16, 32};
       ok = map_rows(&ta, dyrows, H, nrows, 64, BM) &&
-           map_experts(&tb, c.w_down, H, I, E, 64, BN) &&
+           map_experts(&tb, c.w_down, H, I, E, 64, PAIRED ? B_HALF_ROWS : BN) &&
            make_map(&tl, ws + w.off_gu, 2, gdims, gstr, gbox, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                     CU_TENSOR_MAP_SWIZZLE_64B);
       // output planes, stored in boxes of 32 rows x 16 columns with the 32-byte swizzle
@@ -1565,7 +1587,8 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
              : pair == 1 ? run<GK_GEMM2, 1>(w, ws, c, st)
                          : run<GK_GEMM2>(w, ws, c, st);
     case GK_GEMM2_COMBINE: return run<GK_GEMM2_COMBINE>(w, ws, c, st);
-    case GK_ACT_GRAD: return run<GK_ACT_GRAD>(w, ws, c, st);
+    case GK_ACT_GRAD:
+      return pair == 2 ? run<GK_ACT_GRAD, 2>(w, ws, c, st) : run<GK_ACT_GRAD>(w, ws, c, st);
     case GK_INPUT_GRAD:
       return pair == 2   ? run<GK_INPUT_GRAD, 2>(w, ws, c, st)
              : pair == 1 ? run<GK_INPUT_GRAD, 1>(w, ws, c, st)
