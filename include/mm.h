@@ -110,8 +110,8 @@ typedef struct mm_dims {
 #define MM_FLAG_PAIRED_TILES 0x40u
 
 /* mm_forward / mm_backward flag: one CTA per 128-row tile in every grouped GEMM. By default
- * GEMM1, GEMM2 (forward) and input_grad (backward), and the weight gradients when the experts
- * average at least 512 rows, run 256-row tiles shared by the two CTAs of a cluster through one
+ * GEMM1, GEMM2 (forward), act_grad and input_grad (backward), and the weight gradients when the
+ * experts average at least 512 rows, run 256-row tiles shared by the two CTAs of a cluster through one
  * tensor-core MMA (tcgen05 .cta_group::2): each CTA holds its 128 rows of A and half of the
  * weight tile's columns, and receives its own rows of the accumulator. Takes precedence over
  * MM_FLAG_PAIRED_TILES. Results are identical bit for bit in every form. */

@@ -29,8 +29,8 @@
 // the expert's rows (the last 64-row block trimmed to 16-row MMA steps; pad rows are zero, an
 // expert with no rows gets a zero tile).
 //
-// CTA pairs (template argument PAIR = 2, the default for GEMM1, GEMM2, INPUT_GRAD and long
-// weight gradients): two CTAs of a cluster share one 256 x 256 tcgen05.mma.cta_group::2 per
+// CTA pairs (template argument PAIR = 2, the default for GEMM1, GEMM2, ACT_GRAD, INPUT_GRAD and
+// long weight gradients): two CTAs of a cluster share one 256 x 256 tcgen05.mma.cta_group::2 per
 // 16-deep step. Each holds its own 128 rows of A and half of B's columns (32 KB stages, six
 // deep; 48 KB and four deep for the split weight gradients), both CTAs' TMA loads complete on
 // the even CTA's stage barrier, the even CTA's MMA thread issues and multicasts its commits to
