@@ -132,7 +132,7 @@ size_t mm_workspace_size(mm_dims d, uint32_t flags);
 /* Forward pass (RFC §2.1): routing (per-expert histogram, prefix offsets, stable permute of
  * the T*K slots), dispatch, GMM1 + SwiGLU, GMM2, weighted combine into y.
  * `workspace` (>= mm_workspace_size bytes, 256-byte aligned) must not be touched by
- * anything else until the matching mm_backward has been enqueued; two forwards whose
+ * anything else until the last mm_backward for it has been enqueued; two forwards whose
  * backwards are still pending need two workspaces. All tensor pointers 16-byte aligned. */
 mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
                      const float* topk_weights, const void* up_proj_weight,
@@ -146,7 +146,10 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
  *   d_up_proj_weight[e]  = x_slot_e^T [d_gate | d_up]   (zero for an expert with no slot),
  *   d_down_proj_weight[e] = (w * h)_e^T dy_slot_e        (zero for an expert with no slot).
  * x, topk_ids, topk_weights and the two weights must be the forward's (the dispatched x rows
- * and the routing are read back from the workspace; x itself is only checked). */
+ * and the routing are read back from the workspace; x itself is only checked). A backward only
+ * reads what mm_forward kept (routing, dispatched x rows, gate|up) and overwrites its own scratch,
+ * so one forward may be followed by several backwards (another dy: a retained autograd graph),
+ * each giving what a single one would, bit for bit. */
 mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
                       const float* topk_weights, const void* up_proj_weight,
                       const void* down_proj_weight, void* workspace, size_t workspace_bytes,

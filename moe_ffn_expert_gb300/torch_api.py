@@ -53,6 +53,13 @@ class Workspace:
             raise ValueError(f"unsupported sizes T={T} H={H} I={I} E={E} K={K} I_s={shared_I}")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
 
+    @classmethod
+    def wrap(cls, dims, buf: torch.Tensor) -> "Workspace":
+        """A Workspace over an existing buffer (one that a forward has filled)."""
+        ws = cls.__new__(cls)
+        ws.dims, ws.buf, ws.nbytes = dims, buf, buf.numel()
+        return ws
+
     @property
     def ptr(self) -> int:
         return self.buf.data_ptr()
@@ -139,18 +146,23 @@ class HyperMegaMoEFunction(torch.autograd.Function):
         if not any(ctx.needs_input_grad):  # inference (no_grad or no input needs a gradient)
             flags |= _abi.MM_FLAG_FORWARD_ONLY
         y = forward(ws, x, ids, w, wu, wd, flags=flags, shared=shared, tokens_per_expert=tpe)
-        ctx.ws = ws if any(ctx.needs_input_grad) else None
+        ctx.dims = ws.dims
         ctx.wdtype = topk_weights.dtype
         ctx.has_shared = shared is not None
-        ctx.save_for_backward(x, ids, w, wu, wd, *(shared or ()))
+        # the workspace is saved like any other tensor: autograd frees it after the backward,
+        # or keeps it for another one under retain_graph (a backward only reads what the
+        # forward left in it)
+        kept = (ws.buf,) if any(ctx.needs_input_grad) else ()
+        ctx.save_for_backward(x, ids, w, wu, wd, *(shared or ()), *kept)
         return y
 
     @staticmethod
     def backward(ctx, dy):
-        x, ids, w, wu, wd, *shared = ctx.saved_tensors
-        out = backward(ctx.ws, dy.contiguous().to(torch.bfloat16), x, ids, w, wu, wd,
+        x, ids, w, wu, wd, *rest = ctx.saved_tensors
+        *shared, buf = rest
+        ws = Workspace.wrap(ctx.dims, buf)
+        out = backward(ws, dy.contiguous().to(torch.bfloat16), x, ids, w, wu, wd,
                        shared=tuple(shared) if ctx.has_shared else None)
-        ctx.ws = None
         dx, d_topk, d_up, d_down = out[:4]
         ds_up, ds_down = out[4:] if ctx.has_shared else (None, None)
         return dx, None, d_topk.to(ctx.wdtype), d_up, d_down, ds_up, ds_down, None
