@@ -1,0 +1,53 @@
+"""Many seeded random shapes, bit for bit: the default launches twice (run-to-run determinism),
+against the one-CTA launches, the multicast-pair launches, and a forward with the fused combine
+and/or the one-launch GEMM1 -> GEMM2 form. Different schedules of the same arithmetic must give
+the same bits, so a race or an unwritten read in any of them shows up as a difference. The
+oracle bounds are checked on fewer shapes in test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the
+count (default 300, a few seconds)."""
+import os
+import random
+
+import pytest
+import torch
+
+from layer_harness import make_inputs, run_layer
+from moe_ffn_expert_gb300 import _abi
+from workloads import synth
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ("y", "dx", "d_topk_weights", "dW_up", "dW_down")
+
+
+def test_soak_schedules_agree_bit_for_bit():
+    n = int(os.environ.get("MM_SOAK_SHAPES", "300"))
+    rng = random.Random(777)
+    single, mcast = _abi.MM_FLAG_SINGLE_CTA_TILES, _abi.MM_FLAG_PAIRED_TILES
+    fused = (_abi.MM_FLAG_FUSED_COMBINE, _abi.MM_FLAG_FUSED_FORWARD_GEMMS,
+             _abi.MM_FLAG_FUSED_COMBINE | _abi.MM_FLAG_FUSED_FORWARD_GEMMS)
+    failures = []
+    for i in range(n):
+        E = rng.choice([1, 2, 3, 4, 6, 8, 13, 16, 32, 64, 96])
+        K = rng.randint(1, min(8, E))
+        T = rng.choice([1, 5, 64, 127, 128, 129, 255, 333, 777, 1000, 2048, 3001, 4096, 8192])
+        H = 8 * rng.randint(1, 128)
+        I = 8 * rng.randint(1, 64)
+        kind = rng.choice(["uniform", "zipf"])
+        ff = rng.choice(fused)
+        shape = (T, H, I, E, K, kind)
+        inp = make_inputs(synth.small("soak", T, H, I, E, K, routing_kind=kind, seed=5000 + i))
+        a = run_layer(inp)
+        runs = {"again": run_layer(inp),
+                "single": run_layer(inp, flags=single, bwd_flags=single),
+                "mcast": run_layer(inp, flags=mcast, bwd_flags=mcast)}
+        f = run_layer(inp, flags=ff, backward=False)
+        if a["status"] != _abi.MM_OK or f["status"] != _abi.MM_OK or \
+                any(r["status"] != _abi.MM_OK for r in runs.values()):
+            failures.append((shape, "status"))
+            continue
+        diffs = [f"{name}:{k}" for name, r in runs.items() for k in KEYS if not torch.equal(a[k], r[k])]
+        if not torch.equal(a["y"], f["y"]):
+            diffs.append(f"fused 0x{ff:x}: y")
+        if diffs:
+            failures.append((shape, diffs))
+    assert not failures, failures[:10]
