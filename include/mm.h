@@ -4,7 +4,7 @@
  * The operation is the one defined by the RFC "HyperParallel Multicore HyperMegaMoE fused
  * forward/backward operator": §2.1 (forward chain Dispatch -> GMM1/up_proj -> SwiGLU ->
  * GMM2/down_proj -> Combine), §2.2 (backward graph and its gradient list), §2.3 and §10
- * (the two-phase "query workspace size, then execute" split of the ACLNN interface), §3.1
+ * (the ACLNN interface's two phases: a workspace-size query, then the call), §3.1
  * (the five public tensors) and §4 (routing semantics and boundary checks). On one GPU the
  * AllToAll dispatch/combine become a permute/unpermute of rows inside device memory.
  *
