@@ -243,12 +243,15 @@ def _loss(x, ids, w, wu, wd, dy):
     return float((oracle.forward(x, ids, w, wu, wd) * dy).sum())
 
 
-def test_finite_difference_gradients():
+def _fd_failures():
+    """Central float64 finite differences of sum(y * dy) against the oracle's backward on a tiny
+    case; returns {gradient name: first mismatch} (empty when every sampled element agrees)."""
     T, H, I, E, K = 8, 16, 8, 4, 2
     x, ids, w, wu, wd, dy = _rand_case(T=T, H=H, I=I, E=E, K=K, seed=21)
     g = oracle.backward(x, ids, w, wu, wd, dy)
     eps = 1e-6
     gen = torch.Generator().manual_seed(0)
+    bad = {}
 
     def check(name, tensor, grad, n=25):
         flat = tensor.view(-1)
@@ -262,12 +265,19 @@ def test_finite_difference_gradients():
             flat[i] = old
             fd = (lp - lm) / (2 * eps)
             an = grad.reshape(-1)[i].item()
-            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, i, fd, an)
+            if abs(fd - an) > 1e-6 * max(1.0, abs(an)):
+                bad[name] = (i, fd, an)
+                return
 
     check("x", x, g["dx"])
     check("w", w, g["d_topk_weights"], n=T * K)
     check("w_up", wu, g["dW_up"], n=60)
     check("w_down", wd, g["dW_down"], n=40)
+    return bad
+
+
+def test_finite_difference_gradients():
+    assert _fd_failures() == {}
 
 
 # ------------------------------------------------------------------ sampled evaluation
@@ -311,6 +321,59 @@ def test_planted_gate_up_swap_is_caught(monkeypatch):
     y = oracle.forward(x, torch.zeros(T, 1, dtype=torch.int32), torch.ones(T, 1, dtype=F64),
                        torch.cat([wg, wu], 1)[None], wd[None])
     assert not torch.allclose(y, ref, rtol=1e-6, atol=1e-6)
+
+
+def _plant_silu_slope(moe_ffn):
+    # d_gate without the (1 + gate (1 - sigmoid)) factor of silu's derivative
+    def wrong(d_h, gate, up):
+        sg = torch.sigmoid(gate)
+        return d_h * up * sg, d_h * gate * sg
+    return "swiglu_grad", wrong
+
+
+def _plant_d_up_factor(moe_ffn):
+    # d_up = d_h * sigmoid(gate) instead of d_h * silu(gate)
+    def wrong(d_h, gate, up):
+        sg = torch.sigmoid(gate)
+        return d_h * up * sg * (1.0 + gate * (1.0 - sg)), d_h * sg
+    return "swiglu_grad", wrong
+
+
+def _plant_unweighted_w2grad(moe_ffn):
+    # W2Grad from the unweighted dY rows (the routing weight dropped)
+    orig = moe_ffn.expert_backward
+
+    def wrong(X, dY, w, w_up_e, w_down_e):
+        g = orig(X, dY, w, w_up_e, w_down_e)
+        h = moe_ffn.expert_forward(X, w_up_e, w_down_e)[2]
+        g["dW_down"] = h.T @ dY
+        return g
+    return "expert_backward", wrong
+
+
+def _plant_weighted_d_topk(moe_ffn):
+    # d_topk_weights scaled by the routing weight, as if dO were used instead of dY
+    orig = moe_ffn.expert_backward
+
+    def wrong(X, dY, w, w_up_e, w_down_e):
+        g = orig(X, dY, w, w_up_e, w_down_e)
+        g["d_topk"] = g["d_topk"] * w
+        return g
+    return "expert_backward", wrong
+
+
+@pytest.mark.parametrize("plant,caught_by", [(_plant_silu_slope, {"x", "w_up"}),
+                                             (_plant_d_up_factor, {"x", "w_up"}),
+                                             (_plant_unweighted_w2grad, {"w_down"}),
+                                             (_plant_weighted_d_topk, {"w"})])
+def test_planted_backward_mistakes_are_caught(monkeypatch, plant, caught_by):
+    """Each plausible slip in the backward's arithmetic, planted in the oracle, must fail the
+    finite-difference pin on the gradients it touches."""
+    from oracle import moe_ffn
+    name, wrong = plant(moe_ffn)
+    monkeypatch.setattr(moe_ffn, name, wrong)
+    bad = _fd_failures()
+    assert caught_by <= set(bad), (plant.__name__, sorted(bad))
 
 
 # ------------------------------------------------------------------ shared expert (RFC §6.1)
