@@ -61,8 +61,12 @@ typedef enum mm_status {
   MM_ERR_TOKENS_PER_EXPERT = 7 /* a caller's tokens_per_expert differs from the ids' histogram */
 } mm_status;
 
-/* Layer sizes. Supported: T >= 1, H and I multiples of 8 (16-byte rows), 1 <= E <= 1024,
- * 1 <= K <= 16, T*K + E*127 < 2^31. */
+/* Layer sizes. Supported: T >= 0, H and I multiples of 8 (16-byte rows), 1 <= E <= 1024,
+ * 1 <= K <= 16, T*K + E*127 < 2^31. An empty batch (T = 0) is a valid call: the pointers of
+ * T-sized tensors (x, topk_ids, topk_weights, y, dy, dx, d_topk_weights) may then be NULL, the
+ * forward leaves empty routing tables (a caller's tokens_per_expert must be all zero), and the
+ * backward writes zero weight gradients (leaves them unchanged with
+ * MM_FLAG_ACCUMULATE_WEIGHT_GRADS). */
 typedef struct mm_dims {
   int64_t T, H, I, E, K;
 } mm_dims;

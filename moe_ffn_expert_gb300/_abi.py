@@ -95,6 +95,7 @@ def _lib():
         "mm_timing_select": (st, [ctypes.c_uint32]),
         "mm_timing_read": (ctypes.c_int, [_P, _P, ctypes.c_int]),
         "mm_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
+        "mm_route_noalloc": (st, [mm_dims, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -173,6 +174,10 @@ def mm_get_status(workspace, stream=0) -> int:
 
 def mm_routing_export(d, workspace, counts, offsets, row_of_slot, stream=0) -> int:
     return int(_lib().mm_routing_export(d, workspace, counts, offsets, row_of_slot, stream))
+
+
+def mm_route_noalloc(d, topk_ids, counts, offsets, row_of_slot, stream=0) -> int:
+    return int(_lib().mm_route_noalloc(d, topk_ids, counts, offsets, row_of_slot, stream))
 
 
 def mm_status_string(status: int) -> str:

@@ -33,7 +33,7 @@ constexpr uint64_t kTestTimeoutNs = 50000000ull;       // with MM_FLAG_TEST_STAL
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool dims_ok(const mm_dims& d) {
-  if (d.T < 1 || d.H < 8 || d.I < 8 || d.E < 1 || d.K < 1) return false;
+  if (d.T < 0 || d.H < 8 || d.I < 8 || d.E < 1 || d.K < 1) return false;
   if (d.H % 8 || d.I % 8) return false;
   if (d.E > 1024 || d.K > 16) return false;
   if (d.T > (int64_t)1 << 31 || d.H > ((int64_t)1 << 20) || d.I > ((int64_t)1 << 20)) return false;
@@ -258,7 +258,7 @@ static bool plan_all(const mm_dims& d, int64_t shared_I, Plan* p) {
 
 static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, const void* ws,
                               size_t ws_bytes, Plan* p) {
-  if (d.T < 1 || d.H < 1 || d.I < 1 || d.E < 1 || d.K < 1) return MM_ERR_INVALID_ARG;
+  if (d.T < 0 || d.H < 1 || d.I < 1 || d.E < 1 || d.K < 1) return MM_ERR_INVALID_ARG;
   if (se != nullptr && se->I < 1) return MM_ERR_INVALID_ARG;
   if (!plan_all(d, se ? se->I : 0, p)) return MM_ERR_UNSUPPORTED;
   if (ws == nullptr || !aligned(ws, 256) || ws_bytes < p->total) return MM_ERR_WORKSPACE;
@@ -271,6 +271,67 @@ static int pair_mode(uint32_t flags) {
   return (flags & MM_FLAG_SINGLE_CTA_TILES) ? 0 : (flags & MM_FLAG_PAIRED_TILES) ? 1 : 2;
 }
 
+// An empty batch (T = 0): no slot to route or compute. The header and the routing tables are
+// written as empty (zero counts and offsets), and a caller's tokens_per_expert is still compared
+// with them by the scan kernel, which reads no chunk histogram when there is none.
+static mm_status forward_empty(const Plan& p, const mm_shared_expert* se, const int32_t* tpe,
+                               const void* up_proj_weight, const void* down_proj_weight,
+                               void* workspace, void* stream, uint32_t flags) {
+  const Workspace& w = p.w;
+  if (!up_proj_weight || !down_proj_weight || !aligned(up_proj_weight, 16) ||
+      !aligned(down_proj_weight, 16))
+    return MM_ERR_INVALID_ARG;
+  if (se && (!se->up_proj_weight || !se->down_proj_weight || !aligned(se->up_proj_weight, 16) ||
+             !aligned(se->down_proj_weight, 16)))
+    return MM_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = reinterpret_cast<char*>(workspace);
+  g_err[0] = 0;
+  MM_TRY(bind_context());
+  MM_TRY(cudaMemsetAsync(ws + w.off_hdr, 0, HDR_WORDS * sizeof(int32_t), st));
+  if (flags & MM_FLAG_FORWARD_ONLY)
+    MM_TRY(cudaMemsetAsync(ws + w.off_hdr + HDR_NO_BACKWARD * sizeof(int32_t), 1,
+                           sizeof(int32_t), st));
+  MM_TRY(timed(ST_ROUTE_SCAN, st, [&] { return launch_route_scan(w, ws, tpe, st); }));
+  if (flags & MM_FLAG_VALIDATE_IDS) {
+    int32_t status = 0;
+    MM_TRY(cudaMemcpyAsync(&status, ws + w.off_hdr, sizeof(status), cudaMemcpyDeviceToHost, st));
+    MM_TRY(cudaStreamSynchronize(st));
+    if (status != 0) return static_cast<mm_status>(status);
+  }
+  return MM_OK;
+}
+
+// The backward of an empty batch: every weight gradient is zero (written as zeros, or left as it
+// is when accumulating); dx and d_topk_weights have no element.
+static mm_status backward_empty(const Plan& p, const mm_shared_expert* se,
+                                const void* up_proj_weight, const void* down_proj_weight,
+                                void* d_up_proj_weight, void* d_down_proj_weight, void* stream,
+                                uint32_t flags) {
+  const Workspace& w = p.w;
+  if (!up_proj_weight || !down_proj_weight || !d_up_proj_weight || !d_down_proj_weight ||
+      !aligned(up_proj_weight, 16) || !aligned(down_proj_weight, 16) ||
+      !aligned(d_up_proj_weight, 16) || !aligned(d_down_proj_weight, 16))
+    return MM_ERR_INVALID_ARG;
+  if (se && (!se->up_proj_weight || !se->down_proj_weight || !se->d_up_proj_weight ||
+             !se->d_down_proj_weight || !aligned(se->d_up_proj_weight, 16) ||
+             !aligned(se->d_down_proj_weight, 16)))
+    return MM_ERR_INVALID_ARG;
+  if (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) return MM_OK;  // adding zero changes nothing
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  g_err[0] = 0;
+  MM_TRY(bind_context());
+  const size_t es = (flags & MM_FLAG_FP32_WEIGHT_GRADS) ? 4 : 2;
+  const size_t n_up = (size_t)w.E * w.H * 2 * w.I, n_down = (size_t)w.E * w.I * w.H;
+  MM_TRY(cudaMemsetAsync(d_up_proj_weight, 0, n_up * es, st));
+  MM_TRY(cudaMemsetAsync(d_down_proj_weight, 0, n_down * es, st));
+  if (se) {
+    MM_TRY(cudaMemsetAsync(se->d_up_proj_weight, 0, (size_t)w.H * 2 * se->I * es, st));
+    MM_TRY(cudaMemsetAsync(se->d_down_proj_weight, 0, (size_t)se->I * w.H * es, st));
+  }
+  return MM_OK;
+}
+
 static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32_t* tpe,
                               const void* x,
                               const int32_t* topk_ids, const float* topk_weights,
@@ -281,6 +342,8 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   mm_status s = check_common(d, se, workspace, workspace_bytes, &p);
   if (s != MM_OK) return s;
   const Workspace& w = p.w;
+  if (d.T == 0) return forward_empty(p, se, tpe, up_proj_weight, down_proj_weight, workspace,
+                                     stream, flags);
   if (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !y)
     return MM_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(up_proj_weight, 16) || !aligned(down_proj_weight, 16) ||
@@ -371,6 +434,9 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   mm_status s = check_common(d, se, workspace, workspace_bytes, &p);
   if (s != MM_OK) return s;
   const Workspace& w = p.w;
+  if (d.T == 0)
+    return backward_empty(p, se, up_proj_weight, down_proj_weight, d_up_proj_weight,
+                          d_down_proj_weight, stream, flags);
   if (!dy || !x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !dx ||
       !d_topk_weights || !d_up_proj_weight || !d_down_proj_weight)
     return MM_ERR_INVALID_ARG;
@@ -538,7 +604,7 @@ mm_status mm_routing_export(mm_dims d, const void* workspace, int32_t* counts, i
   if (offsets)
     MM_TRY(cudaMemcpyAsync(offsets, ws + w.off_offsets, (w.E + 1) * sizeof(int32_t),
                            cudaMemcpyDefault, st));
-  if (row_of_slot) {
+  if (row_of_slot && w.S > 0) {
     // converted into the backward-only p_part scratch, then copied out
     int32_t* tmp = reinterpret_cast<int32_t*>(const_cast<char*>(ws) + w.off_p_part);
     MM_TRY(launch_export_rows(w, ws, tmp, st));

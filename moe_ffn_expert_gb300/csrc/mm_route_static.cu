@@ -163,7 +163,16 @@ int32_t* scratch_ptr(mm_status* st) {
 
 extern "C" mm_status mm_route_noalloc(mm_dims d, const int32_t* topk_ids, int32_t* counts,
                                       int32_t* offsets, int32_t* row_of_slot, void* stream) {
-  if (d.T < 1 || d.K < 1 || d.E < 1) return MM_ERR_INVALID_ARG;
+  if (d.T < 0 || d.K < 1 || d.E < 1) return MM_ERR_INVALID_ARG;
+  if (d.T == 0) {  // no slot: empty tables (row_of_slot has no element and may be null)
+    if (!counts || !offsets) return MM_ERR_INVALID_ARG;
+    if (d.K > 16 || d.E > NA_MAX_E) return MM_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counts, 0, (size_t)d.E * sizeof(int32_t), s) != cudaSuccess ||
+        cudaMemsetAsync(offsets, 0, (size_t)(d.E + 1) * sizeof(int32_t), s) != cudaSuccess)
+      return MM_ERR_CUDA;
+    return MM_OK;
+  }
   if (!topk_ids || !counts || !offsets || !row_of_slot) return MM_ERR_INVALID_ARG;
   if (d.K > 16 || d.E > NA_MAX_E || d.T > NA_MAX_SLOTS || d.T * d.K > NA_MAX_SLOTS)
     return MM_ERR_UNSUPPORTED;  // beyond the static scratch: use mm_forward with a workspace

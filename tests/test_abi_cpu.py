@@ -35,7 +35,8 @@ def test_workspace_size_and_limits():
     assert _abi.mm_workspace_size(_abi.dims(16, 64, 36, 4, 2)) == 0      # I not a multiple of 8
     assert _abi.mm_workspace_size(_abi.dims(16, 64, 32, 1025, 2)) == 0   # E > 1024
     assert _abi.mm_workspace_size(_abi.dims(16, 64, 32, 4, 17)) == 0     # K > 16
-    assert _abi.mm_workspace_size(_abi.dims(0, 64, 32, 4, 2)) == 0
+    assert _abi.mm_workspace_size(_abi.dims(-1, 64, 32, 4, 2)) == 0     # negative T
+    assert _abi.mm_workspace_size(_abi.dims(0, 64, 32, 4, 2)) > 0       # an empty batch
     assert _abi.mm_workspace_size(_abi.dims(1, 8, 8, 1, 1)) > 0
 
 
