@@ -595,8 +595,7 @@ def main(argv=None):
                     help="mm_forward flags, e.g. 0x8 (one-launch forward GEMMs), 0x10 (combine in "
                          "GEMM2's epilogue), 0x100 (one CTA per tile instead of pair MMAs)")
     ap.add_argument("--bwd-flags", type=lambda v: int(v, 0), default=0,
-                    help="mm_backward flags, e.g. 0x100 (one CTA per tile instead of pair MMAs), "
-                         "0x40 (pairs sharing the weight tile by multicast instead)")
+                    help="mm_backward flags, e.g. 0x100 (one CTA per tile instead of pair MMAs)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--shared-intermediate", type=int, default=0,
                     help="add a shared expert of this intermediate size (0: none)")

@@ -107,18 +107,12 @@ typedef struct mm_dims {
  * MM_ERR_INVALID_ARG in the status word and its GEMMs do nothing (outputs unspecified). */
 #define MM_FLAG_FORWARD_ONLY 0x20u
 
-/* mm_forward / mm_backward flag: run GEMM1, GEMM2 (forward) and input_grad (backward) in clusters
- * of two CTAs that take two row tiles of the same expert and share its weight tile, each CTA
- * loading half of it into both CTAs' shared memory (TMA multicast). Results are identical bit for
- * bit. */
-#define MM_FLAG_PAIRED_TILES 0x40u
-
 /* mm_forward / mm_backward flag: one CTA per 128-row tile in every grouped GEMM. By default
  * GEMM1, GEMM2 (forward), act_grad and input_grad (backward), and the weight gradients when the
  * experts average at least 512 rows, run 256-row tiles shared by the two CTAs of a cluster through one
  * tensor-core MMA (tcgen05 .cta_group::2): each CTA holds its 128 rows of A and half of the
- * weight tile's columns, and receives its own rows of the accumulator. Takes precedence over
- * MM_FLAG_PAIRED_TILES. Results are identical bit for bit in every form. */
+ * weight tile's columns, and receives its own rows of the accumulator. Results are identical bit
+ * for bit in both forms. */
 #define MM_FLAG_SINGLE_CTA_TILES 0x100u
 
 /* mm_forward flag, a test hook for the failure path only: the first grouped GEMM withholds one

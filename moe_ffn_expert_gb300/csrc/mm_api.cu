@@ -265,11 +265,9 @@ static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, cons
   return MM_OK;
 }
 
-// CTA-pair form of the row-grouped GEMMs: 0 one CTA per tile, 1 pairs sharing the weight tile by
-// multicast loads, 2 (default) pairs sharing one M = 256 MMA.
-static int pair_mode(uint32_t flags) {
-  return (flags & MM_FLAG_SINGLE_CTA_TILES) ? 0 : (flags & MM_FLAG_PAIRED_TILES) ? 1 : 2;
-}
+// CTA-pair form of the row-grouped GEMMs: 0 one CTA per tile, 2 (default) pairs sharing one
+// M = 256 MMA.
+static int pair_mode(uint32_t flags) { return (flags & MM_FLAG_SINGLE_CTA_TILES) ? 0 : 2; }
 
 // An empty batch (T = 0): no slot to route or compute. The header and the routing tables are
 // written as empty (zero counts and offsets), and a caller's tokens_per_expert is still compared

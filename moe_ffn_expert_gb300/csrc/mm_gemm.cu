@@ -33,9 +33,9 @@
 // long weight gradients): two CTAs of a cluster share one 256 x 256 tcgen05.mma.cta_group::2 per
 // 16-deep step. Each holds its own 128 rows of A and half of B's columns (32 KB stages, six
 // deep; 48 KB and four deep for the split weight gradients), both CTAs' TMA loads complete on
-// the even CTA's stage barrier, the even CTA's MMA thread issues and multicasts its commits to
-// both CTAs, and each CTA's epilogue drains its own 128 accumulator rows. PAIR = 1 keeps one MMA
-// per CTA and only shares the weight tile by multicast loads.
+// the even CTA's stage barrier, the even CTA's MMA thread issues the MMAs and signals its
+// commits to both CTAs' barriers, and each CTA's epilogue drains its own 128 accumulator rows.
+// Every TMA load of a CTA writes only its own shared memory and reads only this GPU's memory.
 //
 // Warp roles (320 threads, one CTA per SM, grid <= SM count, static round-robin over tiles):
 //   warp 0      one thread issues TMA loads into a 4-stage (3 for act_grad and the weight
@@ -781,23 +781,22 @@ __device__ __forceinline__ void fused_combine_warp(const Args& a, const Tile& t,
 }
 
 
-// PAIR: 0 = one CTA per tile; 1 = clusters of two CTAs, each with its own MMA on its own row tile,
-// sharing the weight tile by multicast loads; 2 = clusters of two CTAs sharing one M = 256 MMA
-// (tcgen05 .cta_group::2): each CTA holds its 128 rows of A and half of B's columns, the even CTA
-// issues the MMAs, each CTA's tensor memory receives its own 128 accumulator rows.
+// PAIR: 0 = one CTA per tile; 2 = clusters of two CTAs sharing one M = 256 MMA (tcgen05
+// .cta_group::2): each CTA holds its 128 rows of A and half of B's columns, the even CTA issues
+// the MMAs, each CTA's tensor memory receives its own 128 accumulator rows.
 template <int KIND, int PAIR = 0>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmL, const __grid_constant__ EpiMaps em,
            const Args a) {
   using TR = Traits<KIND>;
-  constexpr bool PAIRED = PAIR != 0;
-  constexpr bool MMA2 = PAIR == 2;
+  static_assert(PAIR == 0 || PAIR == 2, "one CTA per tile, or CTA-pair MMAs");
+  constexpr bool PAIRED = PAIR == 2;
+  constexpr bool MMA2 = PAIRED;
   pdl_wait();  // the stream's previous kernels are complete (see mm_device.cuh)
   static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
-                    (MMA2 && (TR::WGRAD || KIND == GK_ACT_GRAD)),
-                "paired launches: GEMM1, GEMM2 and INPUT_GRAD; pair MMAs also act_grad and the "
-                "weight gradients");
+                    TR::WGRAD || KIND == GK_ACT_GRAD,
+                "pair MMAs: GEMM1, GEMM2, act_grad, input_grad and the weight gradients");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if constexpr (KIND == GK_ACT_GRAD) {
     // the forward on this workspace kept no gate|up (forward-only): no backward from it
@@ -861,7 +860,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIR == 1 ? 2 : 1);  // PAIR 1: both CTAs' MMAs release a stage
+      mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -898,7 +897,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // paired: both CTAs' barriers are initialised before either multicasts into the other
+  // paired: both CTAs' barriers are initialised before either signals the other's
   if constexpr (PAIRED) cluster_sync();
   const uint32_t tmem_base = *tmem_holder_ptr;
   const uint64_t tmo = a.timeout_ns;
@@ -978,25 +977,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tma_load_2d(sa, &tmA, full_bar(s), k0, t.m0);
           }
-          if constexpr (PAIRED) {
-            // this CTA's half of the shared B tile, multicast to both CTAs of the pair
-            constexpr uint16_t kBoth = 0x3;
-            if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
-              const int c0 = (rank ? a.I : 0) + t.n0;
-              tma_load_3d_mc(sb + (2 * rank + 0) * MN_BLOCK_BYTES, &tmB, full_bar(s), c0, k0, t.e,
-                             kBoth);
-              tma_load_3d_mc(sb + (2 * rank + 1) * MN_BLOCK_BYTES, &tmB, full_bar(s), c0 + 64, k0,
-                             t.e, kBoth);
-            } else if constexpr (KIND == GK_GEMM2) {  // rank r: column blocks 2r and 2r + 1
-#pragma unroll
-              for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)
-                tma_load_3d_mc(sb + j * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64 * j, k0, t.e,
-                               kBoth);
-            } else {  // INPUT_GRAD, K-major B of 256 rows: rank r loads rows 128r..128r+127
-              tma_load_3d_mc(sb + rank * (B_HALF_ROWS * 128), &tmB, full_bar(s), k0,
-                             t.n0 + B_HALF_ROWS * (int)rank, t.e, kBoth);
-            }
-          } else if constexpr (TR::FUSED) {
+          if constexpr (TR::FUSED) {
             if (t.part == 0) {
               tma_load_3d(sb + 0 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0, k0, t.e);
               tma_load_3d(sb + 1 * MN_BLOCK_BYTES, &tmB, full_bar(s), t.n0 + 64, k0, t.e);
@@ -1084,8 +1065,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if constexpr (MMA2)
             umma_commit_pair_mc(empty_bar(s), 0x3);  // both CTAs' producers refill this stage
-          else if constexpr (PAIRED)
-            umma_commit_mc(empty_bar(s), 0x3);  // both CTAs' producers wait on this stage
           else
             umma_commit(empty_bar(s));
         }
@@ -1311,7 +1290,7 @@ inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 template <int KIND, int PAIR = 0>
 cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
-  constexpr bool PAIRED = PAIR != 0;
+  constexpr bool PAIRED = PAIR == 2;
   cudaError_t err = set_smem_attr<KIND, PAIR>();
   if (err != cudaSuccess) return err;
   const int nsm = sm_count();
@@ -1579,20 +1558,14 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
   const int pair = c.paired;
   switch (c.kind) {
     case GK_GEMM1_SWIGLU:
-      return pair == 2   ? run<GK_GEMM1_SWIGLU, 2>(w, ws, c, st)
-             : pair == 1 ? run<GK_GEMM1_SWIGLU, 1>(w, ws, c, st)
-                         : run<GK_GEMM1_SWIGLU>(w, ws, c, st);
+      return pair == 2 ? run<GK_GEMM1_SWIGLU, 2>(w, ws, c, st) : run<GK_GEMM1_SWIGLU>(w, ws, c, st);
     case GK_GEMM2:
-      return pair == 2   ? run<GK_GEMM2, 2>(w, ws, c, st)
-             : pair == 1 ? run<GK_GEMM2, 1>(w, ws, c, st)
-                         : run<GK_GEMM2>(w, ws, c, st);
+      return pair == 2 ? run<GK_GEMM2, 2>(w, ws, c, st) : run<GK_GEMM2>(w, ws, c, st);
     case GK_GEMM2_COMBINE: return run<GK_GEMM2_COMBINE>(w, ws, c, st);
     case GK_ACT_GRAD:
       return pair == 2 ? run<GK_ACT_GRAD, 2>(w, ws, c, st) : run<GK_ACT_GRAD>(w, ws, c, st);
     case GK_INPUT_GRAD:
-      return pair == 2   ? run<GK_INPUT_GRAD, 2>(w, ws, c, st)
-             : pair == 1 ? run<GK_INPUT_GRAD, 1>(w, ws, c, st)
-                         : run<GK_INPUT_GRAD>(w, ws, c, st);
+      return pair == 2 ? run<GK_INPUT_GRAD, 2>(w, ws, c, st) : run<GK_INPUT_GRAD>(w, ws, c, st);
     case GK_W2_GRAD:
       return pair == 2 ? run<GK_W2_GRAD, 2>(w, ws, c, st) : run<GK_W2_GRAD>(w, ws, c, st);
     case GK_W1_GRAD:

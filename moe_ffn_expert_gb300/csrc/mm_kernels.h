@@ -46,6 +46,9 @@ cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const
 cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st);
 // d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]].
 cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st);
+// Records MM_ERR_INVALID_ARG in the status word if the forward kept no gate|up (forward only):
+// the check of a backward that launches no GEMM (T = 0).
+cudaError_t launch_backward_check(const Workspace& w, char* ws, cudaStream_t st);
 // Converts the padded row_of_slot table to positions in the unpadded expert-sorted order.
 cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out, cudaStream_t st);
 
@@ -77,9 +80,9 @@ struct GemmCall {
   // GEMM2 / fused forward: when comb_y is set, the weighted combine into comb_y runs in the
   // epilogue (the per-(token, 128-column chunk) counters at off_cnt must be zero)
   int skip_gu = 0;     // GEMM1 / fused forward: do not store gate|up (forward only)
-  int paired = 0;      // GEMM1 / GEMM2 / INPUT_GRAD on expert-sorted rows, clusters of two CTAs
-                       // over two row tiles of one expert: 1 = each CTA its own MMA, the weight
-                       // tile shared by multicast loads; 2 = one M = 256 MMA of the pair
+  int paired = 0;      // 2: clusters of two CTAs sharing one M = 256 MMA (row-grouped kinds: two
+                       // row tiles of one expert; weight gradients: two row tiles of the weight);
+                       // 0: one CTA per tile
   void* comb_y = nullptr;
   const float* comb_w = nullptr;
   const void* comb_extra = nullptr;

@@ -223,26 +223,23 @@ SINGLE = _abi.MM_FLAG_SINGLE_CTA_TILES
                                        (300, 256, 128, 40, 2),   # many experts with one tile
                                        (2000, 136, 72, 3, 2),    # paired weight gradients, ragged:
                                        (1500, 200, 200, 2, 1)])  # odd weight row tiles, B halves past N
-@pytest.mark.parametrize("flags", [0, _abi.MM_FLAG_PAIRED_TILES])
-def test_paired_tiles_equal_single_tiles(T, H, I, E, K, flags):
+def test_paired_tiles_equal_single_tiles(T, H, I, E, K):
     """The default pair MMAs (two row tiles of one expert, or two weight row tiles, as one
-    M = 256 tcgen05 MMA of a CTA pair) and MM_FLAG_PAIRED_TILES (two CTAs sharing the weight tile
-    by multicast loads) give outputs identical bit for bit to one CTA per tile."""
+    M = 256 tcgen05 MMA of a CTA pair) give outputs identical bit for bit to one CTA per tile."""
     w = synth.small("pair", T, H, I, E, K, seed=T + 7)
     inp = make_inputs(w)
     ref = run_layer(inp, flags=SINGLE, bwd_flags=SINGLE)
-    out = run_layer(inp, flags=flags, bwd_flags=flags)
+    out = run_layer(inp)
     assert out["status"] == _abi.MM_OK and ref["status"] == _abi.MM_OK
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(out[k], ref[k]), k
 
 
-@pytest.mark.parametrize("flags", [0, _abi.MM_FLAG_PAIRED_TILES])
-def test_paired_tiles_on_the_skew_workload(flags):
+def test_paired_tiles_on_the_skew_workload():
     w = synth.BY_NAME["skew"]
     inp = make_inputs(w)
     ref = run_layer(inp, flags=SINGLE, bwd_flags=SINGLE)
-    out = run_layer(inp, flags=flags, bwd_flags=flags)
+    out = run_layer(inp)
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(out[k], ref[k]), k
 

@@ -1,5 +1,5 @@
 """Many seeded random shapes, bit for bit: the default launches twice (run-to-run determinism),
-against the one-CTA launches, the multicast-pair launches, and a forward with the fused combine
+against the one-CTA launches, and a forward with the fused combine
 and/or the one-launch GEMM1 -> GEMM2 form. Different schedules of the same arithmetic must give
 the same bits, so a race or an unwritten read in any of them shows up as a difference. The
 oracle bounds are checked on fewer shapes in test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the
@@ -22,7 +22,7 @@ KEYS = ("y", "dx", "d_topk_weights", "dW_up", "dW_down")
 def test_soak_schedules_agree_bit_for_bit():
     n = int(os.environ.get("MM_SOAK_SHAPES", "300"))
     rng = random.Random(777)
-    single, mcast = _abi.MM_FLAG_SINGLE_CTA_TILES, _abi.MM_FLAG_PAIRED_TILES
+    single = _abi.MM_FLAG_SINGLE_CTA_TILES
     fused = (_abi.MM_FLAG_FUSED_COMBINE, _abi.MM_FLAG_FUSED_FORWARD_GEMMS,
              _abi.MM_FLAG_FUSED_COMBINE | _abi.MM_FLAG_FUSED_FORWARD_GEMMS)
     failures = []
@@ -38,8 +38,7 @@ def test_soak_schedules_agree_bit_for_bit():
         inp = make_inputs(synth.small("soak", T, H, I, E, K, routing_kind=kind, seed=5000 + i))
         a = run_layer(inp)
         runs = {"again": run_layer(inp),
-                "single": run_layer(inp, flags=single, bwd_flags=single),
-                "mcast": run_layer(inp, flags=mcast, bwd_flags=mcast)}
+                "single": run_layer(inp, flags=single, bwd_flags=single)}
         f = run_layer(inp, flags=ff, backward=False)
         if a["status"] != _abi.MM_OK or f["status"] != _abi.MM_OK or \
                 any(r["status"] != _abi.MM_OK for r in runs.values()):
