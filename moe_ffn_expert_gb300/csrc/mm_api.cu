@@ -301,24 +301,27 @@ static mm_status forward_empty(const Plan& p, const mm_shared_expert* se, const 
 }
 
 // The backward of an empty batch: every weight gradient is zero (written as zeros, or left as it
-// is when accumulating); dx and d_topk_weights have no element.
+// is when accumulating); dx and d_topk_weights have no element. A workspace whose forward was
+// forward-only is refused through the status word, as for T > 0.
 static mm_status backward_empty(const Plan& p, const mm_shared_expert* se,
                                 const void* up_proj_weight, const void* down_proj_weight,
-                                void* d_up_proj_weight, void* d_down_proj_weight, void* stream,
-                                uint32_t flags) {
+                                void* d_up_proj_weight, void* d_down_proj_weight, void* workspace,
+                                void* stream, uint32_t flags) {
   const Workspace& w = p.w;
   if (!up_proj_weight || !down_proj_weight || !d_up_proj_weight || !d_down_proj_weight ||
       !aligned(up_proj_weight, 16) || !aligned(down_proj_weight, 16) ||
       !aligned(d_up_proj_weight, 16) || !aligned(d_down_proj_weight, 16))
     return MM_ERR_INVALID_ARG;
   if (se && (!se->up_proj_weight || !se->down_proj_weight || !se->d_up_proj_weight ||
-             !se->d_down_proj_weight || !aligned(se->d_up_proj_weight, 16) ||
+             !se->d_down_proj_weight || !aligned(se->up_proj_weight, 16) ||
+             !aligned(se->down_proj_weight, 16) || !aligned(se->d_up_proj_weight, 16) ||
              !aligned(se->d_down_proj_weight, 16)))
     return MM_ERR_INVALID_ARG;
-  if (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) return MM_OK;  // adding zero changes nothing
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   g_err[0] = 0;
   MM_TRY(bind_context());
+  MM_TRY(launch_backward_check(w, reinterpret_cast<char*>(workspace), st));
+  if (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) return MM_OK;  // adding zero changes nothing
   const size_t es = (flags & MM_FLAG_FP32_WEIGHT_GRADS) ? 4 : 2;
   const size_t n_up = (size_t)w.E * w.H * 2 * w.I, n_down = (size_t)w.E * w.I * w.H;
   MM_TRY(cudaMemsetAsync(d_up_proj_weight, 0, n_up * es, st));
@@ -434,7 +437,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   const Workspace& w = p.w;
   if (d.T == 0)
     return backward_empty(p, se, up_proj_weight, down_proj_weight, d_up_proj_weight,
-                          d_down_proj_weight, stream, flags);
+                          d_down_proj_weight, workspace, stream, flags);
   if (!dy || !x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !dx ||
       !d_topk_weights || !d_up_proj_weight || !d_down_proj_weight)
     return MM_ERR_INVALID_ARG;

@@ -427,6 +427,13 @@ __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts
   }
 }
 
+// A backward with no slot to compute (T = 0) still refuses a workspace whose forward kept no
+// gate|up (MM_FLAG_FORWARD_ONLY), as the act_grad kernel does when T > 0.
+__global__ void k_backward_check(int* hdr) {
+  pdl_wait();
+  if (hdr[HDR_NO_BACKWARD] != 0) set_status(hdr + HDR_STATUS, MM_ERR_INVALID_ARG);
+}
+
 inline unsigned div_up(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
 
 }  // namespace
@@ -492,6 +499,10 @@ cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStrea
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
                     region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
                     region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
+}
+
+cudaError_t launch_backward_check(const Workspace& w, char* ws, cudaStream_t st) {
+  return launch_pdl(k_backward_check, 1, 1, 0, st, region<int>(ws, w.off_hdr));
 }
 
 cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out, cudaStream_t st) {

@@ -12,11 +12,16 @@
 // (NA_SCRATCH_BYTES below); every call shares it, so calls whose kernels overlap on the
 // GPU (two streams, or two host threads) race on it. Host code cannot use the array's
 // name as a device address: the first call on each device looks the address up with
-// cudaGetSymbolAddress (that first call must happen before any stream capture).
+// cudaGetSymbolAddress (that first call must happen before any stream capture). Every call
+// first makes the current device's primary context current on the calling thread, so the
+// address it looked up and the kernels it launches belong to the same context.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mm.h"
+#include "mm_kernels.h"
 
 namespace {
 
@@ -139,24 +144,39 @@ __global__ void __launch_bounds__(128) k_na_rank(const int32_t* __restrict__ ids
   }
 }
 
-// Device address of g_route_scratch for each device, looked up once per device.
+// Records the failing step and CUDA error for mm_last_error_detail; returns MM_ERR_CUDA.
+mm_status fail(const char* step, cudaError_t e) {
+  mm::note_error("mm_route_noalloc: %s: %s (%s)", step, cudaGetErrorString(e), cudaGetErrorName(e));
+  return MM_ERR_CUDA;
+}
+
+// Makes the current device's primary context current on this thread (the one the scratch
+// address below belongs to) and returns the device address of g_route_scratch on it, looked up
+// once per device. Concurrent first calls may both look it up; they store the same address.
 int32_t* scratch_ptr(mm_status* st) {
-  static int32_t* cache[64] = {nullptr};
+  static std::atomic<int32_t*> cache[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    *st = MM_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && (dev < 0 || dev >= 64)) e = cudaErrorInvalidDevice;
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  if (e != cudaSuccess) {
+    *st = fail("device / context", e);
     return nullptr;
   }
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) {
-      *st = MM_ERR_CUDA;
+  int32_t* p = cache[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void* q = nullptr;
+    e = cudaGetSymbolAddress(&q, g_route_scratch);
+    if (e == cudaSuccess && q == nullptr) e = cudaErrorInvalidSymbol;
+    if (e != cudaSuccess) {
+      *st = fail("cudaGetSymbolAddress of the scratch array", e);
       return nullptr;
     }
-    cache[dev] = static_cast<int32_t*>(p);
+    p = static_cast<int32_t*>(q);
+    cache[dev].store(p, std::memory_order_release);
   }
   *st = MM_OK;
-  return cache[dev];
+  return p;
 }
 
 }  // namespace
@@ -164,13 +184,18 @@ int32_t* scratch_ptr(mm_status* st) {
 extern "C" mm_status mm_route_noalloc(mm_dims d, const int32_t* topk_ids, int32_t* counts,
                                       int32_t* offsets, int32_t* row_of_slot, void* stream) {
   if (d.T < 0 || d.K < 1 || d.E < 1) return MM_ERR_INVALID_ARG;
+  mm::note_error("");
   if (d.T == 0) {  // no slot: empty tables (row_of_slot has no element and may be null)
     if (!counts || !offsets) return MM_ERR_INVALID_ARG;
     if (d.K > 16 || d.E > NA_MAX_E) return MM_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail("device / context", e);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(counts, 0, (size_t)d.E * sizeof(int32_t), s) != cudaSuccess ||
-        cudaMemsetAsync(offsets, 0, (size_t)(d.E + 1) * sizeof(int32_t), s) != cudaSuccess)
-      return MM_ERR_CUDA;
+    if ((e = cudaMemsetAsync(counts, 0, (size_t)d.E * sizeof(int32_t), s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(offsets, 0, (size_t)(d.E + 1) * sizeof(int32_t), s)) != cudaSuccess)
+      return fail("clearing the empty tables", e);
     return MM_OK;
   }
   if (!topk_ids || !counts || !offsets || !row_of_slot) return MM_ERR_INVALID_ARG;
@@ -188,10 +213,13 @@ extern "C" mm_status mm_route_noalloc(mm_dims d, const int32_t* topk_ids, int32_
   const unsigned grid = (unsigned)((n_chunks + 3) / 4);
   const size_t smem = 4 * (size_t)E * sizeof(int32_t);
   // the status word must start at zero; the histograms are fully rewritten by each call
-  if (cudaMemsetAsync(scratch, 0, NA_HDR_WORDS * sizeof(int32_t), s) != cudaSuccess)
-    return MM_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(scratch, 0, NA_HDR_WORDS * sizeof(int32_t), s);
+  if (e != cudaSuccess) return fail("clearing the status word", e);
   k_na_count<<<grid, 128, smem, s>>>(topk_ids, scratch, S, E, n_chunks);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail("count kernel launch", e);
   k_na_scan<<<1, 1024, 0, s>>>(scratch, counts, offsets, E, n_chunks);
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail("scan kernel launch", e);
   k_na_rank<<<grid, 128, smem, s>>>(topk_ids, scratch, row_of_slot, S, E, n_chunks);
-  return cudaGetLastError() == cudaSuccess ? MM_OK : MM_ERR_CUDA;
+  if ((e = cudaGetLastError()) != cudaSuccess) return fail("rank kernel launch", e);
+  return MM_OK;
 }

@@ -82,6 +82,15 @@ def test_extended_entry_points_host_checks():
                               16, 256, n, 0, 0) == _abi.MM_ERR_WORKSPACE
     assert _abi.mm_forward_ex(d, _abi.options(None, 18), 16, 16, 16, 16, 16, 16, 256, n, 0,
                               0) == _abi.MM_ERR_INVALID_ARG
+    # an empty batch checks the shared expert's weights as a full one does
+    d0 = _abi.dims(0, 64, 32, 4, 2)
+    n0 = _abi.mm_workspace_size_ex(d0, _abi.options(_abi.shared_expert(48, 16, 16)))
+    for up, down in ((24, 16), (16, 24), (0, 16)):
+        opt = _abi.options(_abi.shared_expert(48, up, down, 16, 16))
+        assert _abi.mm_backward_ex(d0, opt, 0, 0, 0, 0, 16, 16, 256, n0, 0, 0, 16, 16, 0,
+                                   0) == _abi.MM_ERR_INVALID_ARG, (up, down)
+        assert _abi.mm_forward_ex(d0, opt, 0, 0, 0, 16, 16, 0, 256, n0, 0,
+                                  0) == _abi.MM_ERR_INVALID_ARG, (up, down)
 
 
 def test_stage_table():

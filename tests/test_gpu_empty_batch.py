@@ -75,6 +75,26 @@ def test_empty_batch_tokens_per_expert():
         assert _abi.mm_forward_ex(*args, _abi.MM_FLAG_VALIDATE_IDS) == expect
 
 
+def test_empty_batch_backward_after_forward_only():
+    """A backward on the workspace of a forward-only empty batch is refused through the status
+    word, as it is for T > 0; after a training forward the same workspace is accepted again."""
+    H, I, E, K = 256, 128, 6, 2
+    wts = _weights(H, I, E)
+    d = _abi.dims(0, H, I, E, K)
+    n = _abi.mm_workspace_size(d)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    wu, wd = wts["wu"], wts["wd"]
+    du, dd = torch.empty_like(wu), torch.empty_like(wd)
+    for fflags, expect in ((_abi.MM_FLAG_FORWARD_ONLY, _abi.MM_ERR_INVALID_ARG), (0, _abi.MM_OK)):
+        for bflags in (0, _abi.MM_FLAG_ACCUMULATE_WEIGHT_GRADS):
+            assert _abi.mm_forward(d, 0, 0, 0, wu.data_ptr(), wd.data_ptr(), 0, ws.data_ptr(), n,
+                                   st, fflags) == _abi.MM_OK
+            assert _abi.mm_backward(d, 0, 0, 0, 0, wu.data_ptr(), wd.data_ptr(), ws.data_ptr(), n,
+                                    0, 0, du.data_ptr(), dd.data_ptr(), st, bflags) == _abi.MM_OK
+            assert _abi.mm_get_status(ws.data_ptr(), st) == expect, (fflags, bflags)
+
+
 def test_empty_batch_noalloc_routing():
     E = 5
     counts = torch.full((E,), -1, dtype=torch.int32, device="cuda")
