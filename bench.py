@@ -53,17 +53,23 @@ def source_digest():
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(stage, workload):
-    """DRAM bytes per launch from a committed ncu summary, valid only for the current sources."""
+def profiled_traffic(stage, w):
+    """DRAM bytes per launch of `stage` on workload `w`, from a committed ncu capture of one
+    kernel on a smaller case with the same H, I, K and rows per expert (profiles/traffic.json),
+    scaled by the ratio of slots (the same as the ratio of experts). None unless the capture was
+    taken from the current sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(f"{workload}/{stage}")
+    e = d.get("captures", {}).get(stage)
     if not e or e.get("source") != source_digest():
         return None
-    return e.get("dram_bytes_per_launch")
+    c = e["case"]
+    if (c["H"], c["I"], c["K"]) != (w.H, w.I, w.K) or c["T"] * c["K"] * w.E != w.T * w.K * c["E"]:
+        return None
+    return int(round((e["dram_read"] + e["dram_write"]) * w.E / c["E"]))
 
 
 def workload_of(args):
@@ -403,14 +409,24 @@ def run_gpu(args):
     top_flops = GEMM_FLOPS_PER_SLOT[top] * hi * S
     achieved = top_flops / (avg_ms / 1e3) / 1e12
 
-    # HBM-bound stages: algorithmic bytes per launch / event-timed duration, against the measured
-    # copy bandwidth (routing, dispatch and combine rows; act_grad's row planes and weights)
-    Hb, Ib = 2 * H, 2 * I
+    # HBM-bound stages: algorithmic bytes per launch (the least DRAM traffic the step's
+    # definition needs: every input read once, every output written once, at the definition's
+    # dtypes) / event-timed duration, against the measured copy bandwidth
+    Hb = 2 * H
     algo_bytes = {
-        "gather_x": 2 * S * Hb, "gather_dy": 2 * S * Hb,
+        # the token rows read once (the K reads of a row after the first hit L2), the slot rows
+        # written once
+        "gather_x": T * Hb + S * Hb, "gather_dy": T * Hb + S * Hb,
+        # the slot rows, routing index and weight read, the token rows written
         "combine_y": S * Hb + T * Hb + 8 * S, "combine_dx": S * Hb + T * Hb + 4 * S,
-        "act_grad": S * (20 * I + Hb) + E * I * Hb,
+        # in: dy slot rows, bf16 gate|up, W_down, routing weight; out: bf16 [d_gate|d_up],
+        # bf16 w*h and one fp32 <g,h> per slot
+        "act_grad": S * (Hb + 4 * I + 4) + E * I * Hb + S * (4 * I + 2 * I + 4),
     }
+    # what this build's act_grad moves by design: fp32 gate|up in, and [d_gate|d_up] and w*h as
+    # bf16 hi + lo pairs out (the weight gradients' precision), plus one partial per column half
+    impl_bytes = {"act_grad": S * (Hb + 8 * I + 4) + E * I * Hb
+                  + S * (8 * I + 4 * I + 4 * 2 * ((I + 255) // 256))}
     hbm_peak = peaks["hbm_gbs"]
     hbm_stages = {}
     for k, nbytes_k in algo_bytes.items():
@@ -419,10 +435,16 @@ def run_gpu(args):
             gbs = nbytes_k / (ms_k / n_k / 1e3) / 1e9
             hbm_stages[k] = {"GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 3),
                              "bytes_per_launch": int(nbytes_k)}
-    hbm_stages["note"] = ("algorithmic bytes / average launch time, against the measured copy "
-                          "bandwidth; combine_dx runs beside w1_grad on a second stream; a gather "
-                          "reads each token row once per slot (K times), mostly from L2 when the "
-                          "token rows fit there, so its rate can pass the copy bandwidth")
+            if k in impl_bytes:
+                gi = impl_bytes[k] / (ms_k / n_k / 1e3) / 1e9
+                hbm_stages[k].update({"impl_bytes_per_launch": int(impl_bytes[k]),
+                                      "impl_GB/s": round(gi, 1),
+                                      "impl_frac": round(gi / hbm_peak, 3)})
+    hbm_stages["note"] = ("algorithmic bytes (each input read once and each output written once, "
+                          "at the layer definition's dtypes) / average launch time, against the "
+                          "measured copy bandwidth; impl_*: the bytes this build's act_grad moves "
+                          "by design (fp32 gate|up, bf16 hi + lo output pairs); combine_dx runs "
+                          "beside w1_grad on a second stream")
 
     # CPU baseline: the oracle on a bounded sample of this workload
     cpu = (cpu_baseline(w, args.cpu_budget, (wu, wd)) if args.cpu_budget > 0 and not I_s
@@ -451,7 +473,10 @@ def run_gpu(args):
                    "parallelism": "single GPU" if world == 1 else f"{world} independent replicas"},
         "tflops": round(tflops, 2),
         "frac_of_bf16_peak": {"burst": round(tflops / peak_burst, 4),
-                              "sustained": round(tflops / peak_sus, 4), "peaks": peak_src},
+                              "sustained": round(tflops / peak_sus, 4), "peaks": peak_src,
+                              "note": "burst: the peak of a GEMM timed alone at full clock, the "
+                                      "denominator for short timed regions; sustained: a "
+                                      "seconds-long GEMM loop under the power cap"},
         "fwd": {"ms": round(fwd_ms, 4), "tokens_per_s": round(T / (fwd_ms / 1e3), 1),
                 "tflops": round(flops["fwd"] / (fwd_ms / 1e3) / 1e12, 2)},
         "fwd_inference": {"ms": round(infer_ms, 4),
@@ -467,11 +492,15 @@ def run_gpu(args):
         "stages_ms_per_step": {k: round(v, 4) for k, v in stage_ms.items()},
         "hbm_stages": hbm_stages,
         "roofline": {"kernel": top, "bound": "tensor", "achieved": round(achieved, 2),
-                     "peak": peak_sus, "unit": "TFLOP/s", "frac": round(achieved / peak_sus, 4),
-                     "peak_kind": f"bf16 sustained ({peak_src})",
-                     "traffic": profiled_traffic(top, w.name),
+                     "peak": peak_burst, "unit": "TFLOP/s", "frac": round(achieved / peak_burst, 4),
+                     "peak_kind": f"bf16 burst ({peak_src})",
+                     "frac_of_sustained": round(achieved / peak_sus, 4),
+                     "flops_per_launch": int(top_flops),
+                     "ms_per_launch": round(avg_ms, 4),
+                     "traffic": profiled_traffic(top, w),
                      **({"executed_tflops": round(2 * achieved, 2),
-                         "executed_frac": round(2 * achieved / peak_sus, 4),
+                         "executed_frac": round(2 * achieved / peak_burst, 4),
+                         "executed_frac_of_sustained": round(2 * achieved / peak_sus, 4),
                          "executed_note": "the weight gradients issue two MMAs per k-step (bf16 hi "
                                           "and lo planes of the split operand): twice the "
                                           "algorithmic FLOPs"}

@@ -2,9 +2,12 @@
 
 Routing is compared bit for bit; y, dx and the weight gradients within
 |gpu - oracle| <= 1e-2 + 1e-2 |oracle|; d_topk_weights within 2e-2 * max(|oracle|, rms).
-The three smaller workloads are compared in full; the two large ones (the launch
-configuration the benchmark times) on sampled tokens and experts that the oracle computes
-one by one."""
+The tiny, skew, tail and qwen workloads are compared in full, every token and every expert,
+qwen (the benchmark's workload, in its launch configuration) also with the counter-fused forward
+forms; large_hidden on all of its hot experts, eight seeded cold experts and 256 seeded tokens,
+which the oracle computes one by one."""
+import functools
+
 import pytest
 import torch
 
@@ -29,15 +32,26 @@ def _check_routing(out, ids, E):
     assert torch.equal(g_rows.long(), row_of_slot)
 
 
-def _check_full(inp, out):
+def _oracle_full(inp):
     h = _host(inp)
     y = oracle.forward(h["x"], h["topk_ids"], h["topk_weights"], h["w_up"], h["w_down"])
     g = oracle.backward(h["x"], h["topk_ids"], h["topk_weights"], h["w_up"], h["w_down"], h["dy"])
-    assert_close("y", out["y"], y)
-    assert_close("dx", out["dx"], g["dx"])
+    return y, g
+
+
+def _compare_full(out, y, g, tag=""):
+    """Every element; the weight gradients one expert at a time (bounded host memory)."""
+    assert_close("y" + tag, out["y"], y)
+    assert_close("dx" + tag, out["dx"], g["dx"])
     assert_dtopk(out["d_topk_weights"], g["d_topk_weights"])
-    assert_close("dW_down", out["dW_down"], g["dW_down"])
-    assert_close("dW_up", out["dW_up"], g["dW_up"])
+    for e in range(g["dW_up"].shape[0]):
+        assert_close(f"dW_down[{e}]" + tag, out["dW_down"][e], g["dW_down"][e])
+        assert_close(f"dW_up[{e}]" + tag, out["dW_up"][e], g["dW_up"][e])
+
+
+def _check_full(inp, out):
+    y, g = _oracle_full(inp)
+    _compare_full(out, y, g)
 
 
 def _check_sampled(inp, out, n_tokens, experts, seed=0):
@@ -87,15 +101,46 @@ def test_workload_full_parity(name):
         assert torch.count_nonzero(out["dW_down"][14:]) == 0
 
 
-@pytest.mark.parametrize("name,n_tokens,experts", [("qwen", 48, [0, 77, 127]),
-                                                   ("large_hidden", 12, [3, 200])])
-def test_workload_sampled_parity(name, n_tokens, experts):
-    w = synth.BY_NAME[name]
+@functools.lru_cache(maxsize=1)
+def _qwen_reference():
+    """The oracle's outputs over the whole qwen workload (its inputs drawn on the device, which
+    gives the host generator's values bit for bit, and copied to the host)."""
+    w = synth.BY_NAME["qwen"]
+    y, g = _oracle_full(make_inputs(w))
+    torch.cuda.empty_cache()
+    return w, y, g
+
+
+@pytest.mark.parametrize("fwd_flags", [0, _abi.MM_FLAG_FUSED_FORWARD_GEMMS | _abi.MM_FLAG_FUSED_COMBINE],
+                         ids=["default", "counter_fused_forward"])
+def test_qwen_full_parity(fwd_flags):
+    """The benchmark's workload (T=16384, H=2048, I=768, E=128, K=8) in the benchmark's launch
+    configuration, and with GEMM2 released by the ready counters and the combine fused into its
+    epilogue: routing bit for bit, and y, dx, d_topk_weights and both weight gradients of all
+    128 experts against the float64 oracle, element by element."""
+    w, y, g = _qwen_reference()
+    inp = make_inputs(w)
+    out = run_layer(inp, flags=fwd_flags)
+    assert out["status"] == _abi.MM_OK
+    _check_routing(out, inp["topk_ids"], w.E)
+    _compare_full(out, y, g, tag=f" (forward flags 0x{fwd_flags:x})")
+    del out, inp
+    torch.cuda.empty_cache()
+
+
+def test_large_hidden_sampled_parity():
+    """T=8192, H=7168, I=2048, E=256, K=8 (22.5 GB of expert weights), 25 % of the slots on the
+    hot experts 0..7: routing bit for bit; the weight gradients of all eight hot experts and of
+    eight seeded cold ones, and y, dx, d_topk_weights of 256 seeded tokens (plus the first and
+    the last), against the oracle."""
+    w = synth.BY_NAME["large_hidden"]
     inp = make_inputs(w)
     out = run_layer(inp)
     assert out["status"] == _abi.MM_OK
     _check_routing(out, inp["topk_ids"], w.E)
-    _check_sampled(inp, out, n_tokens, experts)
+    gen = torch.Generator().manual_seed(4)
+    cold = (8 + torch.randperm(w.E - 8, generator=gen)[:8]).sort().values.tolist()
+    _check_sampled(inp, out, 256, list(range(8)) + cold, seed=4)
     del out, inp
     torch.cuda.empty_cache()
 
