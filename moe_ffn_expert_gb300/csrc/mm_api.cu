@@ -402,7 +402,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
     MM_TRY(cudaMemsetAsync(ws + w.off_cnt, 0,
                            (size_t)w.T * ((w.H + 127) / 128) * sizeof(int32_t), st));
     c.comb_y = y;
-    c.comb_w = topk_weights;
+    c.comb_w = nullptr;  // GEMM2's rows already carry the routing weight
     c.comb_extra = extra;
     c.comb_extra_lo = extra_lo;
   }
@@ -420,7 +420,8 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   }
   if (!fuse_combine)
     MM_TRY(timed(ST_COMBINE_Y, st, [&] {
-      return launch_combine(w, ws, ws + w.off_o, topk_weights, y, st, extra, extra_lo, true);
+      // GEMM2's rows already carry the routing weight (GEMM1 wrote w*h): an unweighted sum
+      return launch_combine(w, ws, ws + w.off_o, nullptr, y, st, extra, extra_lo, true);
     }));
   return MM_OK;
 }

@@ -5,20 +5,24 @@
 // act_grad, input_grad, W2Grad and W1Grad), every one on 128 x 256 accumulator tiles:
 //
 //   kind          A (rows x red.)            B (red. x cols)              epilogue
-//   GEMM1         x_slot [rows,H]  K-maj     W_up[e]   [H,2I]  N-major    gu = [gate|up] (fp32), h
-//   GEMM2         h      [rows,I]  K-maj     W_down[e] [I,H]   N-major    o (bf16; hi + lo if split)
-//   ACT_GRAD      dy_slot[rows,H]  K-maj     W_down[e]^T       K-major    SwiGLU backward: dgu, hw, <g,h>
+//   GEMM1         x_slot [rows,H]  K-maj     W_up[e]   [H,2I]  N-major    gu = [gate|up] (fp32), w*h
+//   GEMM2         w*h    [rows,I]  K-maj     W_down[e] [I,H]   N-major    w*o (bf16; hi + lo if split)
+//   ACT_GRAD      dy_slot[rows,H]  K-maj     W_down[e]^T       K-major    SwiGLU backward: dgu, <g,h>
 //   INPUT_GRAD    dgu    [rows,2I] K-maj     W_up[e]^T         K-major    dx_slot (bf16)
 //   W2_GRAD       hw_e^T [I,M_e]   M-maj x2  dy_slot_e [M_e,H] N-major    dW_down[e]
 //   W1_GRAD       dgu_e^T[2I,M_e]  M-maj x2  x_slot_e [M_e,H]  N-major    dW_up[e] (stored transposed)
 //   FWD_FUSED     GEMM1 and GEMM2 tiles in one launch (GEMM2 row blocks released by counters)
 //   GEMM2_COMBINE GEMM2 whose epilogue also sums y for the tokens whose last slot it stores
 //
+// The routing weight w of a row is applied where its h is made: GEMM1's epilogue writes w*h, so
+// GEMM2 gives the weighted expert output w*o and the combine sums a token's rows with weight 1
+// (the same products, one rounding of w*h instead of h; the RFC's weighted merge, §4.1).
+//
 // Precision of the weight gradients. They reduce over all rows of an expert (hundreds to
 // thousands), so a bf16 rounding of every row of an operand would leave errors of ~0.5% of the
-// gradient's rms. The forward therefore keeps the gate|up accumulators in fp32, and the
-// act_grad epilogue writes w*h and [d_gate|d_up] as two bf16 planes, hi = bf16(v) and
-// lo = bf16(v - hi), which together carry ~16 mantissa bits. Both weight gradients put that pair
+// gradient's rms. The forward therefore keeps the gate|up accumulators in fp32 and writes w*h,
+// and the act_grad epilogue [d_gate|d_up], as two bf16 planes, hi = bf16(v) and
+// lo = bf16(v - hi), which together carry ~16 mantissa bits (GEMM2 and input_grad read hi only). Both weight gradients put that pair
 // on the A side ("x2" above) and issue two MMAs per k-step (hi and lo against the same B tile)
 // into one fp32 accumulator; W1_GRAD therefore computes dW_up^T and its epilogue transposes.
 // Their stages hold A hi, A lo and B: 64 KB, three of them.
@@ -69,12 +73,12 @@ constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int BAR_BYTES = 512;
 constexpr int GU_CHUNK_BYTES = 2 * 32 * 16 * 4;  // act_grad: 32 rows x 16 fp32 of gate and of up
 constexpr int OUT_PLANE_BYTES = 32 * 16 * 2;     // act_grad: 32 rows x 16 bf16 of one output plane
-constexpr int OUT_CHUNK_BYTES = 6 * OUT_PLANE_BYTES;  // d_gate, d_up, w*h; hi and lo each
+constexpr int OUT_CHUNK_BYTES = 4 * OUT_PLANE_BYTES;  // d_gate and d_up; hi and lo each
 
 // Store maps of the act_grad epilogue: [d_gate|d_up] hi and lo as [rows][2][I] (so a store
-// never crosses from the gate half into the up half), w*h hi and lo as [rows][I].
+// never crosses from the gate half into the up half).
 struct alignas(128) EpiMaps {
-  CUtensorMap dgu_hi, dgu_lo, hw_hi, hw_lo;
+  CUtensorMap dgu_hi, dgu_lo;
   CUtensorMap out;  // the bf16 output of GEMM2, INPUT_GRAD and the weight gradients
   CUtensorMap out_lo;  // its lo part (GEMM2 / INPUT_GRAD with split_out)
   CUtensorMap a2, b2;  // the fused forward's second GEMM: h rows and W_down
@@ -104,11 +108,11 @@ struct Args {
   int64_t ld0;
   __nv_bfloat16* out1;
   int64_t ld1;
-  __nv_bfloat16* out2;  // lo planes of the act_grad epilogue
-  __nv_bfloat16* out3;
+  __nv_bfloat16* out2;  // lo plane of the act_grad epilogue
+  __nv_bfloat16* out3;  // GEMM1: lo plane of w*h
   const float* gu;
   int64_t ld_gu;
-  const float* w_row;
+  const float* w_row;  // routing weight of every padded row (0 for pad rows)
   float* p_part;
   int64_t S_pad;
   int64_t out_expert_stride;
@@ -161,7 +165,7 @@ struct Traits {
   static_assert(A_SPLIT || STAGE_BYTES == ::mm::STAGE_BYTES, "stage layout");
   static_assert(!A_SPLIT || A_LO_OFF + A_BYTES == B_OFF, "A lo plane layout");
   // act_grad trades one mainloop stage for per-warp staging of its gate|up input and of its
-  // six output planes (TMA in, TMA out); the weight gradients' 64 KB stages fit three times
+  // four output planes (TMA in, TMA out); the weight gradients' 64 KB stages fit three times
   static constexpr bool GU_STAGING = (KIND == GK_ACT_GRAD);
   static constexpr int STAGES = (GU_STAGING || WGRAD) ? 3 : 4;
   // GEMM2, INPUT_GRAD and the weight gradients stage their bf16 output per warp (two 32x32
@@ -378,13 +382,16 @@ __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __
 
 // GEMM1 + SwiGLU epilogue of one warp: 32 tile rows (quarter q) x one column half. Accumulator
 // columns [0,128) are gate columns n0.., [128,256) up columns n0..; each 32-column chunk writes
-// the fp32 gate, the fp32 up and h = silu(gate) * up (bf16) through the staging buffer. The
-// accumulator is released (`acce`) right after the last TMEM read, before the last stores.
+// the fp32 gate, the fp32 up and w * silu(gate) * up (w: the row's routing weight) as a bf16 hi
+// plane and, for a backward, its bf16 lo residual, all through the staging buffer (hi in its
+// first 2 KB, lo in the second). The accumulator is released (`acce`) right after the last TMEM
+// read, before the last stores.
 __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile& t, uint32_t tacc,
                                                       int q, int hf, int lane, uint8_t* stage,
                                                       uint32_t acce, bool acce_remote = false) {
   const int64_t row0 = (int64_t)t.m0 + q * 32;
   float* gu = reinterpret_cast<float*>(a.out0);
+  const float w = __ldg(a.w_row + row0 + lane);
 #pragma unroll 1
   for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
     uint32_t ga[32], ub[32];
@@ -407,9 +414,9 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
     for (int j = 0; j < 32; ++j) {
       g[j] = __uint_as_float(ga[j]);
       u[j] = __uint_as_float(ub[j]);
-      h[j] = g[j] * sigmoidf_(g[j]) * u[j];
+      h[j] = w * (g[j] * sigmoidf_(g[j]) * u[j]);
     }
-    if (!a.skip_gu) {  // gate|up are kept only for a backward
+    if (!a.skip_gu) {  // gate|up and the lo plane of w*h are kept only for a backward
       stage_row_f32(stage, lane, g);
       __syncwarp();
       copy_out_f32(stage, lane, gu, row0, a.ld0, n, a.I);
@@ -418,18 +425,22 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
       __syncwarp();
       copy_out_f32(stage, lane, gu + a.I, row0, a.ld0, n, a.I);
       __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = h[j] - __bfloat162float(__float2bfloat16_rn(h[j]));
+      stage_row_bf16(stage + 2048, lane, g);
     }
     stage_row_bf16(stage, lane, h);
     __syncwarp();
     copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I);
+    if (!a.skip_gu) copy_out_bf16(stage + 2048, lane, a.out3, row0, a.ld1, n, a.I);
     __syncwarp();
   }
 }
 
 // SwiGLU backward of one 16-column chunk of one row: g from TMEM, gate (cur[0..3]) and up
-// (cur[4..7]) from the staged fp32 values. Writes this row of the six output planes (d_gate,
-// d_up, w*h; hi and lo each) into the warp's staging planes (32 rows x 32 bytes, 32-byte
-// swizzle: 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)) and accumulates <g, h>.
+// (cur[4..7]) from the staged fp32 values. Writes this row of the four output planes (d_gate,
+// d_up; hi and lo each) into the warp's staging planes (32 rows x 32 bytes, 32-byte swizzle:
+// 16-byte half h of row r sits at half h ^ ((r >> 2) & 1)) and accumulates <g, h>.
 __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cur)[8], float w,
                                                float& p, uint8_t* out_row, int lane) {
   uint32_t v[16];
@@ -442,7 +453,7 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
     const float4 b0 = cur[4 + 2 * g8], b1 = cur[4 + 2 * g8 + 1];
     const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
     const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    float da[8], db[8], hv[8];
+    float da[8], db[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float ga = av[j], ub = bv[j];
@@ -454,7 +465,6 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
       const float dh = w * gv;
       da[j] = dh * ub * sg * (1.0f + ga * (1.0f - sg));
       db[j] = dh * sl;
-      hv[j] = w * h;
     }
     uint8_t* o = out_row + ((g8 ^ swz) << 4);
     uint4 hi, lo;
@@ -464,9 +474,6 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
     split8_bf16(db, hi, lo);
     *reinterpret_cast<uint4*>(o + 1 * OUT_PLANE_BYTES) = hi;
     *reinterpret_cast<uint4*>(o + 3 * OUT_PLANE_BYTES) = lo;
-    split8_bf16(hv, hi, lo);
-    *reinterpret_cast<uint4*>(o + 4 * OUT_PLANE_BYTES) = hi;
-    *reinterpret_cast<uint4*>(o + 5 * OUT_PLANE_BYTES) = lo;
   }
 }
 
@@ -474,7 +481,7 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
 // The warp streams the (tile, 16-column chunk) pairs of its 32 rows and column half. Input:
 // lane 0 TMA-loads the fp32 gate and up values of a chunk (two 32x16 boxes, 64-byte swizzle)
 // into the warp's staging buffer, and issues the next chunk's load as soon as the warp has read
-// the current one. Output: the warp writes the chunk's six 32x16 bf16 planes to its output
+// the current one. Output: the warp writes the chunk's four 32x16 bf16 planes to its output
 // staging buffer and lane 0 stores them with TMA (the tensor maps clip columns past I).
 // PAIR = 2: the tiles are the CTA's halves of CTA-pair MMA tiles (units first, first + step, ..;
 // this CTA is `rank` of its pair); a half past the expert is consumed but stores nothing.
@@ -583,8 +590,6 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
         tma_store_3d(&em->dgu_hi, obuf + 1 * OUT_PLANE_BYTES, n, 1, row0);
         tma_store_3d(&em->dgu_lo, obuf + 2 * OUT_PLANE_BYTES, n, 0, row0);
         tma_store_3d(&em->dgu_lo, obuf + 3 * OUT_PLANE_BYTES, n, 1, row0);
-        tma_store_2d(&em->hw_hi, obuf + 4 * OUT_PLANE_BYTES, n, row0);
-        tma_store_2d(&em->hw_lo, obuf + 5 * OUT_PLANE_BYTES, n, row0);
         bulk_commit();
       }
     }
@@ -881,8 +886,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (TR::GU_STAGING) {
       tma_prefetch_desc(&em.dgu_hi);
       tma_prefetch_desc(&em.dgu_lo);
-      tma_prefetch_desc(&em.hw_hi);
-      tma_prefetch_desc(&em.hw_lo);
     }
   }
   if (warp == 1) {
@@ -1345,8 +1348,10 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.N = (int)I;
       a.out0 = ws + w.off_gu;  // fp32
       a.ld0 = 2 * I;
-      a.out1 = bf(w.off_h);
+      a.out1 = bf(w.off_h);  // w*h, hi
+      a.out3 = bf(w.off_hw_lo);  // w*h, lo
       a.ld1 = I;
+      a.w_row = reinterpret_cast<const float*>(ws + w.off_w_row);
       tiles_max = m_tiles_max * a.n_tiles_n;
       break;
     case GK_FWD_FUSED:
@@ -1367,8 +1372,10 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.N = (int)I;
       a.out0 = ws + w.off_gu;  // fp32
       a.ld0 = 2 * I;
-      a.out1 = bf(w.off_h);
+      a.out1 = bf(w.off_h);  // w*h, hi
+      a.out3 = bf(w.off_hw_lo);  // w*h, lo
       a.ld1 = I;
+      a.w_row = reinterpret_cast<const float*>(ws + w.off_w_row);
       tiles_max = m_tiles_max * (a.n_tiles_n + a.n2);
       break;
     case GK_GEMM2:
@@ -1396,15 +1403,10 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       const uint64_t d3[3] = {(uint64_t)I, 2, (uint64_t)S_pad};
       const uint64_t s3[2] = {(uint64_t)I * 2, (uint64_t)(2 * I) * 2};
       const uint32_t b3[3] = {16, 1, 32};
-      const uint64_t d2[2] = {(uint64_t)I, (uint64_t)S_pad};
-      const uint64_t s2[1] = {(uint64_t)I * 2};
-      const uint32_t b2[2] = {16, 32};
       const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
       const auto SW = CU_TENSOR_MAP_SWIZZLE_32B;
       ok = ok && make_map(&em.dgu_hi, ws + w.off_dgu, 3, d3, s3, b3, BF, SW) &&
-           make_map(&em.dgu_lo, ws + w.off_dgu_lo, 3, d3, s3, b3, BF, SW) &&
-           make_map(&em.hw_hi, ws + w.off_h, 2, d2, s2, b2, BF, SW) &&
-           make_map(&em.hw_lo, ws + w.off_hw_lo, 2, d2, s2, b2, BF, SW);
+           make_map(&em.dgu_lo, ws + w.off_dgu_lo, 3, d3, s3, b3, BF, SW);
       has_lo = true;
       has_em = true;
       a.n_tiles_n = cdiv(I, BN);
@@ -1413,9 +1415,6 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.out0 = bf(w.off_dgu);
       a.out2 = bf(w.off_dgu_lo);
       a.ld0 = 2 * I;
-      a.out1 = bf(w.off_h);  // hi part of w*h reuses the forward's h buffer
-      a.out3 = bf(w.off_hw_lo);
-      a.ld1 = I;
       a.gu = reinterpret_cast<const float*>(ws + w.off_gu);
       a.ld_gu = 2 * I;
       a.w_row = reinterpret_cast<const float*>(ws + w.off_w_row);
@@ -1465,7 +1464,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   }
   if (!ok) return cudaErrorInvalidValue;
   if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
-  if (!has_em) em.dgu_hi = em.dgu_lo = em.hw_hi = em.hw_lo = ta;  // unused but initialised
+  if (!has_em) em.dgu_hi = em.dgu_lo = ta;  // unused but initialised
   if constexpr (!Traits<KIND>::FUSED) em.a2 = em.b2 = ta;                // unused but initialised
   if constexpr (Traits<KIND>::OUT_STAGING) {
     // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle

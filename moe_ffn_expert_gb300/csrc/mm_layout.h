@@ -64,9 +64,9 @@ struct Workspace {
   size_t off_row_of_slot, off_slot_of_row, off_w_row;
   size_t off_x_slot;   // bf16 [S_pad, H]   dispatched x rows (kept for W1Grad)
   size_t off_gu;       // fp32 [S_pad, 2I]  gate|up accumulators (kept for the backward)
-  size_t off_h;        // bf16 [S_pad, I]   forward: h;  backward: hi part of w*h
-  size_t off_hw_lo;    // bf16 [S_pad, I]   backward: lo part of w*h
-  size_t off_o;        // bf16 [S_pad, H]   forward: o;  backward: dx rows
+  size_t off_h;        // bf16 [S_pad, I]   hi part of w*h (kept for the backward)
+  size_t off_hw_lo;    // bf16 [S_pad, I]   lo part of w*h (kept for the backward)
+  size_t off_o;        // bf16 [S_pad, H]   forward: w*o;  backward: dx rows
   size_t off_dy_slot;  // bf16 [S_pad, H]   dispatched dy rows
   size_t off_dgu;      // bf16 [S_pad, 2I]  hi part of [d_gate | d_up]
   size_t off_dgu_lo;   // bf16 [S_pad, 2I]  lo part of [d_gate | d_up]
