@@ -197,52 +197,58 @@ struct Tile {
   int part;  // fused forward: 0 = GEMM1 + SwiGLU tile, 1 = GEMM2 tile
 };
 
+// Work order of the fused forward over nm row blocks (row tiles, or pairs of row tiles for the
+// pair MMAs): GEMM1 units of row-block window 0, then for each later window w its GEMM1 units
+// followed by window w-1's GEMM2 units, then the last window's GEMM2 units. Every GEMM2 unit of a
+// row block comes after all of that block's GEMM1 units, and about a window of GEMM1 work
+// separates them. Unit i -> row block m, part (0 = GEMM1, 1 = GEMM2), column tile nt.
+__device__ __forceinline__ void fused_order(const Args& a, int nm, int i, int& m, int& part,
+                                            int& nt) {
+  const int W = a.win, n1 = a.n_tiles_n, n2 = a.n2;
+  const int nw = (nm + W - 1) / W;
+  const int mL = nm - (nw - 1) * W;  // row blocks of the last window
+  const int A = W * n1, B = W * n2;
+  int w, r;
+  const int first = (nw == 1 ? mL : W) * n1;
+  if (i < first) {
+    w = 0, part = 0, r = i;
+  } else {
+    i -= first;
+    const int full_pairs = nw >= 2 ? nw - 2 : 0;
+    if (i < full_pairs * (A + B)) {
+      const int p = i / (A + B), q = i - p * (A + B);
+      if (q < A)
+        w = p + 1, part = 0, r = q;
+      else
+        w = p, part = 1, r = q - A;
+    } else {
+      i -= full_pairs * (A + B);
+      if (nw >= 2 && i < mL * n1) {
+        w = nw - 1, part = 0, r = i;
+      } else {
+        if (nw >= 2) i -= mL * n1;
+        if (nw >= 2 && i < B) {
+          w = nw - 2, part = 1, r = i;
+        } else {
+          if (nw >= 2) i -= B;
+          w = nw - 1, part = 1, r = i;
+        }
+      }
+    }
+  }
+  const int n = part ? n2 : n1;
+  m = w * W + r / n;
+  nt = r - (r / n) * n;
+}
+
 template <int KIND>
 __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   Tile t;
   t.part = 0;
   t.klast = BK / 16;
   if constexpr (Traits<KIND>::FUSED) {
-    // Order: GEMM1 tiles of row-tile window 0, then for each later window w its GEMM1 tiles
-    // followed by window w-1's GEMM2 tiles, then the last window's GEMM2 tiles. Every GEMM2
-    // tile of a row block comes after all of that block's GEMM1 tiles, and about a window of
-    // GEMM1 work separates them.
-    const int nm = __ldg(a.hdr + HDR_NUM_MTILES);
-    const int W = a.win, n1 = a.n_tiles_n, n2 = a.n2;
-    const int nw = (nm + W - 1) / W;
-    const int mL = nm - (nw - 1) * W;  // row tiles of the last window
-    const int A = W * n1, B = W * n2;
-    int i = tile, w, part, r;
-    const int first = (nw == 1 ? mL : W) * n1;
-    if (i < first) {
-      w = 0, part = 0, r = i;
-    } else {
-      i -= first;
-      const int full_pairs = nw >= 2 ? nw - 2 : 0;
-      if (i < full_pairs * (A + B)) {
-        const int p = i / (A + B), q = i - p * (A + B);
-        if (q < A)
-          w = p + 1, part = 0, r = q;
-        else
-          w = p, part = 1, r = q - A;
-      } else {
-        i -= full_pairs * (A + B);
-        if (nw >= 2 && i < mL * n1) {
-          w = nw - 1, part = 0, r = i;
-        } else {
-          if (nw >= 2) i -= mL * n1;
-          if (nw >= 2 && i < B) {
-            w = nw - 2, part = 1, r = i;
-          } else {
-            if (nw >= 2) i -= B;
-            w = nw - 1, part = 1, r = i;
-          }
-        }
-      }
-    }
-    const int n = part ? n2 : n1;
-    const int mt = w * W + r / n;
-    const int nt = r - (r / n) * n;
+    int mt, part, nt;
+    fused_order(a, __ldg(a.hdr + HDR_NUM_MTILES), tile, mt, part, nt);
     t.part = part;
     t.e = __ldg(a.tile_expert + mt);
     t.m0 = mt * BM;
@@ -297,19 +303,25 @@ __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t ra
     valid = t.m0 < a.M;
     return t;
   }
-  const int p = unit / a.n_tiles_n;
-  const int nt = unit - p * a.n_tiles_n;
+  int p, nt, part = 0;
+  if constexpr (Traits<KIND>::FUSED) {  // the fused order over pairs of row tiles
+    fused_order(a, __ldg(a.hdr + HDR_NUM_MPAIRS), unit, p, part, nt);
+  } else {
+    p = unit / a.n_tiles_n;
+    nt = unit - p * a.n_tiles_n;
+  }
   const int pt = __ldg(a.pair_tile + p);
   const int mt0 = pt >= 0 ? pt : ~pt;
   valid = rank == 0 || pt >= 0;
   Tile t;
-  t.part = 0;
+  t.part = part;
   t.klast = BK / 16;
   t.e = __ldg(a.tile_expert + mt0);
   t.m0 = (mt0 + (int)rank) * BM;
-  t.n0 = (KIND == GK_GEMM1_SWIGLU) ? nt * (BN / 2) : nt * BN;
+  const bool gate_up = KIND == GK_GEMM1_SWIGLU || (Traits<KIND>::FUSED && part == 0);
+  t.n0 = gate_up ? nt * (BN / 2) : nt * BN;
   t.row0 = t.m0;
-  t.kiters = a.k_iters;
+  t.kiters = part ? a.k2 : a.k_iters;
   return t;
 }
 
@@ -800,8 +812,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr bool MMA2 = PAIRED;
   pdl_wait();  // the stream's previous kernels are complete (see mm_device.cuh)
   static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
-                    TR::WGRAD || KIND == GK_ACT_GRAD,
-                "pair MMAs: GEMM1, GEMM2, act_grad, input_grad and the weight gradients");
+                    TR::WGRAD || KIND == GK_ACT_GRAD || TR::FUSED,
+                "pair MMAs: GEMM1, GEMM2, the fused forward, act_grad, input_grad and the weight "
+                "gradients");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if constexpr (KIND == GK_ACT_GRAD) {
     // the forward on this workspace kept no gate|up (forward-only): no backward from it
@@ -845,6 +858,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = (PAIRED && TR::WGRAD) ? a.E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+                    : (PAIRED && TR::FUSED) ? a.hdr[HDR_NUM_MPAIRS] * (a.n_tiles_n + a.n2)
                     : PAIRED                ? a.hdr[HDR_NUM_MPAIRS] * a.n_tiles_n
                     : TR::WGRAD             ? a.E * a.m_tiles_w * a.n_tiles_n
                     : TR::FUSED ? a.hdr[HDR_NUM_MTILES] * (a.n_tiles_n + a.n2)
@@ -912,12 +926,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = first; tile < total && ok; tile += step) {
         bool tile_ok;
         const Tile t = tile_at(tile, tile_ok);
-        (void)tile_ok;
         if constexpr (TR::FUSED) {
-          // a GEMM2 tile waits until every GEMM1 tile of its row block has stored its h rows
+          // a GEMM2 tile waits until every GEMM1 tile of its row block has stored its w*h rows
           // (each of their epilogue warps counts once), then orders those generic-proxy writes
-          // before its TMA reads
-          if (t.part == 1) {
+          // before its TMA reads (a pair's half past the expert computes rows nobody stores)
+          if (t.part == 1 && tile_ok) {
             if (!wait_counter(a.ready + t.m0 / BM, a.ready_target, tmo)) {
               set_status(a.status, MM_ERR_TIMEOUT);
               ok = false;
@@ -945,11 +958,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_2d_pair(sa + TR::A_LO_OFF, &tmL, fb, t.m0, t.row0 + k0);
               tma_load_2d_pair(sa + TR::A_LO_OFF + MN_BLOCK_BYTES, &tmL, fb, t.m0 + 64,
                                t.row0 + k0);
+            } else if constexpr (TR::FUSED) {  // this CTA's 128 rows of A: x or w*h rows
+              tma_load_2d_pair(sa, t.part ? &em.a2 : &tmA, fb, k0, t.m0);
             } else {
               tma_load_2d_pair(sa, &tmA, fb, k0, t.m0);  // this CTA's 128 rows of A
             }
             // this CTA's half of B's columns (its MMA share), in its own shared memory
-            if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
+            if constexpr (TR::FUSED) {  // GEMM1: gate (rank 0) or up blocks; GEMM2: blocks 2r, 2r+1
+              const int c0 = t.part ? t.n0 + 128 * (int)rank : (rank ? a.I : 0) + t.n0;
+              const CUtensorMap* mb = t.part ? &em.b2 : &tmB;
+              tma_load_3d_pair(sb, mb, fb, c0, k0, t.e);
+              tma_load_3d_pair(sb + MN_BLOCK_BYTES, mb, fb, c0 + 64, k0, t.e);
+            } else if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
               const int c0 = (rank ? a.I : 0) + t.n0;
               tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
               tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, k0, t.e);
@@ -1137,7 +1157,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the staging buffer may still be read by this warp's TMA stores of a GEMM2 tile
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw), acce_bar(buf));
+          gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw),
+                                (MMA2 && rank != 0) ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf),
+                                MMA2 && rank != 0);
           // this warp's h (and gate|up) stores are visible device-wide, then it counts once
           __threadfence();
           fence_proxy_async_global();
@@ -1148,7 +1170,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                       smem_raw + (sbuf - raw), chunk_no);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acce_bar(buf));
+          if (lane == 0) release_acc(buf);
           if (a.fuse_combine) fused_combine_warp(a, t, q, hf, lane);
         }
         ++acc_it;
@@ -1363,10 +1385,11 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.k_iters = cdiv(H, BK);
       a.n2 = cdiv(H, BN);
       a.k2 = cdiv(I, BK);
-      // GEMM1 windows of 128 row tiles (~5 waves of GEMM1 tiles) between a row block's GEMM1
-      // and GEMM2 tiles: windows of 8 or 32 row tiles, which interleave the two GEMMs more
-      // finely, were 27 % and 6 % slower on a GB300; 128 and one window were equal to two launches
-      a.win = 128;
+      // GEMM1 windows of 128 row tiles (~5 waves of GEMM1 tiles; 64 pairs of row tiles for the
+      // pair MMAs) between a row block's GEMM1 and GEMM2 tiles: with one CTA per tile, windows of
+      // 8 or 32 row tiles, which interleave the two GEMMs more finely, were 27 % and 6 % slower
+      // on a GB300; 128 and one window were equal to two launches
+      a.win = PAIRED ? 64 : 128;
       a.ready = reinterpret_cast<int*>(ws + w.off_ready);
       a.ready_target = NUM_EPI_WARPS * a.n_tiles_n;
       a.N = (int)I;
@@ -1536,8 +1559,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       max_clusters_of[dev].store(max_clusters, std::memory_order_relaxed);
     }
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int64_t units = Traits<KIND>::WGRAD
-                              ? E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+    const int64_t units = Traits<KIND>::WGRAD ? E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+                          : Traits<KIND>::FUSED ? (m_tiles_max + 1) / 2 * (a.n_tiles_n + a.n2)
                               : (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
     cfg.gridDim = dim3((unsigned)(2 * clusters));
@@ -1569,7 +1592,8 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
       return pair == 2 ? run<GK_W2_GRAD, 2>(w, ws, c, st) : run<GK_W2_GRAD>(w, ws, c, st);
     case GK_W1_GRAD:
       return pair == 2 ? run<GK_W1_GRAD, 2>(w, ws, c, st) : run<GK_W1_GRAD>(w, ws, c, st);
-    case GK_FWD_FUSED: return run<GK_FWD_FUSED>(w, ws, c, st);
+    case GK_FWD_FUSED:
+      return pair == 2 ? run<GK_FWD_FUSED, 2>(w, ws, c, st) : run<GK_FWD_FUSED>(w, ws, c, st);
   }
   return cudaErrorInvalidValue;
 }
