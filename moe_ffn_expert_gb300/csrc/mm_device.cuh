@@ -81,6 +81,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// *p += v at GPU scope with release semantics: the calling thread's earlier memory accesses, and
+// those it has synchronised with (the lanes of its warp after __syncwarp), are visible to any
+// thread that acquires the new value.
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Waits (bounded by limit_ns of %globaltimer) until *p >= target; false if the limit ran out.
 __device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t limit_ns) {
   if (ld_acquire_gpu(p) >= target) return true;
