@@ -109,7 +109,7 @@ typedef struct mm_dims {
 
 /* mm_forward / mm_backward flag: one CTA per 128-row tile in every grouped GEMM. By default
  * GEMM1, GEMM2 (forward), act_grad and input_grad (backward), and the weight gradients when the
- * experts average at least 512 rows, run 256-row tiles shared by the two CTAs of a cluster through one
+ * experts average at least 256 rows, run 256-row tiles shared by the two CTAs of a cluster through one
  * tensor-core MMA (tcgen05 .cta_group::2): each CTA holds its 128 rows of A and half of the
  * weight tile's columns, and receives its own rows of the accumulator. Results are identical bit
  * for bit in both forms. */

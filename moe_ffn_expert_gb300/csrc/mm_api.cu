@@ -464,10 +464,11 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   const int accumulate = (flags & MM_FLAG_ACCUMULATE_WEIGHT_GRADS) ? 1 : 0;
   c.wgrad_f32 = (flags & MM_FLAG_FP32_WEIGHT_GRADS) ? 1 : 0;
   // CTA pairs: input_grad in either form; the weight gradients as pair MMAs only, and only when
-  // the experts average 512 rows or more (on short reductions the pair's lockstep costs more
-  // than its halved operand traffic saves)
+  // the experts average 256 rows or more (below that the pair's lockstep over reductions of a
+  // few 64-row blocks costs more than its halved operand traffic saves: measured on a GB300 at
+  // 187 rows per expert, 2 % slower; at 256, 8-11 % faster)
   const int pair = pair_mode(flags);
-  const int wgrad_pair = (pair == 2 && w.S >= 512 * w.E) ? 2 : 0;
+  const int wgrad_pair = (pair == 2 && w.S >= 256 * w.E) ? 2 : 0;
   c.paired = pair == 2 ? 2 : 0;  // act_grad: pair MMAs or one CTA per tile
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
   MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
@@ -488,7 +489,7 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   GemmCall cs{GK_ACT_GRAD, nullptr, nullptr, nullptr, kDefaultTimeoutNs, 0, 0, dy,
               reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS, 1, c.wgrad_f32};
   // the shared expert is one expert of T rows: the same pair rules
-  const int shared_wgrad_pair = (pair == 2 && w.T >= 512) ? 2 : 0;
+  const int shared_wgrad_pair = (pair == 2 && w.T >= 256) ? 2 : 0;
   if (p.shared) {  // shared expert: act_grad, W2Grad (rows = dy), input_grad
     cs.w_up = se->up_proj_weight;
     cs.w_down = se->down_proj_weight;
