@@ -154,6 +154,12 @@ struct Traits {
   // transpose. Both then run 128 x 256 tiles like the row-grouped kinds.
   static constexpr bool A_SPLIT = WGRAD;
   static constexpr bool TRANSPOSED_OUT = (KIND == GK_W1_GRAD);
+  // GEMM1 runs an expert's lone last row tile as an M = 128 pair MMA (64 rows per CTA). GEMM2 and
+  // input_grad could too (their epilogues follow epi_geom), but measured on a GB300 GEMM2 got 7 %
+  // slower (its 12-block reductions make a half unit's mainloop shorter than the epilogue it
+  // overlaps) and input_grad stayed the same; act_grad and the fused forward keep per-row state
+  // over a CTA's 128 rows (<g,h> partials, ready counts)
+  static constexpr bool HALF = (KIND == GK_GEMM1_SWIGLU);
   static_assert(!TRANSPOSED_OUT || WGRAD, "only a weight gradient is stored transposed");
   static constexpr int TN = BN;  // accumulator columns per tile
   static constexpr int B_BYTES = TN * BK * 2;
@@ -195,7 +201,40 @@ struct Tile {
   int e, m0, n0, kiters, row0;
   int klast;  // 16-deep MMA steps issued for the last reduction block (BK / 16 unless trimmed)
   int part;  // fused forward: 0 = GEMM1 + SwiGLU tile, 1 = GEMM2 tile
+  int half;  // pair MMAs: 1 = an M = 128 unit over one row tile, this CTA's 64 rows from m0
 };
+
+// Where one epilogue warp's share of a tile's accumulator sits and where it goes: 32 rows from
+// row0; nch chunks of 32 columns, chunk j read from tensor-memory column tcol0 + 32 j (GEMM1: its
+// up values from tcol0 + up_off + 32 j) and written to output column ocol0 + 32 j.
+struct EpiGeom {
+  int row0, nch, tcol0, up_off, ocol0;
+};
+
+// Warp (q = lane quarter, hf = column half) of a tile. An M = 256 pair unit (or a one-CTA tile)
+// leaves rows 32 q .. 32 q + 31 of the CTA's 128 in the warp's lanes with all of the unit's
+// columns. An M = 128 pair unit leaves the CTA's 64 rows in lanes 0-63 with the unit's first N/2
+// columns and again in lanes 64-127 with the last N/2, both in tensor-memory columns 0 .. N/2 - 1
+// (measured once on a GB300 with an MMA whose accumulator held its own coordinates).
+template <bool GATE_UP>
+__device__ __forceinline__ EpiGeom epi_geom(const Tile& t, int q, int hf, int TN) {
+  EpiGeom g;
+  if (!t.half) {
+    g.row0 = t.m0 + 32 * q;
+    g.nch = GATE_UP ? 2 : TN / 64;
+    g.tcol0 = GATE_UP ? 64 * hf : (TN / 2) * hf;
+    g.up_off = GATE_UP ? 128 : 0;
+    g.ocol0 = t.n0 + g.tcol0;
+  } else {
+    g.row0 = t.m0 + 32 * (q & 1);
+    g.nch = GATE_UP ? 1 : TN / 128;
+    // GEMM1: a CTA's B half holds 64 gate and the matching 64 up columns
+    g.tcol0 = GATE_UP ? 32 * hf : (TN / 4) * hf;
+    g.up_off = GATE_UP ? 64 : 0;
+    g.ocol0 = GATE_UP ? t.n0 + 64 * (q >> 1) + 32 * hf : t.n0 + (TN / 2) * (q >> 1) + (TN / 4) * hf;
+  }
+  return g;
+}
 
 // Work order of the fused forward over nm row blocks (row tiles, or pairs of row tiles for the
 // pair MMAs): GEMM1 units of row-block window 0, then for each later window w its GEMM1 units
@@ -245,6 +284,7 @@ template <int KIND>
 __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   Tile t;
   t.part = 0;
+  t.half = 0;
   t.klast = BK / 16;
   if constexpr (Traits<KIND>::FUSED) {
     int mt, part, nt;
@@ -283,11 +323,12 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
 
 // Work units of the paired launches. Row-grouped kinds: a unit is two row tiles of the same
 // expert and one column tile, so both CTAs need the same B tile (the expert's weights); CTA r of
-// the pair takes row tile mt0 + r. When an expert has an odd number of row tiles its last
-// pair's second tile is not the expert's: that CTA loads other rows of the buffer (or zeros
-// past it), takes part in the MMAs and stores nothing. Weight gradients: a unit is two 128-row
-// tiles of the weight (same expert, same column tile); a second tile past the weight's rows is
-// likewise computed and not stored.
+// the pair takes row tile mt0 + r. When an expert has an odd number of row tiles its last row
+// tile is a unit of its own: for GEMM1 an M = 128 MMA over the pair (HALF kinds: CTA r takes rows
+// 64 r .. 64 r + 63 of the tile; t.half = 1), for the other kinds an M = 256 MMA whose second CTA
+// loads other rows of the buffer (or zeros past it), takes part in the MMAs and stores nothing. Weight gradients: a unit is two 128-row tiles of the
+// weight (same expert, same column tile); a second tile past the weight's rows is likewise
+// computed and not stored.
 template <int KIND>
 __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
   if constexpr (Traits<KIND>::WGRAD) {
@@ -312,12 +353,13 @@ __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t ra
   }
   const int pt = __ldg(a.pair_tile + p);
   const int mt0 = pt >= 0 ? pt : ~pt;
-  valid = rank == 0 || pt >= 0;
   Tile t;
+  t.half = Traits<KIND>::HALF && pt < 0;
+  valid = rank == 0 || pt >= 0 || t.half;
   t.part = part;
   t.klast = BK / 16;
   t.e = __ldg(a.tile_expert + mt0);
-  t.m0 = (mt0 + (int)rank) * BM;
+  t.m0 = t.half ? mt0 * BM + (BM / 2) * (int)rank : (mt0 + (int)rank) * BM;
   const bool gate_up = KIND == GK_GEMM1_SWIGLU || (Traits<KIND>::FUSED && part == 0);
   t.n0 = gate_up ? nt * (BN / 2) : nt * BN;
   t.row0 = t.m0;
@@ -398,19 +440,19 @@ __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __
 // plane and, for a backward, its bf16 lo residual, all through the staging buffer (hi in its
 // first 2 KB, lo in the second). The accumulator is released (`acce`) right after the last TMEM
 // read, before the last stores.
-__device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile& t, uint32_t tacc,
-                                                      int q, int hf, int lane, uint8_t* stage,
+__device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const EpiGeom& eg,
+                                                      uint32_t tacc, int lane, uint8_t* stage,
                                                       uint32_t acce, bool acce_remote = false) {
-  const int64_t row0 = (int64_t)t.m0 + q * 32;
+  const int64_t row0 = eg.row0;
   float* gu = reinterpret_cast<float*>(a.out0);
   const float w = __ldg(a.w_row + row0 + lane);
 #pragma unroll 1
-  for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+  for (int c = 0; c < eg.nch; ++c) {
     uint32_t ga[32], ub[32];
-    tmem_ld_32x32(tacc + c * 32, ga);
-    tmem_ld_32x32(tacc + 128 + c * 32, ub);
+    tmem_ld_32x32(tacc + eg.tcol0 + c * 32, ga);
+    tmem_ld_32x32(tacc + eg.tcol0 + eg.up_off + c * 32, ub);
     tmem_ld_wait();
-    if (c == 2 * hf + 1) {  // last TMEM read of this warp for the tile
+    if (c == eg.nch - 1) {  // last TMEM read of this warp for the tile
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -420,7 +462,7 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const Tile&
           mbar_arrive(acce);
       }
     }
-    const int n = t.n0 + c * 32;
+    const int n = eg.ocol0 + c * 32;
     float g[32], u[32], h[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
@@ -639,23 +681,23 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
 // staging buffer transposed (lane = output column, value j = output row) and stored at the
 // swapped coordinates. `zero` stores zeros without reading TMEM (an expert with no rows).
 template <int KIND>
-__device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, uint32_t tacc,
-                                                  int q, int hf, int lane, const CUtensorMap* map,
-                                                  uint32_t sbuf, uint8_t* sbuf_ptr,
-                                                  uint32_t& chunk_no, bool zero = false) {
+__device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t,
+                                                  const EpiGeom& eg, uint32_t tacc, int lane,
+                                                  const CUtensorMap* map, uint32_t sbuf,
+                                                  uint8_t* sbuf_ptr, uint32_t& chunk_no,
+                                                  bool zero = false) {
   using TR = Traits<KIND>;
-  constexpr int NC = TR::TN / 64;  // 32-column chunks per half
-  const int row0 = t.m0 + q * 32;
+  const int row0 = eg.row0;
   const bool f32 = TR::WGRAD && a.wgrad_f32;
   const bool split = !TR::WGRAD && a.split_out;
 #pragma unroll 1
-  for (int c = hf * NC; c < hf * NC + NC; ++c) {
+  for (int c = 0; c < eg.nch; ++c) {
     uint32_t v[32];
     if (zero) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0u;
     } else {
-      tmem_ld_32x32(tacc + c * 32, v);
+      tmem_ld_32x32(tacc + eg.tcol0 + c * 32, v);
       tmem_ld_wait();
     }
     // both buffers for the fp32 and split forms, else the one used two chunks ago
@@ -708,7 +750,7 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t, 
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      const int n = t.n0 + c * 32;
+      const int n = eg.ocol0 + c * 32;
       const uint32_t src = sbuf + b * OUT_TILE_BYTES;
       if constexpr (TR::WGRAD) {
         const int x = TR::TRANSPOSED_OUT ? row0 : n, y = TR::TRANSPOSED_OUT ? n : row0;
@@ -827,6 +869,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   constexpr int STAGES = MMA2 ? TR::PAIR_STAGES : TR::STAGES;
   constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(2 * BM, TR::TN, TR::A_MN ? 1 : 0, TR::B_MN ? 1 : 0);
+  constexpr uint32_t PAIR_IDESC_HALF = idesc_bf16_f32(BM, TR::TN, TR::A_MN ? 1 : 0, TR::B_MN ? 1 : 0);
   constexpr uint32_t STAGE_BYTES = MMA2 ? TR::PAIR_STAGE_BYTES : TR::STAGE_BYTES;
   const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // act_grad gate|up staging
   const uint32_t bars = epi_base + TR::EPI_BYTES;
@@ -950,7 +993,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int k0 = kb * BK;
           if constexpr (MMA2) {
             // both CTAs' bytes complete on the even CTA's barrier; only it posts their count
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+            // (an M = 128 unit: each CTA loads 64 rows of A)
+            if (rank == 0)
+              mbar_arrive_expect_tx(full_bar(s), 2 * (STAGE_BYTES - (t.half ? A_BYTES / 2 : 0)));
             const uint32_t fb = mapa_shared(full_bar(s), 0);
             if constexpr (TR::WGRAD) {  // this CTA's 128 rows of A (MN-major), hi and lo
               tma_load_2d_pair(sa, &tmA, fb, t.m0, t.row0 + k0);
@@ -960,6 +1005,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                t.row0 + k0);
             } else if constexpr (TR::FUSED) {  // this CTA's 128 rows of A: x or w*h rows
               tma_load_2d_pair(sa, t.part ? &em.a2 : &tmA, fb, k0, t.m0);
+            } else if (t.half) {  // this CTA's 64 rows of A (tmL: the same rows, 64-row boxes)
+              tma_load_2d_pair(sa, &tmL, fb, k0, t.m0);
             } else {
               tma_load_2d_pair(sa, &tmA, fb, k0, t.m0);  // this CTA's 128 rows of A
             }
@@ -969,10 +1016,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const CUtensorMap* mb = t.part ? &em.b2 : &tmB;
               tma_load_3d_pair(sb, mb, fb, c0, k0, t.e);
               tma_load_3d_pair(sb + MN_BLOCK_BYTES, mb, fb, c0 + 64, k0, t.e);
-            } else if constexpr (KIND == GK_GEMM1_SWIGLU) {  // rank 0: the gate blocks, rank 1: up
-              const int c0 = (rank ? a.I : 0) + t.n0;
-              tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
-              tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, k0, t.e);
+            } else if constexpr (KIND == GK_GEMM1_SWIGLU) {
+              if (t.half) {  // rank r: gate and up columns n0 + 64 r .. n0 + 64 r + 63
+                tma_load_3d_pair(sb, &tmB, fb, t.n0 + 64 * (int)rank, k0, t.e);
+                tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, a.I + t.n0 + 64 * (int)rank, k0,
+                                 t.e);
+              } else {  // rank 0: the gate blocks, rank 1: up
+                const int c0 = (rank ? a.I : 0) + t.n0;
+                tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
+                tma_load_3d_pair(sb + MN_BLOCK_BYTES, &tmB, fb, c0 + 64, k0, t.e);
+              }
             } else if constexpr (KIND == GK_GEMM2) {  // rank r: column blocks 2r and 2r + 1
               const int c0 = t.n0 + 128 * (int)rank;
               tma_load_3d_pair(sb, &tmB, fb, c0, k0, t.e);
@@ -1076,7 +1129,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t ad = sdesc_sw128(sa + ka, lbo_a, 1024);
             const uint64_t bd = sdesc_sw128(sb + kbo, lbo_b, 1024);
             if constexpr (MMA2) {
-              umma_bf16_pair(d, ad, bd, PAIR_IDESC, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d, ad, bd, t.half ? PAIR_IDESC_HALF : PAIR_IDESC,
+                             (kb | kk) != 0 ? 1u : 0u);
               if constexpr (TR::A_SPLIT)
                 umma_bf16_pair(d, sdesc_sw128(sa + TR::A_LO_OFF + ka, lbo_a, 1024), bd, PAIR_IDESC,
                                1u);
@@ -1129,8 +1183,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (t.kiters == 0) {
         if constexpr (TR::WGRAD) {
           if (!a.accumulate && tile_ok)  // adding zero changes nothing
-            staged_store_tile<KIND>(a, t, 0u, q, hf, lane, &em.out, sbuf,
-                                    smem_raw + (sbuf - raw), chunk_no, true);
+            staged_store_tile<KIND>(a, t, epi_geom<false>(t, q, hf, TR::TN), 0u, lane, &em.out,
+                                    sbuf, smem_raw + (sbuf - raw), chunk_no, true);
         }
         continue;
       }
@@ -1157,7 +1211,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the staging buffer may still be read by this warp's TMA stores of a GEMM2 tile
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw),
+          gemm1_epilogue_staged(a, epi_geom<true>(t, q, hf, TR::TN), tacc, lane,
+                                smem_raw + (sbuf - raw),
                                 (MMA2 && rank != 0) ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf),
                                 MMA2 && rank != 0);
           // this warp's w*h (and gate|up) stores, ordered before the async proxy's later reads
@@ -1167,8 +1222,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __syncwarp();
           if (lane == 0) red_add_release_gpu(a.ready + t.m0 / BM, 1);
         } else {
-          staged_store_tile<GK_GEMM2>(a, t, tacc, q, hf, lane, &em.out, sbuf,
-                                      smem_raw + (sbuf - raw), chunk_no);
+          staged_store_tile<GK_GEMM2>(a, t, epi_geom<false>(t, q, hf, TR::TN), tacc, lane,
+                                      &em.out, sbuf, smem_raw + (sbuf - raw), chunk_no);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) release_acc(buf);
@@ -1178,15 +1233,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       if constexpr (TR::ROW_STAGING) {  // releases the accumulator itself
-        gemm1_epilogue_staged(a, t, tacc, q, hf, lane, smem_raw + (sbuf - raw),
+        gemm1_epilogue_staged(a, epi_geom<true>(t, q, hf, TR::TN), tacc, lane,
+                              smem_raw + (sbuf - raw),
                               (MMA2 && rank != 0) ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf),
                               MMA2 && rank != 0);
         ++acc_it;
         continue;
       }
       if constexpr (TR::OUT_STAGING)
-        staged_store_tile<KIND>(a, t, tacc, q, hf, lane, &em.out, sbuf, smem_raw + (sbuf - raw),
-                                chunk_no);
+        staged_store_tile<KIND>(a, t, epi_geom<false>(t, q, hf, TR::TN), tacc, lane, &em.out,
+                                sbuf, smem_raw + (sbuf - raw), chunk_no);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) release_acc(buf);
@@ -1365,7 +1421,9 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   switch (KIND) {
     case GK_GEMM1_SWIGLU:
       ok = map_rows(&ta, xrows, H, nrows, 64, BM) &&
-           map_experts(&tb, c.w_up, 2 * I, H, E, 64, 64);
+           map_experts(&tb, c.w_up, 2 * I, H, E, 64, 64) &&
+           (!PAIRED || map_rows(&tl, xrows, H, nrows, 64, BM / 2));  // the M = 128 units' A
+      has_lo = PAIRED;
       a.n_tiles_n = cdiv(I, BN / 2);
       a.k_iters = cdiv(H, BK);
       a.N = (int)I;
@@ -1487,7 +1545,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
-  if (!has_lo) tl = ta;  // unused by the kinds without a lo plane
+  if (!has_lo) tl = ta;  // unused by the kinds without a lo plane or M = 128 units
   if (!has_em) em.dgu_hi = em.dgu_lo = ta;  // unused but initialised
   if constexpr (!Traits<KIND>::FUSED) em.a2 = em.b2 = ta;                // unused but initialised
   if constexpr (Traits<KIND>::OUT_STAGING) {
