@@ -192,8 +192,12 @@ struct Traits {
   // weight gradients
   static constexpr int PAIR_STAGE_BYTES = B_OFF + B_BYTES / 2;
   static constexpr int PAIR_STAGES = (WGRAD || GU_STAGING) ? 4 : 6;
+  // with half of B per stage, act_grad's epilogue warps keep two gate|up chunks in flight
+  static constexpr int PAIR_GU_BUFS = GU_STAGING ? 2 : 1;
+  static constexpr int PAIR_EPI_BYTES =
+      GU_STAGING ? NUM_EPI_WARPS * (PAIR_GU_BUFS * GU_CHUNK_BYTES + OUT_CHUNK_BYTES) : EPI_BYTES;
   static constexpr size_t PAIR_SMEM =
-      (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + 1024 + BAR_BYTES;
+      (size_t)PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_EPI_BYTES + 1024 + BAR_BYTES;
   static_assert(PAIR_SMEM <= 232448, "pair-MMA shared memory budget");
 };
 
@@ -534,12 +538,12 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
 // act_grad epilogue of one warp: g = dy_slot W_down^T (from TMEM) and the SwiGLU backward.
 // The warp streams the (tile, 16-column chunk) pairs of its 32 rows and column half. Input:
 // lane 0 TMA-loads the fp32 gate and up values of a chunk (two 32x16 boxes, 64-byte swizzle)
-// into the warp's staging buffer, and issues the next chunk's load as soon as the warp has read
-// the current one. Output: the warp writes the chunk's four 32x16 bf16 planes to its output
+// into one of the warp's GU_BUFS staging buffers (chunk i in buffer i % GU_BUFS, on that buffer's
+// barrier), GU_BUFS chunks ahead, and refills a buffer as soon as the warp has read it. Output: the warp writes the chunk's four 32x16 bf16 planes to its output
 // staging buffer and lane 0 stores them with TMA (the tensor maps clip columns past I).
 // PAIR = 2: the tiles are the CTA's halves of CTA-pair MMA tiles (units first, first + step, ..;
 // this CTA is `rank` of its pair); a half past the expert is consumed but stores nothing.
-template <int PAIR>
+template <int PAIR, int GU_BUFS>
 __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorMap* tm_gu,
                                                   const EpiMaps* em, int total, uint32_t tmem_base,
                                                   uint32_t accf0, uint32_t accf1, uint32_t acce0,
@@ -566,7 +570,9 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     while (ce > c0 && n0 + (ce - 1) * 16 >= a.I) --ce;
     return ce;
   };
+  static_assert(GU_BUFS == 1 || GU_BUFS == 2, "gate|up staging depth");
   int ld_tile = first, ld_c = c0;  // next (unit, chunk) to load
+  uint32_t issued = 0;             // chunks loaded so far (the next goes to buffer issued % GU_BUFS)
   auto issue_next = [&]() {
     bool v;
     while (ld_tile < total && ld_c >= chunk_end(tile_at(ld_tile, v).n0)) {
@@ -576,14 +582,18 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     if (ld_tile >= total) return;
     if (lane == 0) {
       const Tile tn = tile_at(ld_tile, v);
+      const uint32_t b = issued % GU_BUFS;
+      const uint32_t bar = gbar + 8u * b, dst = gbuf + b * GU_CHUNK_BYTES;
       fence_proxy_async_smem();  // the buffer's previous contents were read by the warp
-      mbar_arrive_expect_tx(gbar, GU_CHUNK_BYTES);
-      tma_load_2d(gbuf, tm_gu, gbar, tn.n0 + ld_c * 16, tn.m0 + q * 32);
-      tma_load_2d(gbuf + GU_CHUNK_BYTES / 2, tm_gu, gbar, a.I + tn.n0 + ld_c * 16, tn.m0 + q * 32);
+      mbar_arrive_expect_tx(bar, GU_CHUNK_BYTES);
+      tma_load_2d(dst, tm_gu, bar, tn.n0 + ld_c * 16, tn.m0 + q * 32);
+      tma_load_2d(dst + GU_CHUNK_BYTES / 2, tm_gu, bar, a.I + tn.n0 + ld_c * 16, tn.m0 + q * 32);
     }
+    ++issued;
     ++ld_c;
   };
-  issue_next();
+#pragma unroll
+  for (int b = 0; b < GU_BUFS; ++b) issue_next();
   uint32_t acc_it = 0, used = 0;
   bool failed = false;
   uint8_t* out_row = obuf_ptr + lane * 32;
@@ -607,8 +617,9 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     float p = 0.f;
     const int c_end = chunk_end(t.n0);
     for (int c = c0; c < c_end; ++c) {
+      const uint32_t gb = used % GU_BUFS;
       int okg = 1;
-      if (lane == 0) okg = mbar_wait(gbar, used & 1u, tmo) ? 1 : 0;
+      if (lane == 0) okg = mbar_wait(gbar + 8u * gb, (used / GU_BUFS) & 1u, tmo) ? 1 : 0;
       okg = __shfl_sync(0xffffffffu, okg, 0);
       if (!okg) {
         if (lane == 0) set_status(a.status, MM_ERR_TIMEOUT);
@@ -618,7 +629,7 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
       __syncwarp();
       // row `lane` of the two 32x16 fp32 boxes; with the 64-byte swizzle the 16-byte unit u of
       // row r sits at unit u ^ ((r >> 1) & 3)
-      const uint8_t* base = gbuf_ptr + lane * 64;
+      const uint8_t* base = gbuf_ptr + gb * GU_CHUNK_BYTES + lane * 64;
       const int n = t.n0 + c * 16;
       float4 cur[8];
 #pragma unroll
@@ -631,7 +642,7 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
       }
       ++used;
       __syncwarp();
-      issue_next();  // the staging buffer is free again: start the next chunk's load
+      issue_next();  // this staging buffer is free again: start the load GU_BUFS chunks ahead
       if (!tile_ok) continue;  // a pair half past the expert: nothing to compute or store
       // the previous chunk's stores must have finished reading the output staging buffer
       if (lane == 0) bulk_wait_read_all();
@@ -871,14 +882,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint32_t PAIR_IDESC = idesc_bf16_f32(2 * BM, TR::TN, TR::A_MN ? 1 : 0, TR::B_MN ? 1 : 0);
   constexpr uint32_t PAIR_IDESC_HALF = idesc_bf16_f32(BM, TR::TN, TR::A_MN ? 1 : 0, TR::B_MN ? 1 : 0);
   constexpr uint32_t STAGE_BYTES = MMA2 ? TR::PAIR_STAGE_BYTES : TR::STAGE_BYTES;
+  constexpr int GU_BUFS = MMA2 ? TR::PAIR_GU_BUFS : 1;  // act_grad gate|up buffers per warp
   const uint32_t epi_base = sbase + STAGES * STAGE_BYTES;  // act_grad gate|up staging
-  const uint32_t bars = epi_base + TR::EPI_BYTES;
+  const uint32_t bars = epi_base + (MMA2 ? TR::PAIR_EPI_BYTES : TR::EPI_BYTES);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
   auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
   auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-  auto gu_bar = [&](int ew) { return bars + 8u * (2 * STAGES + 4 + ew); };
-  const uint32_t tmem_holder = bars + 8u * (2 * STAGES + 4 + NUM_EPI_WARPS);
+  auto gu_bar = [&](int ew) { return bars + 8u * (2 * STAGES + 4 + GU_BUFS * ew); };
+  const uint32_t tmem_holder = bars + 8u * (2 * STAGES + 4 + GU_BUFS * NUM_EPI_WARPS);
+  static_assert(8 * (2 * STAGES + 4 + GU_BUFS * NUM_EPI_WARPS) + 8 <= BAR_BYTES - 8,
+                "barrier area");
   volatile uint32_t* tmem_holder_ptr =
       reinterpret_cast<volatile uint32_t*>(smem_raw + (tmem_holder - raw));
 
@@ -930,7 +944,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(acce_bar(b), MMA2 ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     }
     if constexpr (TR::GU_STAGING)
-      for (int ew = 0; ew < NUM_EPI_WARPS; ++ew) mbar_init(gu_bar(ew), 1);
+      for (int i = 0; i < GU_BUFS * NUM_EPI_WARPS; ++i) mbar_init(gu_bar(0) + 8u * i, 1);
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -1158,9 +1172,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if constexpr (TR::GU_STAGING) {
     const int ew = warp - 2;
-    const uint32_t gbuf = epi_base + ew * GU_CHUNK_BYTES;
-    const uint32_t obuf = epi_base + NUM_EPI_WARPS * GU_CHUNK_BYTES + ew * OUT_CHUNK_BYTES;
-    act_grad_epilogue<PAIR>(a, &tmL, &em, total, tmem_base, accf_bar(0), accf_bar(1),
+    const uint32_t gbuf = epi_base + ew * GU_BUFS * GU_CHUNK_BYTES;
+    const uint32_t obuf =
+        epi_base + NUM_EPI_WARPS * GU_BUFS * GU_CHUNK_BYTES + ew * OUT_CHUNK_BYTES;
+    act_grad_epilogue<PAIR, GU_BUFS>(a, &tmL, &em, total, tmem_base, accf_bar(0), accf_bar(1),
                             acce_bar(0), acce_bar(1), gu_bar(ew), gbuf, smem_raw + (gbuf - raw),
                             obuf, smem_raw + (obuf - raw), warp, lane, first, step, rank);
   } else {
