@@ -515,6 +515,27 @@ def run_gpu(args):
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
+    if args.trace and rank == 0:  # one more step, traced, after every timed leg
+        from moe_ffn_expert_gb300 import trace as mm_trace
+        tb = mm_trace.TraceBuffer(capacity=1 << 21, device=dev)
+        tb.start()
+        step()
+        recs = tb.stop()
+        summ = mm_trace.summarize(recs)
+        title = (f"Trace of one fwd+bwd step: {w.name} (T={T}, H={H}, I={I}, E={E}, K={K}), "
+                 f"fwd flags 0x{args.fwd_flags:x}, bwd flags 0x{args.bwd_flags:x}")
+        cmd = "python bench.py " + " ".join(sys.argv[1:])
+        notes = (f"Made by `{cmd}`: one step after the timed legs, with the per-tile trace on "
+                 f"({int(recs.size)} records). Times are %globaltimer ns from the first record; "
+                 "tracing adds an atomic per record, so the step here runs a little longer than "
+                 "untraced. mainloop busy: share of the launch's SM-time in which an MMA issuer "
+                 "held a tile (from taking a free accumulator to its last commit, operand waits "
+                 "included; a CTA-pair unit counts for both SMs). epilogue busy: the same for "
+                 "the first epilogue warp of each CTA. epilogue hidden: share of that epilogue "
+                 "time during which the same SM's (or pair's) MMA issuer held the next tile.")
+        with open(args.trace, "w") as f:
+            f.write(mm_trace.report(summ, title, notes))
+        line["trace"] = {"file": args.trace, "records": int(recs.size), "dropped": tb.dropped}
     print(json.dumps(line), flush=True)
 
 
@@ -628,6 +649,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--shared-intermediate", type=int, default=0,
                     help="add a shared expert of this intermediate size (0: none)")
+    ap.add_argument("--trace", default="",
+                    help="after the timed legs, trace one more step (per-tile records, see "
+                         "moe_ffn_expert_gb300/trace.py) and write its timeline to this file")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample (0: skip)")
     args = ap.parse_args(argv)

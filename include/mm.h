@@ -240,7 +240,7 @@ const char* mm_last_error_detail(void);
 /* Human-readable name of a status code. */
 const char* mm_status_string(mm_status s);
 
-/* ABI version of this library (bumped on any signature change). */
+/* ABI version of this library (bumped on any change of the exported functions or structs). */
 int mm_abi_version(void);
 
 /* Optional per-stage timer. When enabled, every kernel the library enqueues is bracketed by
@@ -254,6 +254,44 @@ mm_status mm_timing_enable(int on);
 mm_status mm_timing_select(uint32_t stage_mask);
 int mm_timing_read(double* ms, int64_t* launches, int max_stages);
 const char* mm_stage_name(int stage);
+
+/* Optional per-tile trace: when and where each piece of work ran. The RFC's performance
+ * acceptance (§8) asks for the concurrency and utilisation of the cube (matrix) and vector
+ * units over time; on a GB300 each grouped-GEMM CTA has both in one SM: the tensor-core
+ * mainloop, and the epilogue warps that apply the elementwise math and store the tile. While a
+ * trace buffer is set, every kernel that mm_forward / mm_backward (and their _ex forms) enqueue
+ * writes records into it:
+ *   MM_TRACE_CTA       one per CTA: from its start (after the stream's previous kernel completed)
+ *                      to the end of its work (the CTA's first thread);
+ *   MM_TRACE_MAINLOOP  one per grouped-GEMM tile (per unit of two row tiles for the CTA-pair
+ *                      MMAs, recorded by the even CTA that issues them): from the MMA-issuing
+ *                      thread taking a free accumulator to its commit of the tile's last MMA;
+ *   MM_TRACE_EPILOGUE  one per tile and CTA: from the accumulator being ready to the end of the
+ *                      first epilogue warp's work on it (the other warps' spans are alike).
+ * Times are %globaltimer nanoseconds (one clock for all SMs). The buffer is device memory,
+ * 32-byte aligned: a 32-byte header whose first uint32 counts the records offered, then
+ * bytes / 32 - 1 record slots; records past the last slot are dropped (the count still
+ * includes them). The caller zeroes the header before the calls it wants traced (records are
+ * placed at the count's value). Each traced launch gets the next sequence number
+ * (`launch`), starting at 0 when the buffer is set. A kernel captured into a CUDA graph keeps
+ * the buffer and sequence number it was captured with. Process-global, for use from one thread
+ * while no other thread calls the library (like the stage timer). Each record costs an atomic
+ * add and two stores: time untraced runs. mm_trace_set(NULL, 0) turns tracing off. */
+typedef struct mm_trace_record {
+  uint16_t stage;   /* mm_stage_name(stage) */
+  uint16_t role;    /* MM_TRACE_CTA, MM_TRACE_MAINLOOP or MM_TRACE_EPILOGUE */
+  uint16_t sm;      /* %smid of the SM that ran it */
+  uint16_t rank;    /* the CTA's rank in its pair (CTA-pair MMAs), else 0 */
+  int32_t unit;     /* MM_TRACE_CTA: blockIdx.x; else the tile (or pair unit) index in the launch */
+  uint32_t launch;  /* sequence number of the launch */
+  uint64_t t0, t1;  /* %globaltimer at start and end, ns */
+} mm_trace_record;
+#define MM_TRACE_CTA 0
+#define MM_TRACE_MAINLOOP 1
+#define MM_TRACE_EPILOGUE 2
+/* Sets (or with NULL clears) the trace buffer. MM_ERR_INVALID_ARG if the pointer is not 32-byte
+ * aligned or bytes < 64 (a header and one record). */
+mm_status mm_trace_set(void* device_buffer, size_t bytes);
 
 #ifdef __cplusplus
 }

@@ -31,6 +31,10 @@ MM_FLAG_FUSED_COMBINE = 0x10
 MM_FLAG_FORWARD_ONLY = 0x20
 MM_FLAG_SINGLE_CTA_TILES = 0x100
 MM_NUM_STAGES = 16
+MM_TRACE_CTA = 0
+MM_TRACE_MAINLOOP = 1
+MM_TRACE_EPILOGUE = 2
+TRACE_RECORD_BYTES = 32  # sizeof(mm_trace_record); the buffer's header takes one record's bytes
 
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_BAD_EXPERT_ID", 6: "MM_ERR_TIMEOUT",
@@ -95,6 +99,7 @@ def _lib():
         "mm_timing_read": (ctypes.c_int, [_P, _P, ctypes.c_int]),
         "mm_stage_name": (ctypes.c_char_p, [ctypes.c_int]),
         "mm_route_noalloc": (st, [mm_dims, _P, _P, _P, _P, _P]),
+        "mm_trace_set": (st, [_P, ctypes.c_size_t]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -208,6 +213,11 @@ def mm_timing_read() -> dict:
     cnt = (ctypes.c_int64 * MM_NUM_STAGES)()
     n = _lib().mm_timing_read(ctypes.cast(ms, _P), ctypes.cast(cnt, _P), MM_NUM_STAGES)
     return {_lib().mm_stage_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
+
+
+def mm_trace_set(device_buffer, nbytes: int) -> int:
+    """Sets (device_buffer = 0: clears) the trace buffer; see moe_ffn_expert_gb300.trace."""
+    return int(_lib().mm_trace_set(device_buffer or None, int(nbytes)))
 
 
 def check(status: int, where: str):

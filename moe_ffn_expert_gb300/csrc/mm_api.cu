@@ -65,8 +65,19 @@ struct Timer {
 };
 Timer g_timer;
 
+// ---- optional trace (process-global, not thread-safe): the caller's buffer and the sequence
+// number of the next traced launch
+struct TraceState {
+  uint32_t* buf = nullptr;
+  uint32_t cap = 0;
+  uint32_t next_launch = 0;
+};
+TraceState g_trace;
+// the trace context of the launch this thread is enqueueing (read by the launchers)
+thread_local TraceCtx t_trace_cur = {nullptr, 0, 0, 0};
+
 template <typename F>
-cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
+cudaError_t timed_launch(int stage, cudaStream_t st, F&& launch) {
   if (!g_timer.on || !((g_timer.mask >> stage) & 1u)) return launch();
   cudaEvent_t a = g_timer.get(), b = g_timer.get();
   if (a) cudaEventRecord(a, st);
@@ -78,6 +89,17 @@ cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
     if (a) g_timer.pool.push_back(a);
     if (b) g_timer.pool.push_back(b);
   }
+  return e;
+}
+
+// Every launch of a forward or backward goes through here: the stage timer's events, and the
+// trace context the launcher passes to its kernel.
+template <typename F>
+cudaError_t timed(int stage, cudaStream_t st, F&& launch) {
+  if (g_trace.buf != nullptr)
+    t_trace_cur = {g_trace.buf, g_trace.cap, (uint32_t)stage, g_trace.next_launch++};
+  const cudaError_t e = timed_launch(stage, st, launch);
+  t_trace_cur = {nullptr, 0, 0, 0};
   return e;
 }
 
@@ -150,6 +172,11 @@ cudaError_t bind_context() {
 
 }  // namespace
 
+TraceCtx trace_ctx() { return t_trace_cur; }
+static_assert(sizeof(mm_trace_record) == 32 && offsetof(mm_trace_record, unit) == 8 &&
+                  offsetof(mm_trace_record, launch) == 12 && offsetof(mm_trace_record, t0) == 16,
+              "trace record layout (written by trace_put as two 16-byte words)");
+
 void note_error(const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -209,7 +236,7 @@ using namespace mm;
 
 extern "C" {
 
-int mm_abi_version(void) { return 2; }
+int mm_abi_version(void) { return 3; }
 
 const char* mm_last_error_detail(void) { return g_err; }
 
@@ -651,6 +678,19 @@ int mm_timing_read(double* ms, int64_t* launches, int max_stages) {
 const char* mm_stage_name(int stage) {
   if (stage < 0 || stage >= ST_COUNT) return "";
   return kStageNames[stage];
+}
+
+mm_status mm_trace_set(void* device_buffer, size_t bytes) {
+  if (device_buffer == nullptr) {
+    g_trace = TraceState();
+    return MM_OK;
+  }
+  if (!aligned(device_buffer, 32) || bytes < 64) return MM_ERR_INVALID_ARG;
+  const size_t cap = bytes / 32 - 1;
+  g_trace.buf = reinterpret_cast<uint32_t*>(device_buffer);
+  g_trace.cap = cap > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)cap;
+  g_trace.next_launch = 0;
+  return MM_OK;
 }
 
 }  // extern "C"

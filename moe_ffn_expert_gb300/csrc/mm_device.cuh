@@ -22,6 +22,45 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
+
+// ---- optional trace (mm_trace_record layout of mm.h: stage | role << 16, sm | rank << 16,
+// unit, launch, t0, t1 as little-endian words)
+
+// The start time of a traced span (0 when tracing is off: no clock read).
+__device__ __forceinline__ uint64_t trace_start(const TraceCtx& tc) {
+  return tc.buf != nullptr ? globaltimer_ns() : 0ull;
+}
+
+// Appends one record [t0, now] of `role` for `unit`; a record past the buffer is only counted.
+__device__ __forceinline__ void trace_put(const TraceCtx& tc, uint32_t role, int unit,
+                                          uint32_t rank, uint64_t t0) {
+  if (tc.buf == nullptr) return;
+  const uint64_t t1 = globaltimer_ns();
+  const uint32_t i = atomicAdd(tc.buf, 1u);
+  if (i >= tc.cap) return;
+  uint4* r = reinterpret_cast<uint4*>(tc.buf + 8 * (size_t)(i + 1));
+  r[0] = make_uint4(tc.stage | (role << 16), sm_id() | (rank << 16), (uint32_t)unit, tc.launch);
+  r[1] = make_uint4((uint32_t)t0, (uint32_t)(t0 >> 32), (uint32_t)t1, (uint32_t)(t1 >> 32));
+}
+
+// One MM_TRACE_CTA record per CTA: started where it is constructed (after pdl_wait), recorded by
+// the CTA's first thread when it leaves the kernel, on whichever path it returns.
+struct TraceCta {
+  const TraceCtx& tc;
+  uint64_t t0;
+  uint32_t rank;
+  __device__ __forceinline__ explicit TraceCta(const TraceCtx& c, uint32_t r = 0)
+      : tc(c), t0(trace_start(c)), rank(r) {}
+  __device__ __forceinline__ ~TraceCta() {
+    if (threadIdx.x == 0) trace_put(tc, MM_TRACE_CTA, (int)blockIdx.x, rank, t0);
+  }
+};
+
 // Records the first error of a call in the workspace status word (first writer wins).
 __device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
 

@@ -138,6 +138,7 @@ struct Args {
   int comb_K, comb_H, comb_nch;
   int skip_gu;  // GEMM1: forward only, gate|up are not stored
   const int32_t* pair_tile;  // paired launches: first row tile of each pair (~tile: no second)
+  TraceCtx trace;            // optional per-tile trace (trace.buf == nullptr: off)
 };
 
 template <int KIND>
@@ -597,7 +598,14 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   uint32_t acc_it = 0, used = 0;
   bool failed = false;
   uint8_t* out_row = obuf_ptr + lane * 32;
+  uint64_t ep_t0 = 0;  // the first epilogue warp's span on each accumulator
+  int ep_unit = 0;
+  auto ep_close = [&]() {
+    if (ep_t0 != 0 && lane == 0) trace_put(a.trace, MM_TRACE_EPILOGUE, ep_unit, rank, ep_t0);
+    ep_t0 = 0;
+  };
   for (int tile = first; tile < total; tile += step) {
+    ep_close();
     bool tile_ok;
     const Tile t = tile_at(tile, tile_ok);
     const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
@@ -610,6 +618,10 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     }
     __syncwarp();
     tc_fence_after();
+    if (warp == 2) {
+      ep_t0 = trace_start(a.trace);
+      ep_unit = tile;
+    }
     const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
     const int row0 = t.m0 + q * 32;
     const int64_t row = (int64_t)row0 + lane;
@@ -671,6 +683,7 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     }
     ++acc_it;
   }
+  ep_close();
   if (lane == 0) bulk_wait_all();  // this warp's output stores are complete before it exits
   __syncwarp();
 }
@@ -864,6 +877,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr bool PAIRED = PAIR == 2;
   constexpr bool MMA2 = PAIRED;
   pdl_wait();  // the stream's previous kernels are complete (see mm_device.cuh)
+  const TraceCta trace_cta(a.trace, PAIRED ? cluster_ctarank() : 0u);
   static_assert(!PAIRED || KIND == GK_GEMM1_SWIGLU || KIND == GK_GEMM2 || KIND == GK_INPUT_GRAD ||
                     TR::WGRAD || KIND == GK_ACT_GRAD || TR::FUSED,
                 "pair MMAs: GEMM1, GEMM2, the fused forward, act_grad, input_grad and the weight "
@@ -1121,6 +1135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
+        const uint64_t tm0 = trace_start(a.trace);
         const uint32_t d = tmem_base + buf * TR::TN;
         for (int kb = 0; kb < t.kiters; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -1167,6 +1182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           else
             umma_commit(accf_bar(buf));
         }
+        trace_put(a.trace, MM_TRACE_MAINLOOP, tile, rank, tm0);
         ++acc_it;
       }
     }
@@ -1192,7 +1208,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(acce_bar(b));
     };
     uint32_t acc_it = 0;
+    // the first epilogue warp's span on each accumulator, closed when the warp moves on
+    uint64_t ep_t0 = 0;
+    int ep_unit = 0;
+    auto ep_close = [&]() {
+      if (ep_t0 != 0 && lane == 0) trace_put(a.trace, MM_TRACE_EPILOGUE, ep_unit, rank, ep_t0);
+      ep_t0 = 0;
+    };
     for (int tile = first; tile < total; tile += step) {
+      ep_close();
       bool tile_ok;
       const Tile t = tile_at(tile, tile_ok);
       if (t.kiters == 0) {
@@ -1213,6 +1237,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
       tc_fence_after();
+      if (warp == 2) {
+        ep_t0 = trace_start(a.trace);
+        ep_unit = tile;
+      }
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
       if (!tile_ok) {  // a pair's second tile outside the expert: nothing to store
         tc_fence_before();
@@ -1264,6 +1292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if constexpr (KIND == GK_GEMM2_COMBINE) fused_combine_warp(a, t, q, hf, lane);
       ++acc_it;
     }
+    ep_close();
     if constexpr (TR::OUT_STAGING) {
       if (lane == 0) bulk_wait_all();  // this warp's output stores are complete
       __syncwarp();
@@ -1396,6 +1425,7 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16*>(ws + off); };
 
   Args a{};
+  a.trace = trace_ctx();
   a.hdr = reinterpret_cast<const int*>(ws + w.off_hdr);
   a.status = c.status ? c.status : reinterpret_cast<int*>(ws + w.off_hdr) + HDR_STATUS;
   // token rows: the dispatched (expert-sorted) copies, or x / dy themselves for the shared

@@ -94,4 +94,8 @@ cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStr
 // Records a description of a host-side failure for mm_last_error_detail (this thread).
 void note_error(const char* fmt, ...);
 
+// Trace context for the launch being enqueued on this thread (tracing off: buf == nullptr);
+// every launcher passes it to its kernel.
+TraceCtx trace_ctx();
+
 }  // namespace mm

@@ -50,6 +50,16 @@ enum Stage {
 };
 static_assert(ST_COUNT == MM_NUM_STAGES, "stage table");
 
+// Trace context of one launch (a kernel argument): the caller's buffer (a header word counting
+// the records offered, then 32-byte mm_trace_record slots from byte 32), its record capacity,
+// and the launch's stage and sequence number. buf == nullptr: tracing is off.
+struct TraceCtx {
+  uint32_t* buf;
+  uint32_t cap;
+  uint32_t stage;
+  uint32_t launch;
+};
+
 // Byte offsets of every region in the caller's workspace (all 256-byte aligned).
 struct Workspace {
   int64_t T, H, I, E, K, S;

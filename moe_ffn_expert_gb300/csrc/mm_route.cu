@@ -32,8 +32,9 @@ const T* region(const char* ws, size_t off) {
 
 __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__ ids, int* hdr,
                                                      int32_t* __restrict__ chunk_cnt, int S, int E,
-                                                     int n_chunks) {
+                                                     int n_chunks, TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   extern __shared__ int32_t cnt_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x * 4 + warp;
@@ -80,8 +81,9 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      float* __restrict__ w_row,
                                                      int32_t* __restrict__ pair_tile,
                                                      const int32_t* __restrict__ tpe, int E,
-                                                     int n_chunks) {
+                                                     int n_chunks, TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   __shared__ int wsum[32], wsum_p[32], wsum_q[32];
   __shared__ int tot_s[1024], po_s[1024], qo_s[1024], seg_s[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -218,8 +220,9 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ row_of_slot,
                                                     int32_t* __restrict__ slot_of_row,
                                                     float* __restrict__ w_row, int S, int E,
-                                                    int n_chunks) {
+                                                    int n_chunks, TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   extern __shared__ int32_t cnt_smem[];
   if (hdr[HDR_STATUS] != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,8 +265,10 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src,
                                                      uint4* __restrict__ dst,
                                                      const int32_t* __restrict__ slot_of_row,
-                                                     const int* hdr, int K, int vpr) {
+                                                     const int* hdr, int K, int vpr,
+                                                     TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (hdr[HDR_STATUS] != 0 || row >= hdr[HDR_NUM_MTILES] * BM) return;
@@ -318,8 +323,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
                                                  const uint4* __restrict__ extra,
                                                  const uint4* __restrict__ extra_lo,
                                                  uint4* __restrict__ out, const int* hdr, int T,
-                                                 int K, int vpr) {
+                                                 int K, int vpr, TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (hdr[HDR_STATUS] != 0 || t >= T) return;
@@ -371,8 +377,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint4* __restrict__ rows,
 __global__ void __launch_bounds__(256) k_d_topk(const float* __restrict__ p_part,
                                                 const int32_t* __restrict__ row_of_slot,
                                                 float* __restrict__ d_topk, const int* hdr, int S,
-                                                int n_tiles, int64_t S_pad) {
+                                                int n_tiles, int64_t S_pad, TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   const int s = blockIdx.x * 256 + threadIdx.x;
   if (hdr[HDR_STATUS] != 0 || s >= S) return;
   const int r = row_of_slot[s];
@@ -403,8 +410,10 @@ __global__ void __launch_bounds__(256) k_export_rows(const int32_t* __restrict__
 __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts, int32_t* offsets,
                                                        int32_t* poff, int32_t* tile_expert,
                                                        int32_t* pair_tile, int32_t* slot_of_row,
-                                                       float* w_row, int32_t* row_of_slot, int T) {
+                                                       float* w_row, int32_t* row_of_slot, int T,
+                                                       TraceCtx tc) {
   pdl_wait();
+  const TraceCta trace_cta(tc);
   const int Tp = (T + BM - 1) / BM * BM;
   const int nm = Tp / BM;
   const int r = blockIdx.x * 256 + threadIdx.x;
@@ -442,7 +451,7 @@ cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids,
   const unsigned grid = div_up(w.n_chunks, 4);
   return launch_pdl(k_route_count, grid, 128, 4 * w.E * sizeof(int32_t), st, ids,
                     region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk), (int)w.S,
-                    (int)w.E, (int)w.n_chunks);
+                    (int)w.E, (int)w.n_chunks, trace_ctx());
 }
 
 cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* tokens_per_expert,
@@ -452,7 +461,7 @@ cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* token
                     region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
                     region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_pair_tile),
-                    tokens_per_expert, (int)w.E, (int)w.n_chunks);
+                    tokens_per_expert, (int)w.E, (int)w.n_chunks, trace_ctx());
 }
 
 cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
@@ -461,7 +470,8 @@ cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, 
   return launch_pdl(k_route_rank, grid, 128, 4 * w.E * sizeof(int32_t), st, ids, topk_w,
                     region<int>(ws, w.off_hdr), region<int32_t>(ws, w.off_chunk),
                     region<int32_t>(ws, w.off_row_of_slot), region<int32_t>(ws, w.off_slot_of_row),
-                    region<float>(ws, w.off_w_row), (int)w.S, (int)w.E, (int)w.n_chunks);
+                    region<float>(ws, w.off_w_row), (int)w.S, (int)w.E, (int)w.n_chunks,
+                    trace_ctx());
 }
 
 cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, void* dst,
@@ -469,7 +479,7 @@ cudaError_t launch_gather_rows(const Workspace& w, char* ws, const void* src, vo
   const unsigned grid = div_up(w.S_pad, 8);
   return launch_pdl(k_gather_rows, grid, 256, 0, st, reinterpret_cast<const uint4*>(src),
                     reinterpret_cast<uint4*>(dst), region<int32_t>(ws, w.off_slot_of_row),
-                    region<int>(ws, w.off_hdr), (int)w.K, (int)(w.H / 8));
+                    region<int>(ws, w.off_hdr), (int)w.K, (int)(w.H / 8), trace_ctx());
 }
 
 cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const float* weights,
@@ -481,14 +491,14 @@ cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const
                     region<int32_t>(ws, w.off_row_of_slot), weights,
                     reinterpret_cast<const uint4*>(extra), reinterpret_cast<const uint4*>(extra_lo),
                     reinterpret_cast<uint4*>(out), region<int>(ws, w.off_hdr), (int)w.T, (int)w.K,
-                    (int)(w.H / 8));
+                    (int)(w.H / 8), trace_ctx());
 }
 
 cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st) {
   const unsigned grid = div_up(w.S, 256);
   return launch_pdl(k_d_topk, grid, 256, 0, st, region<float>(ws, w.off_p_part),
                     region<int32_t>(ws, w.off_row_of_slot), d_topk, region<int>(ws, w.off_hdr),
-                    (int)w.S, (int)w.n_act_tiles, w.S_pad);
+                    (int)w.S, (int)w.n_act_tiles, w.S_pad, trace_ctx());
 }
 
 cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st) {
@@ -498,7 +508,7 @@ cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStrea
                     region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
                     region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
-                    region<int32_t>(ws, w.off_row_of_slot), (int)w.T);
+                    region<int32_t>(ws, w.off_row_of_slot), (int)w.T, trace_ctx());
 }
 
 cudaError_t launch_backward_check(const Workspace& w, char* ws, cudaStream_t st) {

@@ -52,7 +52,7 @@ def test_host_validation_without_device():
     assert _abi.mm_backward(d, 0, 16, 16, 16, 16, 16, 256, n, 16, 16, 16, 16, 0, 0) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_get_status(0, 0) == _abi.MM_ERR_WORKSPACE
     assert _abi.mm_status_string(_abi.MM_ERR_BAD_EXPERT_ID) == "expert id out of range"
-    assert _abi.mm_abi_version() == 2
+    assert _abi.mm_abi_version() == 3
     assert _abi.mm_status_string(_abi.MM_ERR_TOKENS_PER_EXPERT) == \
         "tokens_per_expert does not match topk_ids"
 
