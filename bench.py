@@ -419,14 +419,14 @@ def run_gpu(args):
         "gather_x": T * Hb + S * Hb, "gather_dy": T * Hb + S * Hb,
         # the slot rows, routing index and weight read, the token rows written
         "combine_y": S * Hb + T * Hb + 8 * S, "combine_dx": S * Hb + T * Hb + 4 * S,
-        # in: dy slot rows, bf16 gate|up, W_down, routing weight; out: bf16 [d_gate|d_up],
-        # bf16 w*h and one fp32 <g,h> per slot
-        "act_grad": S * (Hb + 4 * I + 4) + E * I * Hb + S * (4 * I + 2 * I + 4),
+        # in: dy slot rows, bf16 gate|up, W_down, routing weight; out: bf16 [d_gate|d_up] and
+        # one fp32 <g,h> per slot (w*h, which W2Grad reads, is written by GEMM1's epilogue)
+        "act_grad": S * (Hb + 4 * I + 4) + E * I * Hb + S * (4 * I + 4),
     }
-    # what this build's act_grad moves by design: fp32 gate|up in, and [d_gate|d_up] and w*h as
-    # bf16 hi + lo pairs out (the weight gradients' precision), plus one partial per column half
+    # what this build's act_grad moves by design: fp32 gate|up in, [d_gate|d_up] as bf16 hi + lo
+    # planes out (the weight gradients' precision), plus one partial per column half
     impl_bytes = {"act_grad": S * (Hb + 8 * I + 4) + E * I * Hb
-                  + S * (8 * I + 4 * I + 4 * 2 * ((I + 255) // 256))}
+                  + S * (8 * I + 4 * 2 * ((I + 255) // 256))}
     hbm_peak = peaks["hbm_gbs"]
     hbm_stages = {}
     for k, nbytes_k in algo_bytes.items():

@@ -161,6 +161,7 @@ struct Traits {
   // overlaps) and input_grad stayed the same; act_grad and the fused forward keep per-row state
   // over a CTA's 128 rows (<g,h> partials, ready counts)
   static constexpr bool HALF = (KIND == GK_GEMM1_SWIGLU);
+  static_assert(!HALF || (!WGRAD && !FUSED), "half units are row tiles of the row-grouped GEMM1");
   static_assert(!TRANSPOSED_OUT || WGRAD, "only a weight gradient is stored transposed");
   static constexpr int TN = BN;  // accumulator columns per tile
   static constexpr int B_BYTES = TN * BK * 2;
