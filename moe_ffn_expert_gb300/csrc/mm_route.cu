@@ -71,7 +71,9 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
 // owning a contiguous range of the chunk histograms; thread tid serves expert tid % E, so a
 // warp reads 32 consecutive experts of one chunk (coalesced). The P threads of an expert sum
 // their ranges, the expert totals are scanned across experts (plain and padded to BM rows),
-// and each thread then turns its range into running padded-row bases.
+// and each thread then turns its range into running padded-row bases. The row-tile, pair and
+// pad-row tables are written last, one warp per expert with coalesced stores (per-expert
+// threads writing them took most of the kernel's time: their stores were scattered).
 __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restrict__ chunk_cnt,
                                                      int32_t* __restrict__ counts,
                                                      int32_t* __restrict__ offsets,
@@ -179,37 +181,40 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
     }
   }
   __syncthreads();
-  if (!active) return;
-  // chunk histograms -> running padded-row base of each chunk (this thread's range)
-  const int po = po_s[e];
-  int run = po + before;
-  int k = k0;
-  for (; k + 8 <= k1; k += 8) {  // eight loads in flight, then the running sums
-    int v[8];
+  if (active) {
+    // chunk histograms -> running padded-row base of each chunk (this thread's range)
+    int run = po_s[e] + before;
+    int k = k0;
+    for (; k + 8 <= k1; k += 8) {  // eight loads in flight, then the running sums
+      int v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = chunk_cnt[(size_t)(k + i) * E + e];
+      for (int i = 0; i < 8; ++i) v[i] = chunk_cnt[(size_t)(k + i) * E + e];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      chunk_cnt[(size_t)(k + i) * E + e] = run;
-      run += v[i];
+      for (int i = 0; i < 8; ++i) {
+        chunk_cnt[(size_t)(k + i) * E + e] = run;
+        run += v[i];
+      }
+    }
+    for (; k < k1; ++k) {
+      const int v = chunk_cnt[(size_t)k * E + e];
+      chunk_cnt[(size_t)k * E + e] = run;
+      run += v;
     }
   }
-  for (; k < k1; ++k) {
-    const int v = chunk_cnt[(size_t)k * E + e];
-    chunk_cnt[(size_t)k * E + e] = run;
-    run += v;
-  }
-  // the expert's row tiles, row-tile pairs and pad-row markers, split over its P threads
-  const int pcount = (total + BM - 1) / BM * BM;
-  for (int t = po / BM + j; t < (po + pcount) / BM; t += P) tile_expert[t] = e;
-  const int ntile = pcount / BM, qo = qo_s[e];
-  for (int i = j; i < (ntile + 1) / 2; i += P) {
-    const int t0 = po / BM + 2 * i;
-    pair_tile[qo + i] = 2 * i + 1 < ntile ? t0 : ~t0;
-  }
-  for (int r = po + total + j; r < po + pcount; r += P) {
-    slot_of_row[r] = -1;
-    w_row[r] = 0.0f;
+  // each expert's row tiles, row-tile pairs and pad-row markers: one warp per expert at a time,
+  // its lanes over consecutive entries, so that every store instruction is coalesced
+  for (int ex = warp; ex < E; ex += (int)(blockDim.x >> 5)) {
+    const int tot = tot_s[ex], po = po_s[ex], qo = qo_s[ex];
+    const int pcount = (tot + BM - 1) / BM * BM, ntile = pcount / BM;
+    for (int t = lane; t < ntile; t += 32) tile_expert[po / BM + t] = ex;
+    for (int i = lane; i < (ntile + 1) / 2; i += 32) {
+      const int t0 = po / BM + 2 * i;
+      pair_tile[qo + i] = 2 * i + 1 < ntile ? t0 : ~t0;
+    }
+    for (int r = po + tot + lane; r < po + pcount; r += 32) {
+      slot_of_row[r] = -1;
+      w_row[r] = 0.0f;
+    }
   }
 }
 

@@ -1,6 +1,6 @@
 """Seeded random layer shapes (ragged T, H and I multiples of 8, expert counts from 1 to 96,
 K up to 8, uniform and Zipf routing) through the C ABI: the default launches (CTA-pair MMAs,
-paired weight gradients when experts average 512 rows or more) equal the one-CTA launches bit
+paired weight gradients when experts average 256 rows or more) equal the one-CTA launches bit
 for bit, and both meet the float64 oracle's bounds (routing bit-exact)."""
 import random
 
