@@ -516,6 +516,8 @@ def run_gpu(args):
         "cpu_baseline": cpu,
     }
     if args.trace and rank == 0:  # one more step, traced, after every timed leg
+        import numpy as np
+
         from moe_ffn_expert_gb300 import trace as mm_trace
         tb = mm_trace.TraceBuffer(capacity=1 << 21, device=dev)
         tb.start()
@@ -535,6 +537,7 @@ def run_gpu(args):
                  "time during which the same SM's (or pair's) MMA issuer held the next tile.")
         with open(args.trace, "w") as f:
             f.write(mm_trace.report(summ, title, notes))
+        np.save(os.path.splitext(args.trace)[0] + ".npy", recs)  # the raw records beside it
         line["trace"] = {"file": args.trace, "records": int(recs.size), "dropped": tb.dropped}
     print(json.dumps(line), flush=True)
 

@@ -175,7 +175,7 @@ cudaError_t bind_context() {
 TraceCtx trace_ctx() { return t_trace_cur; }
 static_assert(sizeof(mm_trace_record) == 32 && offsetof(mm_trace_record, unit) == 8 &&
                   offsetof(mm_trace_record, launch) == 12 && offsetof(mm_trace_record, t0) == 16,
-              "trace record layout (written by trace_put as two 16-byte words)");
+              "trace record layout (written by trace_end as two 16-byte words)");
 
 void note_error(const char* fmt, ...) {
   va_list ap;

@@ -31,33 +31,40 @@ __device__ __forceinline__ uint32_t sm_id() {
 // ---- optional trace (mm_trace_record layout of mm.h: stage | role << 16, sm | rank << 16,
 // unit, launch, t0, t1 as little-endian words)
 
-// The start time of a traced span (0 when tracing is off: no clock read).
-__device__ __forceinline__ uint64_t trace_start(const TraceCtx& tc) {
-  return tc.buf != nullptr ? globaltimer_ns() : 0ull;
+// A traced span: its record slot, reserved when the span starts (the atomic's round trip then
+// overlaps the span instead of delaying its end), and its start time. Tracing off: no atomic,
+// no clock read.
+struct TraceSpan {
+  uint32_t slot;
+  uint64_t t0;
+};
+
+__device__ __forceinline__ TraceSpan trace_begin(const TraceCtx& tc) {
+  if (tc.buf == nullptr) return TraceSpan{0u, 0ull};
+  const uint32_t slot = atomicAdd(tc.buf, 1u);
+  return TraceSpan{slot, globaltimer_ns()};
 }
 
-// Appends one record [t0, now] of `role` for `unit`; a record past the buffer is only counted.
-__device__ __forceinline__ void trace_put(const TraceCtx& tc, uint32_t role, int unit,
-                                          uint32_t rank, uint64_t t0) {
-  if (tc.buf == nullptr) return;
+// Writes the span's record [t0, now] of `role` for `unit`; a slot past the buffer is only counted.
+__device__ __forceinline__ void trace_end(const TraceCtx& tc, const TraceSpan& sp, uint32_t role,
+                                          int unit, uint32_t rank) {
+  if (tc.buf == nullptr || sp.slot >= tc.cap) return;
   const uint64_t t1 = globaltimer_ns();
-  const uint32_t i = atomicAdd(tc.buf, 1u);
-  if (i >= tc.cap) return;
-  uint4* r = reinterpret_cast<uint4*>(tc.buf + 8 * (size_t)(i + 1));
+  uint4* r = reinterpret_cast<uint4*>(tc.buf + 8 * (size_t)(sp.slot + 1));
   r[0] = make_uint4(tc.stage | (role << 16), sm_id() | (rank << 16), (uint32_t)unit, tc.launch);
-  r[1] = make_uint4((uint32_t)t0, (uint32_t)(t0 >> 32), (uint32_t)t1, (uint32_t)(t1 >> 32));
+  r[1] = make_uint4((uint32_t)sp.t0, (uint32_t)(sp.t0 >> 32), (uint32_t)t1, (uint32_t)(t1 >> 32));
 }
 
-// One MM_TRACE_CTA record per CTA: started where it is constructed (after pdl_wait), recorded by
-// the CTA's first thread when it leaves the kernel, on whichever path it returns.
+// One MM_TRACE_CTA record per CTA: started where it is constructed (after pdl_wait) by the CTA's
+// first thread, recorded by that thread when it leaves the kernel, on whichever path it returns.
 struct TraceCta {
   const TraceCtx& tc;
-  uint64_t t0;
+  TraceSpan sp;
   uint32_t rank;
   __device__ __forceinline__ explicit TraceCta(const TraceCtx& c, uint32_t r = 0)
-      : tc(c), t0(trace_start(c)), rank(r) {}
+      : tc(c), sp(threadIdx.x == 0 ? trace_begin(c) : TraceSpan{0u, 0ull}), rank(r) {}
   __device__ __forceinline__ ~TraceCta() {
-    if (threadIdx.x == 0) trace_put(tc, MM_TRACE_CTA, (int)blockIdx.x, rank, t0);
+    if (threadIdx.x == 0) trace_end(tc, sp, MM_TRACE_CTA, (int)blockIdx.x, rank);
   }
 };
 

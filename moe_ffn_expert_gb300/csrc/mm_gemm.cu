@@ -575,15 +575,19 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   static_assert(GU_BUFS == 1 || GU_BUFS == 2, "gate|up staging depth");
   int ld_tile = first, ld_c = c0;  // next (unit, chunk) to load
   uint32_t issued = 0;             // chunks loaded so far (the next goes to buffer issued % GU_BUFS)
+  // ld_tile decoded once per unit (decoding it for every chunk put the table reads' latency
+  // in front of each chunk's load)
+  bool ld_v;
+  Tile tn{};
+  if (first < total) tn = tile_at(first, ld_v);
   auto issue_next = [&]() {
-    bool v;
-    while (ld_tile < total && ld_c >= chunk_end(tile_at(ld_tile, v).n0)) {
+    while (ld_tile < total && ld_c >= chunk_end(tn.n0)) {
       ld_tile += step;
       ld_c = c0;
+      if (ld_tile < total) tn = tile_at(ld_tile, ld_v);
     }
     if (ld_tile >= total) return;
     if (lane == 0) {
-      const Tile tn = tile_at(ld_tile, v);
       const uint32_t b = issued % GU_BUFS;
       const uint32_t bar = gbar + 8u * b, dst = gbuf + b * GU_CHUNK_BYTES;
       fence_proxy_async_smem();  // the buffer's previous contents were read by the warp
@@ -599,11 +603,12 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   uint32_t acc_it = 0, used = 0;
   bool failed = false;
   uint8_t* out_row = obuf_ptr + lane * 32;
-  uint64_t ep_t0 = 0;  // the first epilogue warp's span on each accumulator
+  TraceSpan ep_sp{0u, 0ull};  // the first epilogue warp's span on each accumulator
+  bool ep_open = false;
   int ep_unit = 0;
   auto ep_close = [&]() {
-    if (ep_t0 != 0 && lane == 0) trace_put(a.trace, MM_TRACE_EPILOGUE, ep_unit, rank, ep_t0);
-    ep_t0 = 0;
+    if (ep_open && lane == 0) trace_end(a.trace, ep_sp, MM_TRACE_EPILOGUE, ep_unit, rank);
+    ep_open = false;
   };
   for (int tile = first; tile < total; tile += step) {
     ep_close();
@@ -619,8 +624,9 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
     }
     __syncwarp();
     tc_fence_after();
-    if (warp == 2) {
-      ep_t0 = trace_start(a.trace);
+    if (warp == 2 && a.trace.buf != nullptr) {
+      if (lane == 0) ep_sp = trace_begin(a.trace);
+      ep_open = true;
       ep_unit = tile;
     }
     const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * BN;
@@ -1136,7 +1142,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t tm0 = trace_start(a.trace);
+        const TraceSpan tsp = trace_begin(a.trace);
         const uint32_t d = tmem_base + buf * TR::TN;
         for (int kb = 0; kb < t.kiters; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -1183,7 +1189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           else
             umma_commit(accf_bar(buf));
         }
-        trace_put(a.trace, MM_TRACE_MAINLOOP, tile, rank, tm0);
+        trace_end(a.trace, tsp, MM_TRACE_MAINLOOP, tile, rank);
         ++acc_it;
       }
     }
@@ -1210,11 +1216,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     uint32_t acc_it = 0;
     // the first epilogue warp's span on each accumulator, closed when the warp moves on
-    uint64_t ep_t0 = 0;
+    TraceSpan ep_sp{0u, 0ull};
+    bool ep_open = false;
     int ep_unit = 0;
     auto ep_close = [&]() {
-      if (ep_t0 != 0 && lane == 0) trace_put(a.trace, MM_TRACE_EPILOGUE, ep_unit, rank, ep_t0);
-      ep_t0 = 0;
+      if (ep_open && lane == 0) trace_end(a.trace, ep_sp, MM_TRACE_EPILOGUE, ep_unit, rank);
+      ep_open = false;
     };
     for (int tile = first; tile < total; tile += step) {
       ep_close();
@@ -1238,8 +1245,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
       tc_fence_after();
-      if (warp == 2) {
-        ep_t0 = trace_start(a.trace);
+      if (warp == 2 && a.trace.buf != nullptr) {
+        if (lane == 0) ep_sp = trace_begin(a.trace);
+        ep_open = true;
         ep_unit = tile;
       }
       const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + buf * TR::TN;
