@@ -22,9 +22,10 @@
 // thousands), so a bf16 rounding of every row of an operand would leave errors of ~0.5% of the
 // gradient's rms. The forward therefore keeps the gate|up accumulators in fp32 and writes w*h,
 // and the act_grad epilogue [d_gate|d_up], as two bf16 planes, hi = bf16(v) and
-// lo = bf16(v - hi), which together carry ~16 mantissa bits (GEMM2 and input_grad read hi only). Both weight gradients put that pair
-// on the A side ("x2" above) and issue two MMAs per k-step (hi and lo against the same B tile)
-// into one fp32 accumulator; W1_GRAD therefore computes dW_up^T and its epilogue transposes.
+// lo = bf16(v - hi), which together carry ~16 mantissa bits (GEMM2 and input_grad read hi
+// only). Both weight gradients put that pair on the A side ("x2" above) and issue two MMAs per
+// k-step (hi and lo against the same B tile) into one fp32 accumulator; W1_GRAD therefore
+// computes dW_up^T and its epilogue transposes.
 // Their stages hold A hi, A lo and B: 64 KB, three of them.
 //
 // Row-grouped kinds walk 128-row tiles of the expert-sorted (padded) row buffers; each tile
@@ -36,7 +37,8 @@
 // CTA pairs (template argument PAIR = 2, the default for GEMM1, GEMM2, ACT_GRAD, INPUT_GRAD and
 // long weight gradients): two CTAs of a cluster share one 256 x 256 tcgen05.mma.cta_group::2 per
 // 16-deep step. Each holds its own 128 rows of A and half of B's columns (32 KB stages, six
-// deep; 48 KB and four deep for the split weight gradients), both CTAs' TMA loads complete on
+// deep, four for act_grad beside its epilogue's staging; 48 KB and four deep for the split
+// weight gradients), both CTAs' TMA loads complete on
 // the even CTA's stage barrier, the even CTA's MMA thread issues the MMAs and signals its
 // commits to both CTAs' barriers, and each CTA's epilogue drains its own 128 accumulator rows.
 // Every TMA load of a CTA writes only its own shared memory and reads only this GPU's memory.

@@ -133,3 +133,38 @@ def test_trace_overflow_and_off():
     torch.cuda.synchronize()
     assert torch.equal(buf[:4], head)
     assert (buf[nbytes:] == 0xAB).all()
+
+
+def test_trace_of_the_one_launch_forward_and_a_shared_expert():
+    """The one-launch forward records one mainloop per GEMM1 and per GEMM2 unit in a single
+    launch; a shared expert's seven launches (its tables and GEMMs) carry its stage."""
+    T, H, I, E, K = 1500, 256, 256, 6, 2
+    w = synth.small("trace_fused", T, H, I, E, K, seed=93)
+    inp = make_inputs(w)
+    names = trace.stage_names()
+    tb = trace.TraceBuffer(1 << 16)
+    tb.start()
+    out = run_layer(inp, flags=_abi.MM_FLAG_FUSED_FORWARD_GEMMS, backward=False)
+    recs = tb.stop()
+    assert out["status"] == _abi.MM_OK and tb.dropped == 0
+    stages = [names[int(recs["stage"][recs["launch"] == lid][0])]
+              for lid in sorted(set(recs["launch"].tolist()))]
+    assert stages == ["route_count", "route_scan", "route_rank", "gather_x", "gemm1_gemm2",
+                      "combine_y"]
+    counts, _, _ = export_routing(out, E, T * K)
+    pairs = sum(cdiv(cdiv(int(c), 128), 2) for c in counts.tolist())
+    fused = recs[recs["stage"] == names.index("gemm1_gemm2")]
+    ml = fused[fused["role"] == _abi.MM_TRACE_MAINLOOP]
+    assert sorted(ml["unit"].tolist()) == list(range(pairs * (cdiv(I, 128) + cdiv(H, 256))))
+
+    su, sd = synth.shared_up(w, 384, device="cuda"), synth.shared_down(w, 384, device="cuda")
+    tb.start()
+    out = run_layer(inp, shared=(su, sd))
+    recs = tb.stop()
+    assert out["status"] == _abi.MM_OK and tb.dropped == 0
+    shared = recs[recs["stage"] == names.index("shared_expert")]
+    assert len(set(shared["launch"].tolist())) == 7
+    # the shared expert's GEMMs are grouped GEMMs like the routed ones: mainloop records in six
+    # of its seven launches (not in its routing tables)
+    with_ml = {int(l) for l in shared["launch"][shared["role"] == _abi.MM_TRACE_MAINLOOP]}
+    assert len(with_ml) == 6
