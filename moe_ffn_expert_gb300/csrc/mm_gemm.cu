@@ -334,9 +334,9 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
 // the pair takes row tile mt0 + r. When an expert has an odd number of row tiles its last row
 // tile is a unit of its own: for GEMM1 an M = 128 MMA over the pair (HALF kinds: CTA r takes rows
 // 64 r .. 64 r + 63 of the tile; t.half = 1), for the other kinds an M = 256 MMA whose second CTA
-// loads other rows of the buffer (or zeros past it), takes part in the MMAs and stores nothing. Weight gradients: a unit is two 128-row tiles of the
-// weight (same expert, same column tile); a second tile past the weight's rows is likewise
-// computed and not stored.
+// loads other rows of the buffer (or zeros past it), takes part in the MMAs and stores nothing.
+// Weight gradients: a unit is two 128-row tiles of the weight (same expert, same column tile);
+// a second tile past the weight's rows is likewise computed and not stored.
 template <int KIND>
 __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
   if constexpr (Traits<KIND>::WGRAD) {
@@ -542,9 +542,10 @@ __device__ __forceinline__ void act_grad_chunk(uint32_t taddr, const float4 (&cu
 // act_grad epilogue of one warp: g = dy_slot W_down^T (from TMEM) and the SwiGLU backward.
 // The warp streams the (tile, 16-column chunk) pairs of its 32 rows and column half. Input:
 // lane 0 TMA-loads the fp32 gate and up values of a chunk (two 32x16 boxes, 64-byte swizzle)
-// into one of the warp's GU_BUFS staging buffers (chunk i in buffer i % GU_BUFS, on that buffer's
-// barrier), GU_BUFS chunks ahead, and refills a buffer as soon as the warp has read it. Output: the warp writes the chunk's four 32x16 bf16 planes to its output
-// staging buffer and lane 0 stores them with TMA (the tensor maps clip columns past I).
+// into one of the warp's GU_BUFS staging buffers (chunk i in buffer i % GU_BUFS, on that
+// buffer's barrier), GU_BUFS chunks ahead, and refills a buffer as soon as the warp has read it.
+// Output: the warp writes the chunk's four 32x16 bf16 planes to its output staging buffer and
+// lane 0 stores them with TMA (the tensor maps clip columns past I).
 // PAIR = 2: the tiles are the CTA's halves of CTA-pair MMA tiles (units first, first + step, ..;
 // this CTA is `rank` of its pair); a half past the expert is consumed but stores nothing.
 template <int PAIR, int GU_BUFS>
