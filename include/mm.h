@@ -247,7 +247,7 @@ int mm_abi_version(void);
  * CUDA events on its stream. mm_timing_read synchronises those events, writes for each stage
  * (up to max_stages) the summed milliseconds and the number of launches since the last read,
  * clears them, and returns the number of stages (MM_NUM_STAGES). mm_stage_name names a stage. */
-#define MM_NUM_STAGES 16
+#define MM_NUM_STAGES 17
 mm_status mm_timing_enable(int on);
 /* Restricts the timer to the stages whose bit (1 << stage) is set in stage_mask (default: all),
  * so that a timed run can bracket only the kernel it reports on. */

@@ -30,7 +30,7 @@ MM_FLAG_FUSED_FORWARD_GEMMS = 0x8
 MM_FLAG_FUSED_COMBINE = 0x10
 MM_FLAG_FORWARD_ONLY = 0x20
 MM_FLAG_SINGLE_CTA_TILES = 0x100
-MM_NUM_STAGES = 16
+MM_NUM_STAGES = 17
 MM_TRACE_CTA = 0
 MM_TRACE_MAINLOOP = 1
 MM_TRACE_EPILOGUE = 2

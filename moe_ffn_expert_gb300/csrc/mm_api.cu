@@ -6,8 +6,9 @@
 //   (GEMM1 and GEMM2 in one launch with MM_FLAG_FUSED_FORWARD_GEMMS; the combine inside GEMM2
 //   with MM_FLAG_FUSED_COMBINE).
 // Backward (§2.2): gather dy rows -> act_grad + SwiGLU backward -> d_topk_weights ->
-//   W2Grad -> input_grad -> [shared expert act_grad, W2Grad, input_grad] ->
-//   combine dx (side stream) || W1Grad -> [shared expert W1Grad].
+//   W2Grad (-> sum of split experts' partial slices) -> input_grad ->
+//   [shared expert act_grad, W2Grad, input_grad] ->
+//   combine dx (side stream) || W1Grad (-> sum of partial slices) -> [shared expert W1Grad].
 // The host never waits on the device here (except the optional id pre-check); the caller's
 // stream orders everything (the side stream is forked from it and joined back within the
 // call). The two-phase size query / execute split mirrors §2.3.
@@ -107,7 +108,7 @@ const char* kStageNames[ST_COUNT] = {
     "route_count", "route_scan",  "route_rank", "gather_x",   "gemm1_swiglu",
     "gemm2",       "combine_y",   "gather_dy",  "act_grad",   "d_topk",
     "w2_grad",     "input_grad",  "combine_dx", "w1_grad",    "shared_expert",
-    "gemm1_gemm2"};
+    "gemm1_gemm2", "wgrad_reduce"};
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -225,6 +226,13 @@ bool plan_workspace(const mm_dims& d, Workspace* w, bool direct_rows) {
   p.off_dgu_lo = take((size_t)p.S_pad * 2 * d.I * 2);
   p.off_p_part = take((size_t)p.n_act_tiles * p.S_pad * sizeof(float));
   p.off_o_lo = take(direct_rows ? (size_t)p.S_pad * d.H * 2 : 0);
+  if (!direct_rows) {  // the partial slices reuse the o / dx and dy row buffers
+    p.wg_slices[WG_W2] = std::min<int64_t>(1024, (p.S_pad * d.H * 2) / (d.I * d.H * 4));
+    p.wg_slices[WG_W1] = std::min<int64_t>(1024, (p.S_pad * d.H * 2) / (2 * d.I * d.H * 4));
+  }
+  p.wg_slices_max = std::max(p.wg_slices[WG_W2], p.wg_slices[WG_W1]);
+  p.off_wg_plan = take((size_t)2 * (d.E + p.wg_slices_max) * 16);
+  p.off_wg_red = take((size_t)2 * d.E * 16);
   p.total = off;
   *w = p;
   return true;
@@ -504,6 +512,13 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   c.accumulate = accumulate;
   c.paired = wgrad_pair;
   MM_TRY(timed(ST_W2_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  // split experts' W2Grad partial slices (in the o / dx row buffer) summed into the output
+  // before input_grad writes its dx rows there
+  if (wgrad_split_possible(w, WG_W2))
+    MM_TRY(timed(ST_WGRAD_REDUCE, st, [&] {
+      return launch_wgrad_reduce(w, ws, WG_W2, d_down_proj_weight, c.wgrad_f32 != 0,
+                                 accumulate != 0, st);
+    }));
   c.kind = GK_INPUT_GRAD;
   c.d_w = nullptr;
   c.accumulate = 0;
@@ -548,7 +563,12 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   c.d_w = d_up_proj_weight;
   c.accumulate = accumulate;
   c.paired = wgrad_pair;
-  const cudaError_t e_w1 = timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); });
+  cudaError_t e_w1 = timed(ST_W1_GRAD, st, [&] { return launch_gemm(w, ws, c, st); });
+  if (e_w1 == cudaSuccess && wgrad_split_possible(w, WG_W1))  // split experts' partial slices
+    e_w1 = timed(ST_WGRAD_REDUCE, st, [&] {
+      return launch_wgrad_reduce(w, ws, WG_W1, d_up_proj_weight, c.wgrad_f32 != 0,
+                                 accumulate != 0, st);
+    });
   MM_TRY(cudaEventRecord(side->join, side->s));  // the join is enqueued whatever happened above
   MM_TRY(cudaStreamWaitEvent(st, side->join, 0));
   MM_TRY(e_comb);

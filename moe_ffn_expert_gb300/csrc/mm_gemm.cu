@@ -84,6 +84,7 @@ struct alignas(128) EpiMaps {
   CUtensorMap out;  // the bf16 output of GEMM2, INPUT_GRAD and the weight gradients
   CUtensorMap out_lo;  // its lo part (GEMM2 / INPUT_GRAD with split_out)
   CUtensorMap a2, b2;  // the fused forward's second GEMM: h rows and W_down
+  CUtensorMap part;    // weight gradients: fp32 partial slices of split experts' row chunks
 };
 
 static_assert(offsetof(EpiMaps, out_lo) == offsetof(EpiMaps, out) + sizeof(CUtensorMap),
@@ -141,6 +142,8 @@ struct Args {
   int skip_gu;  // GEMM1: forward only, gate|up are not stored
   const int32_t* pair_tile;  // paired launches: first row tile of each pair (~tile: no second)
   TraceCtx trace;            // optional per-tile trace (trace.buf == nullptr: off)
+  const int4* wg_plan;       // weight gradients: the row chunks of this kind (see WgKind)
+  int wg_kind;               // WG_W2 or WG_W1
 };
 
 template <int KIND>
@@ -210,6 +213,7 @@ struct Tile {
   int klast;  // 16-deep MMA steps issued for the last reduction block (BK / 16 unless trimmed)
   int part;  // fused forward: 0 = GEMM1 + SwiGLU tile, 1 = GEMM2 tile
   int half;  // pair MMAs: 1 = an M = 128 unit over one row tile, this CTA's 64 rows from m0
+  int slot;  // weight gradients: the fp32 partial slice of a split expert's chunk, -1: the output
 };
 
 // Where one epilogue warp's share of a tile's accumulator sits and where it goes: 32 rows from
@@ -293,6 +297,7 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
   Tile t;
   t.part = 0;
   t.half = 0;
+  t.slot = -1;
   t.klast = BK / 16;
   if constexpr (Traits<KIND>::FUSED) {
     int mt, part, nt;
@@ -304,17 +309,22 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
     t.row0 = t.m0;
     t.kiters = part ? a.k2 : a.k_iters;
   } else if constexpr (Traits<KIND>::WGRAD) {
-    const int per_e = a.m_tiles_w * a.n_tiles_n;
-    t.e = tile / per_e;
-    const int rem = tile - t.e * per_e;
+    // tile = (row chunk of the plan, row tile of the weight, column tile); a chunk is an
+    // expert's rows or, for a split expert, a run of whole 64-row blocks of them
+    const int per_c = a.m_tiles_w * a.n_tiles_n;
+    const int c = tile / per_c;
+    const int rem = tile - c * per_c;
     const int mt = rem / a.n_tiles_n;
     const int nt = rem - mt * a.n_tiles_n;
+    const int4 ch = __ldg(a.wg_plan + c);  // {expert, first padded row, rows, slice}
+    t.e = ch.x;
     t.m0 = mt * BM;
     t.n0 = nt * Traits<KIND>::TN;
-    t.row0 = __ldg(a.poff + t.e);
-    // the reduction runs over the expert's rows only: whole blocks of BK rows, then as many
+    t.row0 = ch.y;
+    t.slot = ch.w;
+    // the reduction runs over the chunk's rows only: whole blocks of BK rows, then as many
     // 16-row MMA steps as the last block needs (its pad rows are zero and add nothing)
-    const int rows = __ldg(a.counts + t.e);
+    const int rows = ch.z;
     t.kiters = (rows + BK - 1) / BK;
     if (t.kiters > 0) t.klast = (rows - (t.kiters - 1) * BK + 15) / 16;
   } else {
@@ -340,14 +350,14 @@ __device__ __forceinline__ Tile decode_tile(const Args& a, int tile) {
 template <int KIND>
 __device__ __forceinline__ Tile decode_pair(const Args& a, int unit, uint32_t rank, bool& valid) {
   if constexpr (Traits<KIND>::WGRAD) {
-    // unit = (expert, pair of weight row tiles, column tile); rank r takes row tile 2p + r
+    // unit = (row chunk, pair of weight row tiles, column tile); rank r takes row tile 2p + r
     const int mp = (a.m_tiles_w + 1) / 2;
-    const int per_e = mp * a.n_tiles_n;
-    const int e = unit / per_e;
-    const int rem = unit - e * per_e;
+    const int per_c = mp * a.n_tiles_n;
+    const int c = unit / per_c;
+    const int rem = unit - c * per_c;
     const int p = rem / a.n_tiles_n;
     const int nt = rem - p * a.n_tiles_n;
-    Tile t = decode_tile<KIND>(a, (e * a.m_tiles_w + 2 * p) * a.n_tiles_n + nt);
+    Tile t = decode_tile<KIND>(a, (c * a.m_tiles_w + 2 * p) * a.n_tiles_n + nt);
     t.m0 += (int)rank * BM;
     valid = t.m0 < a.M;
     return t;
@@ -714,15 +724,20 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
 // W1Grad's accumulator holds dW_up^T (rows = columns of dW_up): its chunks are written to the
 // staging buffer transposed (lane = output column, value j = output row) and stored at the
 // swapped coordinates. `zero` stores zeros without reading TMEM (an expert with no rows).
-template <int KIND>
+// PART (weight gradients): the tile of a split expert's row chunk goes in fp32 to its partial
+// slice t.slot through `map` (the partial slices' map: the output's layout, the slice as the
+// third coordinate), never added in; the reduce kernel sums the slices into the output. Each
+// instantiation stores through the one map it is given (no choice between maps at run time).
+template <int KIND, bool PART = false>
 __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t,
                                                   const EpiGeom& eg, uint32_t tacc, int lane,
                                                   const CUtensorMap* map, uint32_t sbuf,
                                                   uint8_t* sbuf_ptr, uint32_t& chunk_no,
                                                   bool zero = false) {
   using TR = Traits<KIND>;
+  static_assert(!PART || TR::WGRAD, "partial slices are weight-gradient tiles");
   const int row0 = eg.row0;
-  const bool f32 = TR::WGRAD && a.wgrad_f32;
+  const bool f32 = TR::WGRAD && (PART || a.wgrad_f32);
   const bool split = !TR::WGRAD && a.split_out;
 #pragma unroll 1
   for (int c = 0; c < eg.nch; ++c) {
@@ -788,7 +803,9 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t,
       const uint32_t src = sbuf + b * OUT_TILE_BYTES;
       if constexpr (TR::WGRAD) {
         const int x = TR::TRANSPOSED_OUT ? row0 : n, y = TR::TRANSPOSED_OUT ? n : row0;
-        if (a.accumulate)
+        if (PART)
+          tma_store_3d(map, src, x, y, t.slot);
+        else if (a.accumulate)
           tma_reduce_add_3d(map, src, x, y, t.e);
         else
           tma_store_3d(map, src, x, y, t.e);
@@ -938,10 +955,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (failed_before) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = (PAIRED && TR::WGRAD) ? a.E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+  const int total = (PAIRED && TR::WGRAD)
+                        ? a.hdr[HDR_WG_CHUNKS + a.wg_kind] * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
                     : (PAIRED && TR::FUSED) ? a.hdr[HDR_NUM_MPAIRS] * (a.n_tiles_n + a.n2)
                     : PAIRED                ? a.hdr[HDR_NUM_MPAIRS] * a.n_tiles_n
-                    : TR::WGRAD             ? a.E * a.m_tiles_w * a.n_tiles_n
+                    : TR::WGRAD ? a.hdr[HDR_WG_CHUNKS + a.wg_kind] * a.m_tiles_w * a.n_tiles_n
                     : TR::FUSED ? a.hdr[HDR_NUM_MTILES] * (a.n_tiles_n + a.n2)
                                 : a.hdr[HDR_NUM_MTILES] * a.n_tiles_n;
   // work units of this CTA: tile (or pair) first, first + step, ...
@@ -974,6 +992,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
     if constexpr (TR::A_SPLIT || TR::GU_STAGING) tma_prefetch_desc(&tmL);
     if constexpr (TR::OUT_STAGING) tma_prefetch_desc(&em.out);
+    if constexpr (TR::WGRAD) tma_prefetch_desc(&em.part);
     if constexpr (TR::FUSED) {
       tma_prefetch_desc(&em.a2);
       tma_prefetch_desc(&em.b2);
@@ -1295,9 +1314,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++acc_it;
         continue;
       }
-      if constexpr (TR::OUT_STAGING)
+      if constexpr (TR::WGRAD) {
+        if (t.slot >= 0)  // a split expert's row chunk: its fp32 partial slice
+          staged_store_tile<KIND, true>(a, t, epi_geom<false>(t, q, hf, TR::TN), tacc, lane,
+                                        &em.part, sbuf, smem_raw + (sbuf - raw), chunk_no);
+        else
+          staged_store_tile<KIND>(a, t, epi_geom<false>(t, q, hf, TR::TN), tacc, lane, &em.out,
+                                  sbuf, smem_raw + (sbuf - raw), chunk_no);
+      } else if constexpr (TR::OUT_STAGING) {
         staged_store_tile<KIND>(a, t, epi_geom<false>(t, q, hf, TR::TN), tacc, lane, &em.out,
                                 sbuf, smem_raw + (sbuf - raw), chunk_no);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) release_acc(buf);
@@ -1584,7 +1611,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
       a.ld0 = H;
       a.out_expert_stride = I * H;
-      tiles_max = E * a.m_tiles_w * a.n_tiles_n;
+      a.wg_kind = WG_W2;
+      tiles_max = (E + w.wg_slices[WG_W2]) * a.m_tiles_w * a.n_tiles_n;
       break;
     case GK_W1_GRAD:  // accumulates dW_up^T: rows = the 2I columns of dW_up, columns = H
       ok = map_rows(&ta, ws + w.off_dgu, 2 * I, S_pad, 64, 64) &&
@@ -1598,12 +1626,14 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       a.out0 = reinterpret_cast<__nv_bfloat16*>(c.d_w);
       a.ld0 = 2 * I;
       a.out_expert_stride = H * 2 * I;
-      tiles_max = E * a.m_tiles_w * a.n_tiles_n;
+      a.wg_kind = WG_W1;
+      tiles_max = (E + w.wg_slices[WG_W1]) * a.m_tiles_w * a.n_tiles_n;
       break;
   }
   if (!ok) return cudaErrorInvalidValue;
   if (!has_lo) tl = ta;  // unused by the kinds without a lo plane or M = 128 units
   if (!has_em) em.dgu_hi = em.dgu_lo = ta;  // unused but initialised
+  if constexpr (!Traits<KIND>::WGRAD) em.part = ta;                      // unused but initialised
   if constexpr (!Traits<KIND>::FUSED) em.a2 = em.b2 = ta;                // unused but initialised
   if constexpr (Traits<KIND>::OUT_STAGING) {
     // bf16 output in boxes of 32 rows x 32 columns, 64-byte swizzle
@@ -1627,6 +1657,17 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
                     a.wgrad_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : SW))
         return cudaErrorInvalidValue;
       em.out_lo = em.out;  // unused but initialised
+      // the row chunks of this kind's plan, and the fp32 partial slices of split experts: the
+      // output's layout with the slice as the third coordinate, in the o / dx row buffer
+      // (W2Grad) or the dy row buffer (W1Grad), which are free while these kernels run
+      const int k = a.wg_kind;
+      a.wg_plan = reinterpret_cast<const int4*>(ws + w.off_wg_plan) + k * (E + w.wg_slices_max);
+      const size_t part_off = (k == WG_W1 && w.wg_slices[WG_W1] > 0) ? w.off_dy_slot : w.off_o;
+      const uint64_t dp[3] = {d3[0], d3[1], (uint64_t)std::max<int64_t>(1, w.wg_slices[k])};
+      const uint64_t sp[2] = {(uint64_t)a.ld0 * 4, (uint64_t)a.out_expert_stride * 4};
+      if (!make_map(&em.part, ws + part_off, 3, dp, sp, b3, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     } else {  // [S_pad][N]
       const uint64_t d2[2] = {(uint64_t)a.N, (uint64_t)S_pad};
       const uint64_t s2[1] = {(uint64_t)a.ld0 * 2};
@@ -1675,7 +1716,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
       max_clusters_of[dev].store(max_clusters, std::memory_order_relaxed);
     }
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int64_t units = Traits<KIND>::WGRAD ? E * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
+    const int64_t units = Traits<KIND>::WGRAD
+                              ? (E + w.wg_slices[a.wg_kind]) * ((a.m_tiles_w + 1) / 2) * a.n_tiles_n
                           : Traits<KIND>::FUSED ? (m_tiles_max + 1) / 2 * (a.n_tiles_n + a.n2)
                               : (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
@@ -1691,6 +1733,8 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
 }
 
 }  // namespace
+
+int device_sm_count() { return sm_count(); }
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st) {
   const int pair = c.paired;

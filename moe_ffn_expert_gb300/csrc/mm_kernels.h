@@ -98,4 +98,16 @@ void note_error(const char* fmt, ...);
 // every launcher passes it to its kernel.
 TraceCtx trace_ctx();
 
+// SMs of the current device (0 if it cannot be queried).
+int device_sm_count();
+
+// Whether the routing scan may split an expert's rows for weight-gradient `kind` (decided from
+// the sizes alone; when false no expert is split and no sum needs launching).
+bool wgrad_split_possible(const Workspace& w, int kind);
+
+// The sums of split weight gradients (see WgKind): out[e] for every split expert e of `kind`
+// from its fp32 partial slices, in chunk order; bf16 or fp32 output, optionally added in.
+cudaError_t launch_wgrad_reduce(const Workspace& w, char* ws, int kind, void* out, bool out_f32,
+                                bool accumulate, cudaStream_t st);
+
 }  // namespace mm

@@ -25,7 +25,28 @@ enum HeaderWord {
   HDR_BAD_SLOT = 2,    // first slot seen with an invalid expert id (diagnostics)
   HDR_NO_BACKWARD = 3, // nonzero: the forward kept no gate|up (MM_FLAG_FORWARD_ONLY)
   HDR_NUM_MPAIRS = 4,  // pairs of row tiles of one expert (the paired GEMMs' work units)
+  HDR_WG_CHUNKS = 5,   // 2 words: row chunks of the weight-gradient plan (W2Grad, W1Grad)
+  HDR_WG_SPLITS = 7,   // 2 words: experts whose weight gradient is split into several chunks
   HDR_WORDS = 64
+};
+
+// Weight-gradient plan (one per weight-gradient kind, written by the routing scan): the
+// reduction over an expert's rows runs as one or more row chunks. An expert whose rows are long
+// against the launch's average load per CTA pair is split into chunks of whole 64-row blocks;
+// each chunk's tile goes to an fp32 partial slice and a reduce kernel sums the slices in chunk
+// order. Chunk c: {expert, first padded row, rows, slice (-1: the output itself)}; split expert
+// j: {expert, first slice, slices, 0}. Split chunks come first, then the other experts' chunks
+// in expert order.
+enum WgKind { WG_W2 = 0, WG_W1 = 1 };
+
+// What the routing scan needs to write the plans (int32 quadruples).
+struct WgPlanArgs {
+  int32_t* plan;    // [2][plan_stride][4] row chunks
+  int32_t* red;     // [2][E][4] split experts
+  int units[2];     // CTA-pair work units per row chunk (row-tile pairs x column tiles)
+  int slices[2];    // partial slices that fit for each kind
+  int plan_stride;  // E + the larger slice count
+  int pairs;        // CTA pairs the weight-gradient launches run on
 };
 
 // Stage ids of the per-stage timer.
@@ -46,6 +67,7 @@ enum Stage {
   ST_W1_GRAD,
   ST_SHARED,     // every launch of the shared expert (forward and backward)
   ST_FWD_GEMMS,  // the fused GEMM1 + SwiGLU -> GEMM2 launch
+  ST_WGRAD_REDUCE,  // the sums of split weight gradients' partial slices
   ST_COUNT
 };
 static_assert(ST_COUNT == MM_NUM_STAGES, "stage table");
@@ -82,6 +104,13 @@ struct Workspace {
   size_t off_dgu_lo;   // bf16 [S_pad, 2I]  lo part of [d_gate | d_up]
   size_t off_p_part;   // fp32 [n_act_tiles, S_pad] per-column-half partials of <g, h>
   size_t off_o_lo;     // bf16 [S_pad, H]   direct-row layout only: lo part of o / dx rows
+  size_t off_wg_plan;  // int4 [2][E + wg_slices_max] weight-gradient row chunks (see WgKind)
+  size_t off_wg_red;   // int4 [2][E] split experts of each weight-gradient kind
+  // fp32 partial slices of split weight gradients: W2Grad's in the o / dx row buffer (free from
+  // the forward's combine until input_grad writes it), W1Grad's in the dy row buffer (free
+  // after act_grad and W2Grad); how many slices of each kind fit (0: no split)
+  int64_t wg_slices[2];
+  int64_t wg_slices_max;
   size_t total;
 };
 

@@ -15,6 +15,8 @@
 //          and writes the row-tile -> expert table and the pad-row markers;
 //   rank:  each warp replays its chunk in slot order, so a slot's row is its expert's base
 //          plus the number of earlier slots of that expert: a stable order in s.
+#include <algorithm>
+
 #include "mm_device.cuh"
 #include "mm_kernels.h"
 
@@ -67,6 +69,135 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
   for (int i = lane; i < E; i += 32) chunk_cnt[(size_t)chunk * E + i] = cnt[i];
 }
 
+// The weight-gradient plans (see WgKind), by one warp of the scan (a few sums and prefix sums
+// over the experts, 32 at a time). The launch's load per CTA pair is the sum over experts of
+// (64-row blocks x units per chunk) over the pairs; an expert with more than twice that many
+// blocks (and more than 32) is cut into chunks of about that many whole blocks, so that no unit
+// outlasts the average load by much. If the slices that needs do not fit, the threshold doubles
+// until they do (or nothing is split). The plan depends only on the routing and the sizes (not
+// on the CTA layout of the launches), so every launch form sums the same partials in the same
+// order.
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Exclusive prefix over the lanes of v (and, through `total`, the warp's sum).
+__device__ __forceinline__ int warp_excl(int v, int lane, int& total) {
+  int inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, d);
+    if (lane >= d) inc += y;
+  }
+  total = __shfl_sync(0xffffffffu, inc, 31);
+  return inc - v;
+}
+
+__device__ __forceinline__ int wgrad_chunks(int blocks, long long thr) {
+  if (blocks <= 2 * thr) return 1;
+  int s = (int)((blocks + thr - 1) / thr);
+  const int per = (blocks + s - 1) / s;  // whole blocks per chunk
+  return (blocks + per - 1) / per;
+}
+
+__device__ void wgrad_plan(int* hdr, const WgPlanArgs& wg, const int* tot_s, const int* po_s,
+                           int E) {
+  // a kind whose sizes rule out any split: one chunk per expert, every thread one expert
+  const int tid = threadIdx.x;
+  for (int k = 0; k < 2; ++k) {
+    if (wg.slices[k] >= 2) continue;
+    if (tid < E) {
+      int32_t* c = wg.plan + ((size_t)k * wg.plan_stride + tid) * 4;
+      c[0] = tid;
+      c[1] = po_s[tid];
+      c[2] = tot_s[tid];
+      c[3] = -1;
+    }
+    if (tid == 0) {
+      hdr[HDR_WG_CHUNKS + k] = E;
+      hdr[HDR_WG_SPLITS + k] = 0;
+    }
+  }
+  if ((wg.slices[0] < 2 && wg.slices[1] < 2) || tid >= 32) return;
+  const int lane = tid;
+  auto blocks_of = [&](int e) { return e < E ? (tot_s[e] + BK - 1) / BK : 0; };
+  int sum_blocks = 0;
+  for (int e0 = 0; e0 < E; e0 += 32) sum_blocks += warp_sum(blocks_of(e0 + lane));
+  for (int k = 0; k < 2; ++k) {
+    if (wg.slices[k] < 2) continue;
+    int32_t* plan = wg.plan + (size_t)k * wg.plan_stride * 4;
+    int32_t* red = wg.red + (size_t)k * E * 4;
+    long long thr = (long long)wg.units[k] * sum_blocks / (wg.pairs > 0 ? wg.pairs : 1);
+    if (thr < 16) thr = 16;
+    bool split = true;
+    for (int round = 0;; ++round) {  // warp-uniform: the chunk count is a warp sum
+      int need = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int s = wgrad_chunks(blocks_of(e0 + lane), thr);
+        need += warp_sum(s > 1 ? s : 0);
+      }
+      if (need <= wg.slices[k]) break;
+      if (round == 40) {
+        split = false;
+        break;
+      }
+      thr *= 2;
+    }
+    // totals first (split chunks come first in the table), then the entries
+    int n_split = 0, n_splitters = 0;
+    if (split)
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int s = wgrad_chunks(blocks_of(e0 + lane), thr);
+        n_split += warp_sum(s > 1 ? s : 0);
+        n_splitters += warp_sum(s > 1 ? 1 : 0);
+      }
+    int base_a = 0, base_b = 0, base_c = 0;  // running chunk, unsplit and splitter indices
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int blocks = blocks_of(e);
+      const int s = (split && e < E) ? wgrad_chunks(blocks, thr) : 1;
+      int ta, tb, tc;
+      const int xa = warp_excl(s > 1 ? s : 0, lane, ta);
+      const int xb = warp_excl((e < E && s == 1) ? 1 : 0, lane, tb);
+      const int xc = warp_excl(s > 1 ? 1 : 0, lane, tc);
+      if (e < E) {
+        const int rows = tot_s[e], po = po_s[e];
+        if (s > 1) {  // chunks base_a + xa .., each with the slice of its own index
+          const int per_rows = ((blocks + s - 1) / s) * BK;
+          for (int i = 0; i < s; ++i) {
+            const int ci = base_a + xa + i;
+            int32_t* c = plan + 4 * ci;
+            c[0] = e;
+            c[1] = po + i * per_rows;
+            c[2] = min(per_rows, rows - i * per_rows);
+            c[3] = ci;
+          }
+          int32_t* r = red + 4 * (base_c + xc);
+          r[0] = e;
+          r[1] = base_a + xa;
+          r[2] = s;
+          r[3] = 0;
+        } else {  // one chunk after every split chunk, in expert order
+          int32_t* c = plan + 4 * (n_split + base_b + xb);
+          c[0] = e;
+          c[1] = po;
+          c[2] = rows;
+          c[3] = -1;
+        }
+      }
+      base_a += ta;
+      base_b += tb;
+      base_c += tc;
+    }
+    if (lane == 0) {
+      hdr[HDR_WG_CHUNKS + k] = n_split + base_b;
+      hdr[HDR_WG_SPLITS + k] = n_splitters;
+    }
+  }
+}
+
 // One CTA of 1024 threads. Each expert gets P = 1024 / E threads (a power of two, 1 to 32), each
 // owning a contiguous range of the chunk histograms; thread tid serves expert tid % E, so a
 // warp reads 32 consecutive experts of one chunk (coalesced). The P threads of an expert sum
@@ -83,7 +214,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      float* __restrict__ w_row,
                                                      int32_t* __restrict__ pair_tile,
                                                      const int32_t* __restrict__ tpe, int E,
-                                                     int n_chunks, TraceCtx tc) {
+                                                     int n_chunks, WgPlanArgs wg, TraceCtx tc) {
   pdl_wait();
   const TraceCta trace_cta(tc);
   __shared__ int wsum[32], wsum_p[32], wsum_q[32];
@@ -216,6 +347,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
       w_row[r] = 0.0f;
     }
   }
+  wgrad_plan(hdr, wg, tot_s, po_s, E);
 }
 
 __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ ids,
@@ -416,6 +548,7 @@ __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts
                                                        int32_t* poff, int32_t* tile_expert,
                                                        int32_t* pair_tile, int32_t* slot_of_row,
                                                        float* w_row, int32_t* row_of_slot, int T,
+                                                       int32_t* wg_plan, int wg_plan_stride,
                                                        TraceCtx tc) {
   pdl_wait();
   const TraceCta trace_cta(tc);
@@ -423,7 +556,18 @@ __global__ void __launch_bounds__(256) k_shared_tables(int* hdr, int32_t* counts
   const int nm = Tp / BM;
   const int r = blockIdx.x * 256 + threadIdx.x;
   if (r < HDR_WORDS)  // every header word
-    hdr[r] = r == HDR_NUM_MTILES ? nm : r == HDR_NUM_MPAIRS ? (nm + 1) / 2 : 0;
+    hdr[r] = r == HDR_NUM_MTILES                                       ? nm
+             : r == HDR_NUM_MPAIRS                                     ? (nm + 1) / 2
+             : (r == HDR_WG_CHUNKS + WG_W2 || r == HDR_WG_CHUNKS + WG_W1) ? 1
+                                                                       : 0;
+  // weight-gradient plans: one row chunk, all T rows, stored to the output (never split)
+  if (r < 2) {
+    int32_t* c = wg_plan + 4 * (size_t)r * wg_plan_stride;
+    c[0] = 0;
+    c[1] = 0;
+    c[2] = T;
+    c[3] = -1;
+  }
   // row tiles 2i and 2i + 1 form pair i (~2i when the second is past the last row tile)
   if (r < (nm + 1) / 2) pair_tile[r] = 2 * r + 1 < nm ? 2 * r : ~(2 * r);
   if (r == 0) {
@@ -448,6 +592,59 @@ __global__ void k_backward_check(int* hdr) {
   if (hdr[HDR_NO_BACKWARD] != 0) set_status(hdr + HDR_STATUS, MM_ERR_INVALID_ARG);
 }
 
+// The sums of split weight gradients (see WgKind). Work item i = (split expert j, group of four
+// elements q of its M x N gradient): out[e] = the sum over the expert's chunks, in chunk order,
+// of their fp32 partial slices, rounded once to bf16 (or kept in fp32), or added into out the way
+// the direct path's reduce-add stores add (bf16: bf16(out + bf16(sum)); fp32: out + sum).
+// Grid-stride; with no split expert the launch returns at once.
+__global__ void __launch_bounds__(256) k_wgrad_reduce(const int* hdr, int kind,
+                                                      const int4* __restrict__ red,
+                                                      const float4* __restrict__ part, void* out,
+                                                      int64_t slice4, int out_f32, int accumulate,
+                                                      TraceCtx tc) {
+  pdl_wait();
+  const TraceCta trace_cta(tc);
+  if (hdr[HDR_STATUS] != 0) return;
+  const int64_t total = (int64_t)hdr[HDR_WG_SPLITS + kind] * slice4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(i / slice4);
+    const int64_t q = i - (int64_t)j * slice4;
+    const int4 r = __ldg(red + j);  // {expert, first slice, slices, 0}
+    float4 acc = __ldg(part + (int64_t)r.y * slice4 + q);
+    for (int s = 1; s < r.z; ++s) {
+      const float4 v = __ldg(part + (int64_t)(r.y + s) * slice4 + q);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t o = (int64_t)r.x * slice4 + q;
+    if (out_f32) {
+      float4* op = reinterpret_cast<float4*>(out) + o;
+      if (accumulate) {
+        const float4 b = *op;
+        acc.x = b.x + acc.x;
+        acc.y = b.y + acc.y;
+        acc.z = b.z + acc.z;
+        acc.w = b.w + acc.w;
+      }
+      *op = acc;
+    } else {
+      uint2* op = reinterpret_cast<uint2*>(out) + o;
+      float f[4] = {acc.x, acc.y, acc.z, acc.w};
+      if (accumulate) {
+        const uint2 b = *op;
+        const float old[4] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y)};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          f[u] = old[u] + __bfloat162float(__float2bfloat16_rn(f[u]));
+      }
+      *op = make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
+    }
+  }
+}
+
 inline unsigned div_up(int64_t a, int64_t b) { return (unsigned)((a + b - 1) / b); }
 
 }  // namespace
@@ -459,14 +656,46 @@ cudaError_t launch_route_count(const Workspace& w, char* ws, const int32_t* ids,
                     (int)w.E, (int)w.n_chunks, trace_ctx());
 }
 
+namespace {
+
+// CTA-pair units per row chunk of a weight-gradient kind (row-tile pairs x 256-column tiles).
+int64_t wgrad_units(const Workspace& w, int kind) {
+  const int64_t rows_w = kind == WG_W1 ? 2 * w.I : w.I;
+  return ((rows_w + BM - 1) / BM + 1) / 2 * ((w.H + BN - 1) / BN);
+}
+
+}  // namespace
+
+// Whether the plan of weight-gradient `kind` may split an expert, decided from the sizes alone:
+// an expert with distinct experts per token holds at most T rows (ceil(T / 64) blocks), and the
+// average load per CTA pair is at least units x floor(S / 64) / pairs blocks; a split needs the
+// first to exceed twice the second (and 32 blocks), and at least two partial slices. When it
+// cannot happen the scan writes one chunk per expert and no sum is launched. (Duplicate experts
+// in a token can make an expert longer than T rows; such an expert is then simply not split.)
+bool wgrad_split_possible(const Workspace& w, int kind) {
+  if (w.wg_slices[kind] < 2) return false;
+  const int64_t pairs = std::max(1, device_sm_count() / 2);
+  const int64_t thr = std::max<int64_t>(16, wgrad_units(w, kind) * (w.S / BK) / pairs);
+  return (w.T + BK - 1) / BK > 2 * thr;
+}
+
 cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* tokens_per_expert,
                               cudaStream_t st) {
+  WgPlanArgs wg{};
+  wg.plan = region<int32_t>(ws, w.off_wg_plan);
+  wg.red = region<int32_t>(ws, w.off_wg_red);
+  for (int k = 0; k < 2; ++k) {
+    wg.units[k] = (int)wgrad_units(w, k);
+    wg.slices[k] = wgrad_split_possible(w, k) ? (int)w.wg_slices[k] : 0;
+  }
+  wg.plan_stride = (int)(w.E + w.wg_slices_max);
+  wg.pairs = device_sm_count() / 2;
   return launch_pdl(k_route_scan, 1, 1024, 0, st, region<int>(ws, w.off_hdr),
                     region<int32_t>(ws, w.off_chunk), region<int32_t>(ws, w.off_counts),
                     region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
                     region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_pair_tile),
-                    tokens_per_expert, (int)w.E, (int)w.n_chunks, trace_ctx());
+                    tokens_per_expert, (int)w.E, (int)w.n_chunks, wg, trace_ctx());
 }
 
 cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
@@ -513,7 +742,8 @@ cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStrea
                     region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_pair_tile),
                     region<int32_t>(ws, w.off_slot_of_row), region<float>(ws, w.off_w_row),
-                    region<int32_t>(ws, w.off_row_of_slot), (int)w.T, trace_ctx());
+                    region<int32_t>(ws, w.off_row_of_slot), (int)w.T,
+                    region<int32_t>(ws, w.off_wg_plan), (int)(w.E + w.wg_slices_max), trace_ctx());
 }
 
 cudaError_t launch_backward_check(const Workspace& w, char* ws, cudaStream_t st) {
@@ -527,6 +757,21 @@ cudaError_t launch_export_rows(const Workspace& w, const char* ws, int32_t* out,
       region<int32_t>(ws, w.off_poff), region<int32_t>(ws, w.off_offsets), out,
       region<int>(ws, w.off_hdr), (int)w.S);
   return cudaGetLastError();
+}
+
+}  // namespace mm
+
+namespace mm {
+
+cudaError_t launch_wgrad_reduce(const Workspace& w, char* ws, int kind, void* out, bool out_f32,
+                                bool accumulate, cudaStream_t st) {
+  const int64_t mn = kind == WG_W1 ? 2 * w.I * w.H : w.I * w.H;  // elements of one gradient
+  const size_t part_off = (kind == WG_W1 && w.wg_slices[WG_W1] > 0) ? w.off_dy_slot : w.off_o;
+  const unsigned grid = (unsigned)std::max(1, device_sm_count() * 2);
+  return launch_pdl(k_wgrad_reduce, grid, 256, 0, st, region<int>(ws, w.off_hdr), kind,
+                    reinterpret_cast<const int4*>(ws + w.off_wg_red) + (size_t)kind * w.E,
+                    reinterpret_cast<const float4*>(ws + part_off), out, mn / 4,
+                    out_f32 ? 1 : 0, accumulate ? 1 : 0, trace_ctx());
 }
 
 }  // namespace mm

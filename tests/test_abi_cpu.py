@@ -95,7 +95,7 @@ def test_extended_entry_points_host_checks():
 
 def test_stage_table():
     names = [_abi._lib().mm_stage_name(i).decode() for i in range(_abi.MM_NUM_STAGES)]
-    assert names[0] == "route_count" and names[-1] == "gemm1_gemm2" and len(set(names)) == 16
+    assert names[0] == "route_count" and names[-1] == "wgrad_reduce" and len(set(names)) == 17
     assert _abi.mm_timing_read() == {n: (0.0, 0) for n in names}
 
 

@@ -264,3 +264,51 @@ def test_pair_mma_weight_grads_output_forms(bwd):
     if not bwd & ACC:
         assert torch.count_nonzero(out["dW_up"][-1]) == 0
         assert torch.count_nonzero(out["dW_down"][-1]) == 0
+
+
+@pytest.mark.parametrize("bwd", [0, F32, F32 | ACC, ACC])
+def test_split_weight_gradients(bwd):
+    """A hot expert (every token's first slot, 64 row blocks against an average load of 16 per
+    CTA pair) has both weight gradients split into four row chunks whose fp32 partial slices a
+    reduce kernel sums. The pair-MMA and one-CTA launches give the same bits; without
+    accumulation the result meets the oracle's bound, bf16(fp32 result) equals the bf16 result,
+    and with it the output is the base plus the once-rounded sum; the trace shows the chunks'
+    units and the two reduce launches."""
+    from moe_ffn_expert_gb300 import trace
+    w = synth.small("split", 4096, 256, 128, 8, 2, routing_kind="skew", seed=41)
+    inp = make_inputs(w)
+    base = {}
+    if bwd & ACC:
+        g = torch.Generator(device="cuda").manual_seed(7)
+        dt = torch.float32 if bwd & F32 else torch.bfloat16
+        base = {"d_up": torch.randn(inp["w_up"].shape, generator=g, device="cuda").to(dt),
+                "d_down": torch.randn(inp["w_down"].shape, generator=g, device="cuda").to(dt)}
+    ref = run_layer(inp, flags=SINGLE, bwd_flags=bwd | SINGLE,
+                    **{k: v.clone() for k, v in base.items()})
+    tb = trace.TraceBuffer(1 << 16)
+    tb.start()
+    out = run_layer(inp, bwd_flags=bwd, **{k: v.clone() for k, v in base.items()})
+    recs = tb.stop()
+    assert out["status"] == _abi.MM_OK and ref["status"] == _abi.MM_OK
+    for k in ("dW_up", "dW_down", "dx", "d_topk_weights"):
+        assert torch.equal(out[k], ref[k]), k
+    names = trace.stage_names()
+    for st in ("w2_grad", "w1_grad"):  # 4 chunks of expert 0 + experts 1..5 (6, 7 are empty)
+        r = recs[recs["stage"] == names.index(st)]
+        assert (r["role"] == _abi.MM_TRACE_MAINLOOP).sum() == 9, st
+    assert len(set(recs["launch"][recs["stage"] == names.index("wgrad_reduce")].tolist())) == 2
+    if not bwd & ACC:
+        h = {k: v.cpu() for k, v in inp.items()}
+        g = oracle.backward(h["x"], h["topk_ids"], h["topk_weights"], h["w_up"], h["w_down"],
+                            h["dy"])
+        assert_close("dW_up", out["dW_up"], g["dW_up"])
+        assert_close("dW_down", out["dW_down"], g["dW_down"])
+        if bwd & F32:
+            plain = run_layer(inp)
+            for k in ("dW_up", "dW_down"):
+                assert torch.equal(out[k].to(torch.bfloat16), plain[k]), k
+    else:
+        plain = run_layer(inp, bwd_flags=bwd & F32)
+        for k, b in (("dW_up", base["d_up"]), ("dW_down", base["d_down"])):
+            want = b + plain[k] if bwd & F32 else (b.float() + plain[k].float()).to(torch.bfloat16)
+            assert torch.equal(out[k], want), k
