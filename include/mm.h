@@ -147,7 +147,10 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
  * and the routing are read back from the workspace; x itself is only checked). A backward only
  * reads what mm_forward kept (routing, dispatched x rows, gate|up) and overwrites its own scratch,
  * so one forward may be followed by several backwards (another dy: a retained autograd graph),
- * each giving what a single one would, bit for bit. */
+ * each giving what a single one would, bit for bit. An expert with far more rows than the
+ * average (skewed routing) may have its weight-gradient reduction cut into row chunks whose fp32
+ * partial sums are added in a fixed order before the output's one rounding: still deterministic,
+ * and the same in every CTA layout. */
 mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
                       const float* topk_weights, const void* up_proj_weight,
                       const void* down_proj_weight, void* workspace, size_t workspace_bytes,
