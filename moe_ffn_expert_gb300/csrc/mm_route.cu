@@ -69,14 +69,7 @@ __global__ void __launch_bounds__(128) k_route_count(const int32_t* __restrict__
   for (int i = lane; i < E; i += 32) chunk_cnt[(size_t)chunk * E + i] = cnt[i];
 }
 
-// The weight-gradient plans (see WgKind), by one warp of the scan (a few sums and prefix sums
-// over the experts, 32 at a time). The launch's load per CTA pair is the sum over experts of
-// (64-row blocks x units per chunk) over the pairs; an expert with more than twice that many
-// blocks (and more than 32) is cut into chunks of about that many whole blocks, so that no unit
-// outlasts the average load by much. If the slices that needs do not fit, the threshold doubles
-// until they do (or nothing is split). The plan depends only on the routing and the sizes (not
-// on the CTA layout of the launches), so every launch form sums the same partials in the same
-// order.
+// Sum of v over the warp's lanes.
 __device__ __forceinline__ int warp_sum(int v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -95,6 +88,8 @@ __device__ __forceinline__ int warp_excl(int v, int lane, int& total) {
   return inc - v;
 }
 
+// Chunks for an expert of `blocks` 64-row blocks at threshold `thr` blocks: one unless the
+// expert has more than twice that, else about blocks / thr chunks of equal whole blocks.
 __device__ __forceinline__ int wgrad_chunks(int blocks, long long thr) {
   if (blocks <= 2 * thr) return 1;
   int s = (int)((blocks + thr - 1) / thr);
@@ -102,9 +97,17 @@ __device__ __forceinline__ int wgrad_chunks(int blocks, long long thr) {
   return (blocks + per - 1) / per;
 }
 
+// The weight-gradient plans (see WgKind), at the end of the routing scan. A kind whose sizes rule
+// out any split (slices < 2, decided on the host) gets one chunk per expert from every thread at
+// once. Otherwise one warp plans it (a few sums and prefix sums over the experts, 32 at a time):
+// the launch's load per CTA pair is the sum over experts of (64-row blocks x units per chunk)
+// over the pairs; an expert with more than twice that many blocks (and more than 32) is cut into
+// chunks of about that many whole blocks, so that no unit outlasts the average load by much. If
+// the slices that needs do not fit, the threshold doubles until they do (or nothing is split).
+// The plan depends only on the routing and the sizes (not on the CTA layout of the launches), so
+// every launch form sums the same partials in the same order.
 __device__ void wgrad_plan(int* hdr, const WgPlanArgs& wg, const int* tot_s, const int* po_s,
                            int E) {
-  // a kind whose sizes rule out any split: one chunk per expert, every thread one expert
   const int tid = threadIdx.x;
   for (int k = 0; k < 2; ++k) {
     if (wg.slices[k] >= 2) continue;
