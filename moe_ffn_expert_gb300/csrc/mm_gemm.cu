@@ -817,6 +817,11 @@ __device__ __forceinline__ void staged_store_tile(const Args& a, const Tile& t,
     }
     ++chunk_no;
   }
+  // A bf16 tile may come next in this warp, and its chunks wait only for the store before last
+  // (one buffer each); the fp32 partial stores read both buffers, so they must be done reading.
+  if constexpr (PART) {
+    if (!a.wgrad_f32 && lane == 0) bulk_wait_read_all();
+  }
 }
 
 // Combine fused into GEMM2's epilogue, for one warp's 32 rows x 128 columns (chunk j of H)
