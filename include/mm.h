@@ -150,7 +150,8 @@ mm_status mm_forward(mm_dims d, const void* x, const int32_t* topk_ids,
  * each giving what a single one would, bit for bit. An expert with far more rows than the
  * average (skewed routing) may have its weight-gradient reduction cut into row chunks whose fp32
  * partial sums are added in a fixed order before the output's one rounding: still deterministic,
- * and the same in every CTA layout. */
+ * and the same in every CTA layout (the chunks follow the routing, the sizes and the device's SM
+ * count, so GPUs with different SM counts may round such an expert's gradient differently). */
 mm_status mm_backward(mm_dims d, const void* dy, const void* x, const int32_t* topk_ids,
                       const float* topk_weights, const void* up_proj_weight,
                       const void* down_proj_weight, void* workspace, size_t workspace_bytes,

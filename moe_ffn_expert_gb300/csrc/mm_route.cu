@@ -104,8 +104,8 @@ __device__ __forceinline__ int wgrad_chunks(int blocks, long long thr) {
 // over the pairs; an expert with more than twice that many blocks (and more than 32) is cut into
 // chunks of about that many whole blocks, so that no unit outlasts the average load by much. If
 // the slices that needs do not fit, the threshold doubles until they do (or nothing is split).
-// The plan depends only on the routing and the sizes (not on the CTA layout of the launches), so
-// every launch form sums the same partials in the same order.
+// The plan depends only on the routing, the sizes and the device's SM count (not on the CTA
+// layout of the launches), so every launch form sums the same partials in the same order.
 __device__ void wgrad_plan(int* hdr, const WgPlanArgs& wg, const int* tot_s, const int* po_s,
                            int E) {
   const int tid = threadIdx.x;

@@ -1,9 +1,10 @@
 """Many seeded random shapes, bit for bit: the default launches twice (run-to-run determinism),
-against the one-CTA launches, and a forward with the fused combine
-and/or the one-launch GEMM1 -> GEMM2 form. Different schedules of the same arithmetic must give
-the same bits, so a race or an unwritten read in any of them shows up as a difference. The
-oracle bounds are checked on fewer shapes in test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the
-count (default 300, a few seconds)."""
+against the one-CTA launches, a forward with the fused combine and/or the one-launch GEMM1 ->
+GEMM2 form, and a backward in another weight-gradient output form (fp32, and/or added into
+zeroed outputs), whose bf16 rounding must equal the default bf16 gradients. Different schedules
+of the same arithmetic must give the same bits, so a race or an unwritten read in any of them
+shows up as a difference. The oracle bounds are checked on fewer shapes in
+test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the count (default 300, a few seconds)."""
 import os
 import random
 
@@ -22,6 +23,8 @@ KEYS = ("y", "dx", "d_topk_weights", "dW_up", "dW_down")
 def test_soak_schedules_agree_bit_for_bit():
     n = int(os.environ.get("MM_SOAK_SHAPES", "300"))
     rng = random.Random(777)
+    rng_forms = random.Random(778)  # a stream of its own: the shapes stay those of seed 777
+    f32, acc = _abi.MM_FLAG_FP32_WEIGHT_GRADS, _abi.MM_FLAG_ACCUMULATE_WEIGHT_GRADS
     single = _abi.MM_FLAG_SINGLE_CTA_TILES
     fused = (_abi.MM_FLAG_FUSED_COMBINE, _abi.MM_FLAG_FUSED_FORWARD_GEMMS,
              _abi.MM_FLAG_FUSED_COMBINE | _abi.MM_FLAG_FUSED_FORWARD_GEMMS)
@@ -40,13 +43,21 @@ def test_soak_schedules_agree_bit_for_bit():
         runs = {"again": run_layer(inp),
                 "single": run_layer(inp, flags=single, bwd_flags=single)}
         f = run_layer(inp, flags=ff, backward=False)
-        if a["status"] != _abi.MM_OK or f["status"] != _abi.MM_OK or \
+        wf = rng_forms.choice([f32, acc, f32 | acc])
+        gdt = torch.float32 if wf & f32 else torch.bfloat16
+        g = run_layer(inp, bwd_flags=wf,
+                      d_up=torch.zeros(inp["w_up"].shape, dtype=gdt, device="cuda"),
+                      d_down=torch.zeros(inp["w_down"].shape, dtype=gdt, device="cuda"))
+        if a["status"] != _abi.MM_OK or f["status"] != _abi.MM_OK or g["status"] != _abi.MM_OK or \
                 any(r["status"] != _abi.MM_OK for r in runs.values()):
             failures.append((shape, "status"))
             continue
         diffs = [f"{name}:{k}" for name, r in runs.items() for k in KEYS if not torch.equal(a[k], r[k])]
         if not torch.equal(a["y"], f["y"]):
             diffs.append(f"fused 0x{ff:x}: y")
+        for k in ("dW_up", "dW_down"):
+            if not torch.equal(g[k].to(torch.bfloat16), a[k]):
+                diffs.append(f"weight-gradient form 0x{wf:x}: {k}")
         if diffs:
             failures.append((shape, diffs))
     assert not failures, failures[:10]
