@@ -1,7 +1,8 @@
 """Many seeded random shapes, bit for bit: the default launches twice (run-to-run determinism),
 against the one-CTA launches, a forward with the fused combine and/or the one-launch GEMM1 ->
 GEMM2 form, and a backward in another weight-gradient output form (fp32, and/or added into
-zeroed outputs), whose bf16 rounding must equal the default bf16 gradients. Different schedules
+zeroed outputs), whose bf16 rounding must equal the default bf16 gradients; every fourth shape
+also runs with a shared expert of random size, default against one-CTA launches. Different schedules
 of the same arithmetic must give the same bits, so a race or an unwritten read in any of them
 shows up as a difference. The oracle bounds are checked on fewer shapes in
 test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the count (default 300, a few seconds)."""
@@ -58,6 +59,17 @@ def test_soak_schedules_agree_bit_for_bit():
         for k in ("dW_up", "dW_down"):
             if not torch.equal(g[k].to(torch.bfloat16), a[k]):
                 diffs.append(f"weight-gradient form 0x{wf:x}: {k}")
+        if i % 4 == 3:  # a shared expert: its own sub-workspace, tables and seven launches
+            I_s = 8 * rng_forms.randint(1, 64)
+            w = synth.small("soak", T, H, I, E, K, routing_kind=kind, seed=5000 + i)
+            sh = (synth.shared_up(w, I_s, device="cuda"), synth.shared_down(w, I_s, device="cuda"))
+            sa = run_layer(inp, shared=sh)
+            sb = run_layer(inp, shared=sh, flags=single, bwd_flags=single)
+            if sa["status"] != _abi.MM_OK or sb["status"] != _abi.MM_OK:
+                diffs.append("shared: status")
+            else:
+                diffs += [f"shared I_s={I_s}: {k}" for k in KEYS + ("dS_up", "dS_down")
+                          if not torch.equal(sa[k], sb[k])]
         if diffs:
             failures.append((shape, diffs))
     assert not failures, failures[:10]
