@@ -443,6 +443,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// 1 / (1 + e^-z) with CUDA's fast exponential and fast division intrinsics (no IEEE division and
+// its special-case branch per element); e^-z = inf for very negative z gives 0, as it should.
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 }  // namespace mm
