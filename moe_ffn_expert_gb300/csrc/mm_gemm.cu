@@ -409,7 +409,9 @@ __device__ __forceinline__ void split8_bf16(const float* v, uint4& hi, uint4& lo
 // Coalesced copy-out through a per-warp 4 KB staging buffer. A lane first writes its own row
 // (32 values) into the buffer; after __syncwarp the warp reads it back row-major so that each
 // store instruction covers whole 128-byte lines of consecutive rows, instead of 32 rows at
-// 16 bytes each. 16-byte unit u of row r sits at unit u ^ (r & 7) (fp32, 128-byte rows) or
+// 16 bytes each. The stores are streaming (evict-first) unless asked otherwise: GEMM1's outputs
+// are next read by a later kernel, after far more data than L2 holds has passed through it, so
+// they need not displace the GEMMs' operand tiles there. 16-byte unit u of row r sits at unit u ^ (r & 7) (fp32, 128-byte rows) or
 // u ^ ((r >> 1) & 3) (bf16, 64-byte rows), so both the row writes and the line reads are free of
 // bank conflicts.
 __device__ __forceinline__ void stage_row_f32(uint8_t* stage, int lane, const float* v) {
@@ -429,7 +431,7 @@ __device__ __forceinline__ void copy_out_f32(const uint8_t* stage, int lane, flo
   for (int i = 0; i < 8; ++i) {
     const int r = 4 * i + (lane >> 3);
     const float4 v = *reinterpret_cast<const float4*>(stage + r * 128 + ((u ^ (r & 7)) << 4));
-    *reinterpret_cast<float4*>(base + (row0 + r) * ld + n + 4 * u) = v;
+    __stcs(reinterpret_cast<float4*>(base + (row0 + r) * ld + n + 4 * u), v);
   }
 }
 
@@ -441,14 +443,19 @@ __device__ __forceinline__ void stage_row_bf16(uint8_t* stage, int lane, const f
 }
 
 __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __nv_bfloat16* base,
-                                              int64_t row0, int64_t ld, int n, int N) {
+                                              int64_t row0, int64_t ld, int n, int N,
+                                              bool streaming = true) {
   const int u = lane & 3;
   if (n + 8 * u >= N) return;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 8 * i + (lane >> 2);
     const uint4 v = *reinterpret_cast<const uint4*>(stage + r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
-    *reinterpret_cast<uint4*>(base + (row0 + r) * ld + n + 8 * u) = v;
+    uint4* dst = reinterpret_cast<uint4*>(base + (row0 + r) * ld + n + 8 * u);
+    if (streaming)
+      __stcs(dst, v);
+    else
+      *dst = v;
   }
 }
 
@@ -457,10 +464,12 @@ __device__ __forceinline__ void copy_out_bf16(const uint8_t* stage, int lane, __
 // the fp32 gate, the fp32 up and w * silu(gate) * up (w: the row's routing weight) as a bf16 hi
 // plane and, for a backward, its bf16 lo residual, all through the staging buffer (hi in its
 // first 2 KB, lo in the second). The accumulator is released (`acce`) right after the last TMEM
-// read, before the last stores.
+// read, before the last stores. `fused`: the one-launch forward, whose GEMM2 tiles read the w*h
+// hi rows back within the same launch, so those are stored without the streaming hint.
 __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const EpiGeom& eg,
                                                       uint32_t tacc, int lane, uint8_t* stage,
-                                                      uint32_t acce, bool acce_remote = false) {
+                                                      uint32_t acce, bool acce_remote = false,
+                                                      bool fused = false) {
   const int64_t row0 = eg.row0;
   float* gu = reinterpret_cast<float*>(a.out0);
   const float w = __ldg(a.w_row + row0 + lane);
@@ -503,7 +512,8 @@ __device__ __forceinline__ void gemm1_epilogue_staged(const Args& a, const EpiGe
     }
     stage_row_bf16(stage, lane, h);
     __syncwarp();
-    copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I);
+    // the one-launch forward's GEMM2 tiles read the w*h rows back soon: normal stores there
+    copy_out_bf16(stage, lane, a.out1, row0, a.ld1, n, a.I, !fused);
     if (!a.skip_gu) copy_out_bf16(stage + 2048, lane, a.out3, row0, a.ld1, n, a.I);
     __syncwarp();
   }
@@ -1293,7 +1303,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           gemm1_epilogue_staged(a, epi_geom<true>(t, q, hf, TR::TN), tacc, lane,
                                 smem_raw + (sbuf - raw),
                                 (MMA2 && rank != 0) ? mapa_shared(acce_bar(buf), 0) : acce_bar(buf),
-                                MMA2 && rank != 0);
+                                MMA2 && rank != 0, true);
           // this warp's w*h (and gate|up) stores, ordered before the async proxy's later reads
           // by each lane, are released at GPU scope by one count from lane 0 (a full fence by
           // every lane instead cost this kernel ~3 %)
