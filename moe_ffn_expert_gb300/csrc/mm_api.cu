@@ -506,12 +506,20 @@ static mm_status backward_impl(mm_dims d, const mm_shared_expert* se, const void
   const int wgrad_pair = (pair == 2 && w.S >= 256 * w.E) ? 2 : 0;
   c.paired = pair == 2 ? 2 : 0;  // act_grad: pair MMAs or one CTA per tile
   MM_TRY(timed(ST_ACT_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
-  MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   c.kind = GK_W2_GRAD;
   c.d_w = d_down_proj_weight;
   c.accumulate = accumulate;
   c.paired = wgrad_pair;
+  // d_topk_weights: in W2Grad's launch (its epilogue warps, before their first tile), or, if
+  // that grid is too small for the slots, a kernel of its own after it
+  bool d_topk_taken = false;
+  c.d_topk = d_topk_weights;
+  c.d_topk_taken = &d_topk_taken;
   MM_TRY(timed(ST_W2_GRAD, st, [&] { return launch_gemm(w, ws, c, st); }));
+  c.d_topk = nullptr;
+  c.d_topk_taken = nullptr;
+  if (!d_topk_taken)
+    MM_TRY(timed(ST_D_TOPK, st, [&] { return launch_d_topk(w, ws, d_topk_weights, st); }));
   // split experts' W2Grad partial slices (in the o / dx row buffer) summed into the output
   // before input_grad writes its dx rows there
   if (wgrad_split_possible(w, WG_W2))

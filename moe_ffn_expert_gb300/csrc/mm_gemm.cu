@@ -144,6 +144,12 @@ struct Args {
   TraceCtx trace;            // optional per-tile trace (trace.buf == nullptr: off)
   const int4* wg_plan;       // weight gradients: the row chunks of this kind (see WgKind)
   int wg_kind;               // WG_W2 or WG_W1
+  // W2Grad: d_topk_weights computed by the epilogue warps before their first tile (see
+  // epilogue_d_topk); null when a separate kernel does it
+  float* d_topk;
+  const int32_t* row_of_slot_d;
+  int d_topk_S;
+  int d_topk_tiles;
 };
 
 template <int KIND>
@@ -701,7 +707,8 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
       }
     }
     if (failed) break;
-    // one partial per (column tile, half): the d_topk kernel sums them in a fixed order
+    // one partial per (column tile, half), summed in a fixed order by W2Grad's epilogue warps
+    // (epilogue_d_topk) or the d_topk kernel
     if (tile_ok) a.p_part[(int64_t)(2 * (t.n0 / BN) + hf) * a.S_pad + row] = p;
     tc_fence_before();
     __syncwarp();
@@ -716,6 +723,29 @@ __device__ __forceinline__ void act_grad_epilogue(const Args& a, const CUtensorM
   ep_close();
   if (lane == 0) bulk_wait_all();  // this warp's output stores are complete before it exits
   __syncwarp();
+}
+
+// d_topk_weights[s] = the sum, in column-tile order, of act_grad's <g, h> partials of slot s's
+// row (the separate d_topk kernel's arithmetic, bit for bit). Run by the epilogue warps of the
+// W2Grad launch, the first after act_grad, before they wait for their first accumulator: the
+// partials are complete (the launch waited for act_grad) and the wait is otherwise idle time.
+// `et` is the thread's index among the CTA's epilogue threads; slots are spread over the grid.
+__device__ __forceinline__ void epilogue_d_topk(const Args& a, int et) {
+  constexpr int ET = NUM_EPI_WARPS * 32;
+  const int nt = a.d_topk_tiles;
+  for (int s = (int)blockIdx.x * ET + et; s < a.d_topk_S; s += (int)gridDim.x * ET) {
+    const int64_t r = __ldg(a.row_of_slot_d + s);
+    float acc = 0.f;
+    for (int j0 = 0; j0 < nt; j0 += 8) {  // eight loads in flight, then the sum in tile order
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = j0 + u < nt ? a.p_part[(int64_t)(j0 + u) * a.S_pad + r] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (j0 + u < nt) acc += v[u];
+    }
+    a.d_topk[s] = acc;
+  }
 }
 
 // Output epilogue of one warp for the kinds with a TMA-stored output (GEMM2, INPUT_GRAD, the
@@ -1251,6 +1281,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else
         mbar_arrive(acce_bar(b));
     };
+    if constexpr (KIND == GK_W2_GRAD) {
+      if (a.d_topk != nullptr) epilogue_d_topk(a, (warp - 2) * 32 + lane);
+    }
     uint32_t acc_it = 0;
     // the first epilogue warp's span on each accumulator, closed when the warp moves on
     TraceSpan ep_sp{0u, 0ull};
@@ -1699,6 +1732,20 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
   } else {
     em.out = em.out_lo = ta;  // unused but initialised
   }
+  // W2Grad takes over d_topk_weights when its grid has the threads for it (at most 8 slots per
+  // epilogue thread, a few microseconds of loads before the first accumulator is due); otherwise
+  // the caller launches the d_topk kernel
+  auto take_d_topk = [&](int ctas) {
+    if (KIND != GK_W2_GRAD || c.d_topk == nullptr || c.d_topk_taken == nullptr) return;
+    if ((int64_t)ctas * NUM_EPI_WARPS * 32 * 8 < w.S) return;
+    a.d_topk = c.d_topk;
+    a.row_of_slot_d = reinterpret_cast<const int32_t*>(ws + w.off_row_of_slot);
+    a.p_part = reinterpret_cast<float*>(ws + w.off_p_part);
+    a.S_pad = S_pad;
+    a.d_topk_S = (int)w.S;
+    a.d_topk_tiles = (int)w.n_act_tiles;
+    *c.d_topk_taken = true;
+  };
   if constexpr (PAIRED) {
     // clusters of two CTAs over pairs of row tiles: as many clusters as fit at once (a
     // persistent grid must not wait for SMs), at most one per pair-column unit
@@ -1737,11 +1784,13 @@ cudaError_t run(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st
                               : (tiles_max / std::max(1, a.n_tiles_n) + 1) / 2 * a.n_tiles_n;
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_clusters, units));
     cfg.gridDim = dim3((unsigned)(2 * clusters));
+    take_d_topk(2 * clusters);
     cfg.numAttrs = 2;  // and programmatic stream serialization (the occupancy query had only the
                        // cluster shape)
     return cudaLaunchKernelEx(&cfg, k_gemm<KIND, PAIR>, ta, tb, tl, em, a);
   } else {
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(nsm, tiles_max));
+    take_d_topk(grid);
     return launch_pdl(k_gemm<KIND, 0>, grid, NUM_THREADS, Traits<KIND>::SMEM, st, ta, tb, tl, em,
                       a);
   }

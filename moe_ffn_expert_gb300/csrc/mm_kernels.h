@@ -44,7 +44,9 @@ cudaError_t launch_combine(const Workspace& w, char* ws, const void* rows, const
                            const void* extra_lo = nullptr, bool row_table = false);
 // Identity routing tables of the shared expert's sub-workspace (ws points at its base).
 cudaError_t launch_shared_tables(const Workspace& ws_shared, char* ws, cudaStream_t st);
-// d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]].
+// d_topk[s] = sum over column tiles (ascending) of p_part[tile][row_of_slot[s]]. Launched only
+// when the W2Grad launch, which normally computes these in its epilogue warps, has too few CTAs
+// for the slots.
 cudaError_t launch_d_topk(const Workspace& w, char* ws, float* d_topk, cudaStream_t st);
 // Records MM_ERR_INVALID_ARG in the status word if the forward kept no gate|up (forward only):
 // the check of a backward that launches no GEMM (T = 0).
@@ -87,6 +89,10 @@ struct GemmCall {
   const float* comb_w = nullptr;
   const void* comb_extra = nullptr;
   const void* comb_extra_lo = nullptr;
+  // W2Grad: d_topk_weights [T, K] may be computed by this launch's epilogue warps; if they take
+  // it, *d_topk_taken is set and no d_topk kernel is needed
+  float* d_topk = nullptr;
+  bool* d_topk_taken = nullptr;
 };
 
 cudaError_t launch_gemm(const Workspace& w, char* ws, const GemmCall& c, cudaStream_t st);
