@@ -91,9 +91,18 @@ typedef struct mm_dims {
 /* mm_forward flag: run GEMM1 + SwiGLU and GEMM2 in one persistent launch in which a row block's
  * GEMM2 tiles start as soon as all of its GEMM1 tiles have stored their h rows (per-row-block
  * ready counters in the workspace, bounded waits; the RFC's event-counter release of dependent
- * tiles, §5.1) instead of two stream-ordered launches. Results are identical bit for bit; on a
- * GB300 both take the same time, so the default is the two launches. */
+ * tiles, §5.1) instead of two stream-ordered launches. Results are identical bit for bit in both
+ * forms. Without this flag or MM_FLAG_SEPARATE_FORWARD_GEMMS, mm_forward picks the one launch by
+ * itself where it measured faster on a GB300: CTA-pair launches (no MM_FLAG_SINGLE_CTA_TILES,
+ * MM_FLAG_FUSED_COMBINE or MM_FLAG_TEST_STALL) whose two GEMMs come to 1 to 16 waves of work,
+ * estimated from the sizes as ceil(T*K / 256) x (ceil(I / 128) + ceil(H / 256)) units over half
+ * the SM count. There the one launch overlaps GEMM1's last partial wave with GEMM2's start; with
+ * more waves its releases cost more than that, with less than one GEMM2 cannot start early. */
 #define MM_FLAG_FUSED_FORWARD_GEMMS 0x8u
+
+/* mm_forward flag: always run GEMM1 + SwiGLU and GEMM2 as two stream-ordered launches (never the
+ * one launch above). Together with MM_FLAG_FUSED_FORWARD_GEMMS: MM_ERR_INVALID_ARG. */
+#define MM_FLAG_SEPARATE_FORWARD_GEMMS 0x40u
 
 /* mm_forward flag: fold the weighted combine into GEMM2's epilogue instead of running it as its
  * own kernel. Each epilogue warp, after its o rows are stored and visible, counts each row's token

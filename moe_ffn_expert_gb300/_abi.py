@@ -29,6 +29,7 @@ MM_FLAG_FP32_WEIGHT_GRADS = 0x4
 MM_FLAG_FUSED_FORWARD_GEMMS = 0x8
 MM_FLAG_FUSED_COMBINE = 0x10
 MM_FLAG_FORWARD_ONLY = 0x20
+MM_FLAG_SEPARATE_FORWARD_GEMMS = 0x40
 MM_FLAG_SINGLE_CTA_TILES = 0x100
 MM_NUM_STAGES = 17
 MM_TRACE_CTA = 0

@@ -304,6 +304,22 @@ static mm_status check_common(const mm_dims& d, const mm_shared_expert* se, cons
 // M = 256 MMA.
 static int pair_mode(uint32_t flags) { return (flags & MM_FLAG_SINGLE_CTA_TILES) ? 0 : 2; }
 
+// GEMM1 -> GEMM2 as one counter-released launch: when asked for, or, unless the caller asked for
+// two launches, where it measured faster (include/mm.h, MM_FLAG_FUSED_FORWARD_GEMMS): CTA-pair
+// launches of 1 to 16 waves, estimated as ceil(S / 256) row-tile pairs x (ceil(I / 128) GEMM1 +
+// ceil(H / 256) GEMM2 column tiles) over the SM pairs. Measured on a GB300 (H = 2048, I = 768,
+// 1024 rows per expert): forward 4-7 % faster at 8k and 16k slots (3 and 12 waves), 1-3 % slower
+// from 32k slots (24 waves) up; skew and tail workloads 4 and 3 % faster steps.
+static bool fused_forward(const Workspace& w, uint32_t flags) {
+  if (flags & MM_FLAG_FUSED_FORWARD_GEMMS) return true;
+  if (flags & (MM_FLAG_SEPARATE_FORWARD_GEMMS | MM_FLAG_SINGLE_CTA_TILES | MM_FLAG_FUSED_COMBINE |
+               MM_FLAG_TEST_STALL))
+    return false;
+  const int64_t pairs = std::max(1, device_sm_count() / 2);
+  const int64_t units = (w.S + 255) / 256 * ((w.I + 127) / 128 + (w.H + 255) / 256);
+  return units >= pairs && units <= 16 * pairs;
+}
+
 // An empty batch (T = 0): no slot to route or compute. The header and the routing tables are
 // written as empty (zero counts and offsets), and a caller's tokens_per_expert is still compared
 // with them by the scan kernel, which reads no chunk histogram when there is none.
@@ -378,6 +394,8 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
   mm_status s = check_common(d, se, workspace, workspace_bytes, &p);
   if (s != MM_OK) return s;
   const Workspace& w = p.w;
+  if ((flags & MM_FLAG_FUSED_FORWARD_GEMMS) && (flags & MM_FLAG_SEPARATE_FORWARD_GEMMS))
+    return MM_ERR_INVALID_ARG;
   if (d.T == 0) return forward_empty(p, se, tpe, up_proj_weight, down_proj_weight, workspace,
                                      stream, flags);
   if (!x || !topk_ids || !topk_weights || !up_proj_weight || !down_proj_weight || !y)
@@ -441,7 +459,7 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
     c.comb_extra = extra;
     c.comb_extra_lo = extra_lo;
   }
-  if (flags & MM_FLAG_FUSED_FORWARD_GEMMS) {
+  if (fused_forward(w, flags)) {
     // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored
     MM_TRY(cudaMemsetAsync(ws + w.off_ready, 0, (size_t)(w.S_pad / BM) * sizeof(int32_t), st));
     c.kind = GK_FWD_FUSED;

@@ -49,6 +49,8 @@ def test_host_validation_without_device():
     assert _abi.mm_forward(d, 0, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_forward(d, 24, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_forward(_abi.dims(16, 60, 32, 4, 2), 16, 16, 16, 16, 16, 16, 256, n, 0, 0) == _abi.MM_ERR_UNSUPPORTED
+    both = _abi.MM_FLAG_FUSED_FORWARD_GEMMS | _abi.MM_FLAG_SEPARATE_FORWARD_GEMMS  # contradictory
+    assert _abi.mm_forward(d, 16, 16, 16, 16, 16, 16, 256, n, 0, both) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_backward(d, 0, 16, 16, 16, 16, 16, 256, n, 16, 16, 16, 16, 0, 0) == _abi.MM_ERR_INVALID_ARG
     assert _abi.mm_get_status(0, 0) == _abi.MM_ERR_WORKSPACE
     assert _abi.mm_status_string(_abi.MM_ERR_BAD_EXPERT_ID) == "expert id out of range"

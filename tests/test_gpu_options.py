@@ -121,10 +121,38 @@ def test_fused_forward_gemms_equal_two_launches(T, H, I, E, K):
     w = synth.small("fused", T, H, I, E, K, seed=T)
     inp = make_inputs(w)
     a = run_layer(inp, flags=_abi.MM_FLAG_FUSED_FORWARD_GEMMS)
-    b = run_layer(inp)
+    b = run_layer(inp, flags=_abi.MM_FLAG_SEPARATE_FORWARD_GEMMS)
     assert a["status"] == _abi.MM_OK and b["status"] == _abi.MM_OK
     for k in ("y", "dx", "d_topk_weights", "dW_up", "dW_down"):
         assert torch.equal(a[k], b[k]), k
+
+
+def test_forward_picks_one_launch_by_size():
+    """Without a forward-form flag the forward runs GEMM1 -> GEMM2 as one counter-released launch
+    for mid-sized layers (here 8192 slots: ~6 waves of work units on a GB300) and as two launches
+    for a tiny one (under one wave) and when asked for two; every form gives the same bits."""
+    from moe_ffn_expert_gb300 import trace
+    names = trace.stage_names()
+
+    def fwd_stages(inp, flags):
+        tb = trace.TraceBuffer(1 << 16)
+        tb.start()
+        out = run_layer(inp, flags=flags, backward=False)
+        recs = tb.stop()
+        assert out["status"] == _abi.MM_OK
+        return out, {names[int(st)] for st in set(recs["stage"].tolist())}
+
+    mid = make_inputs(synth.small("auto_fwd", 1024, 2048, 768, 8, 8, seed=51))
+    a, st_a = fwd_stages(mid, 0)
+    b, st_b = fwd_stages(mid, _abi.MM_FLAG_SEPARATE_FORWARD_GEMMS)
+    assert "gemm1_gemm2" in st_a and "gemm1_swiglu" not in st_a
+    assert "gemm1_gemm2" not in st_b and {"gemm1_swiglu", "gemm2"} <= st_b
+    assert torch.equal(a["y"], b["y"])
+    tiny = make_inputs(synth.small("auto_fwd_tiny", 300, 256, 128, 4, 2, seed=52))
+    _, st_t = fwd_stages(tiny, 0)
+    assert "gemm1_gemm2" not in st_t
+    one_cta, st_s = fwd_stages(mid, _abi.MM_FLAG_SINGLE_CTA_TILES)  # one CTA per tile: two launches
+    assert "gemm1_gemm2" not in st_s and torch.equal(one_cta["y"], a["y"])
 
 
 def test_fused_forward_bounded_waits_end_the_call():

@@ -42,10 +42,10 @@ def expected_units(counts, T, H, I, E, K, single):
             "w2_grad": busy * w2_rows * cdiv(H, 256), "w1_grad": busy * w1_rows * cdiv(H, 256)}, wpair
 
 
-def traced_step(inp, capacity=1 << 16, flags=0):
+def traced_step(inp, capacity=1 << 16, flags=0, bwd_flags=None):
     tb = trace.TraceBuffer(capacity)
     tb.start()
-    out = run_layer(inp, flags=flags, bwd_flags=flags)
+    out = run_layer(inp, flags=flags, bwd_flags=flags if bwd_flags is None else bwd_flags)
     recs = tb.stop()
     return out, recs, tb
 
@@ -55,8 +55,9 @@ def test_trace_describes_the_schedule(single):
     T, H, I, E, K = 2048, 256, 256, 8, 2
     inp = make_inputs(synth.small("trace", T, H, I, E, K, seed=91))
     flags = _abi.MM_FLAG_SINGLE_CTA_TILES if single else 0
-    ref = run_layer(inp, flags=flags, bwd_flags=flags)
-    out, recs, tb = traced_step(inp, flags=flags)
+    fwd = flags | _abi.MM_FLAG_SEPARATE_FORWARD_GEMMS  # GEMM1 and GEMM2 as two launches
+    ref = run_layer(inp, flags=fwd, bwd_flags=flags)
+    out, recs, tb = traced_step(inp, flags=fwd, bwd_flags=flags)
     assert out["status"] == _abi.MM_OK and tb.dropped == 0 and recs.size == tb.offered
     for k in KEYS:  # tracing changes nothing the layer computes
         assert torch.equal(out[k], ref[k]), k
