@@ -460,8 +460,8 @@ static mm_status forward_impl(mm_dims d, const mm_shared_expert* se, const int32
     c.comb_extra_lo = extra_lo;
   }
   if (fused_forward(w, flags)) {
-    // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored
-    MM_TRY(cudaMemsetAsync(ws + w.off_ready, 0, (size_t)(w.S_pad / BM) * sizeof(int32_t), st));
+    // one launch: GEMM2 row blocks start as soon as their GEMM1 tiles are stored (the routing
+    // scan zeroed the ready counters of the row tiles in use)
     c.kind = GK_FWD_FUSED;
     MM_TRY(timed(ST_FWD_GEMMS, st, [&] { return launch_gemm(w, ws, c, st); }));
     c.inject_stall = 0;

@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
                                                      int32_t* __restrict__ slot_of_row,
                                                      float* __restrict__ w_row,
                                                      int32_t* __restrict__ pair_tile,
+                                                     int32_t* __restrict__ ready,
                                                      const int32_t* __restrict__ tpe, int E,
                                                      int n_chunks, WgPlanArgs wg, TraceCtx tc) {
   pdl_wait();
@@ -335,12 +336,17 @@ __global__ void __launch_bounds__(1024) k_route_scan(int* hdr, int32_t* __restri
       run += v;
     }
   }
-  // each expert's row tiles, row-tile pairs and pad-row markers: one warp per expert at a time,
-  // its lanes over consecutive entries, so that every store instruction is coalesced
+  // each expert's row tiles (and their ready counters for the one-launch forward, zeroed here so
+  // that no memset has to run between the launches), row-tile pairs and pad-row markers: one warp
+  // per expert at a time, its lanes over consecutive entries, so that every store instruction is
+  // coalesced
   for (int ex = warp; ex < E; ex += (int)(blockDim.x >> 5)) {
     const int tot = tot_s[ex], po = po_s[ex], qo = qo_s[ex];
     const int pcount = (tot + BM - 1) / BM * BM, ntile = pcount / BM;
-    for (int t = lane; t < ntile; t += 32) tile_expert[po / BM + t] = ex;
+    for (int t = lane; t < ntile; t += 32) {
+      tile_expert[po / BM + t] = ex;
+      ready[po / BM + t] = 0;
+    }
     for (int i = lane; i < (ntile + 1) / 2; i += 32) {
       const int t0 = po / BM + 2 * i;
       pair_tile[qo + i] = 2 * i + 1 < ntile ? t0 : ~t0;
@@ -700,7 +706,8 @@ cudaError_t launch_route_scan(const Workspace& w, char* ws, const int32_t* token
                     region<int32_t>(ws, w.off_offsets), region<int32_t>(ws, w.off_poff),
                     region<int32_t>(ws, w.off_tile_expert), region<int32_t>(ws, w.off_slot_of_row),
                     region<float>(ws, w.off_w_row), region<int32_t>(ws, w.off_pair_tile),
-                    tokens_per_expert, (int)w.E, (int)w.n_chunks, wg, trace_ctx());
+                    region<int32_t>(ws, w.off_ready), tokens_per_expert, (int)w.E,
+                    (int)w.n_chunks, wg, trace_ctx());
 }
 
 cudaError_t launch_route_rank(const Workspace& w, char* ws, const int32_t* ids, const float* topk_w,
