@@ -417,9 +417,9 @@ __device__ __forceinline__ void split8_bf16(const float* v, uint4& hi, uint4& lo
 // store instruction covers whole 128-byte lines of consecutive rows, instead of 32 rows at
 // 16 bytes each. The stores are streaming (evict-first) unless asked otherwise: GEMM1's outputs
 // are next read by a later kernel, after far more data than L2 holds has passed through it, so
-// they need not displace the GEMMs' operand tiles there. 16-byte unit u of row r sits at unit u ^ (r & 7) (fp32, 128-byte rows) or
-// u ^ ((r >> 1) & 3) (bf16, 64-byte rows), so both the row writes and the line reads are free of
-// bank conflicts.
+// they need not displace the GEMMs' operand tiles there. 16-byte unit u of row r sits at unit
+// u ^ (r & 7) (fp32, 128-byte rows) or u ^ ((r >> 1) & 3) (bf16, 64-byte rows), so both the row
+// writes and the line reads are free of bank conflicts.
 __device__ __forceinline__ void stage_row_f32(uint8_t* stage, int lane, const float* v) {
   uint8_t* rowp = stage + lane * 128;
 #pragma unroll
@@ -739,7 +739,8 @@ __device__ __forceinline__ void epilogue_d_topk(const Args& a, int et) {
     for (int j0 = 0; j0 < nt; j0 += 8) {  // eight loads in flight, then the sum in tile order
       float v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = j0 + u < nt ? a.p_part[(int64_t)(j0 + u) * a.S_pad + r] : 0.f;
+      for (int u = 0; u < 8; ++u)
+        v[u] = j0 + u < nt ? a.p_part[(int64_t)(j0 + u) * a.S_pad + r] : 0.f;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         if (j0 + u < nt) acc += v[u];
