@@ -5,7 +5,8 @@ zeroed outputs), whose bf16 rounding must equal the default bf16 gradients; ever
 also runs with a shared expert of random size, default against one-CTA launches. Different schedules
 of the same arithmetic must give the same bits, so a race or an unwritten read in any of them
 shows up as a difference. The oracle bounds are checked on fewer shapes in
-test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the count (default 300, a few seconds)."""
+test_gpu_random_shapes.py. MM_SOAK_SHAPES sets the count (default 300, a few seconds) and
+MM_SOAK_SEED the shape sequence (default 777)."""
 import os
 import random
 
@@ -23,8 +24,9 @@ KEYS = ("y", "dx", "d_topk_weights", "dW_up", "dW_down")
 
 def test_soak_schedules_agree_bit_for_bit():
     n = int(os.environ.get("MM_SOAK_SHAPES", "300"))
-    rng = random.Random(777)
-    rng_forms = random.Random(778)  # a stream of its own: the shapes stay those of seed 777
+    seed = int(os.environ.get("MM_SOAK_SEED", "777"))
+    rng = random.Random(seed)
+    rng_forms = random.Random(seed + 1)  # a stream of its own: the shapes stay those of `seed`
     f32, acc = _abi.MM_FLAG_FP32_WEIGHT_GRADS, _abi.MM_FLAG_ACCUMULATE_WEIGHT_GRADS
     single = _abi.MM_FLAG_SINGLE_CTA_TILES
     fused = (_abi.MM_FLAG_FUSED_COMBINE, _abi.MM_FLAG_FUSED_FORWARD_GEMMS,
@@ -39,7 +41,8 @@ def test_soak_schedules_agree_bit_for_bit():
         kind = rng.choice(["uniform", "zipf"])
         ff = rng.choice(fused)
         shape = (T, H, I, E, K, kind)
-        inp = make_inputs(synth.small("soak", T, H, I, E, K, routing_kind=kind, seed=5000 + i))
+        inp = make_inputs(synth.small("soak", T, H, I, E, K, routing_kind=kind,
+                                      seed=5000 + i + 100003 * (seed - 777)))
         a = run_layer(inp)
         runs = {"again": run_layer(inp),
                 "single": run_layer(inp, flags=single, bwd_flags=single)}
@@ -61,7 +64,8 @@ def test_soak_schedules_agree_bit_for_bit():
                 diffs.append(f"weight-gradient form 0x{wf:x}: {k}")
         if i % 4 == 3:  # a shared expert: its own sub-workspace, tables and seven launches
             I_s = 8 * rng_forms.randint(1, 64)
-            w = synth.small("soak", T, H, I, E, K, routing_kind=kind, seed=5000 + i)
+            w = synth.small("soak", T, H, I, E, K, routing_kind=kind,
+                            seed=5000 + i + 100003 * (seed - 777))
             sh = (synth.shared_up(w, I_s, device="cuda"), synth.shared_down(w, I_s, device="cuda"))
             sa = run_layer(inp, shared=sh)
             sb = run_layer(inp, shared=sh, flags=single, bwd_flags=single)
